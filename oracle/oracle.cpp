@@ -1,0 +1,643 @@
+// Oracle: a plain, slow, single-threaded CPU statement of what the resharding
+// library computes. It is test infrastructure. Only the tests, the smoke check
+// and the benchmark's CPU-baseline leg load it. It shares no code, header or
+// table with the CUDA library and must stay that way.
+//
+// What each function follows (page title, section):
+//   * shard geometry: "ONNX multi-device proposal ... ShardingSpec" (zskr.cn),
+//     sections "Sharding as a Split" and "index rule for multi-axis splits"
+//     (the nested loop: axis a outer, axis b inner, shards appended in that
+//     order); "Sharding as a Broadcast" and "mixing split and broadcast"
+//     (device_map groups); OneFlow SBP page (szpsdzdm.com), 2D SBP
+//     (broadcast, split(0)) on ranks [[0,1],[2,3]]: mesh dim 0 is the outer
+//     level, mesh dim 1 the inner one.
+//   * partial sum: OneFlow SBP page, definition of partial: the logical tensor
+//     is the element-wise sum of the per-device tensors.
+//   * infer_spmd: Paddle "SPMD rules" page (contextqmd.com), steps 1-3 of the
+//     einsum-based rule (einsum, ShardingMergeForTensors,
+//     GetDimsMappingForAxes); reductions over a sharded axis leave a partial
+//     result: ONNX page, section on reduction operators.
+//   * reshape rule: Paddle page, DimTrans table (InputDim, Flatten, Split,
+//     Singleton) and its sharding rule.
+//   * TP-MLP: ColossalAI 1D tensor parallelism page (mhpq.cn) section 2 and
+//     2.1: Y_i = X A_i, Z = sum_i Y_i B_i; GELU between the GEMMs from the
+//     Domino page (mzlw.cn), forward section ("GeMM GeLU GeMM").
+//
+// Readings where the pages are silent (each is listed in the design notes):
+//   * uneven extents: ceil-sized leading shards, applied level by level;
+//   * shard() of a partial layout: the device whose partial coordinates are
+//     all zero holds the tensor, the others hold zeros;
+//   * GELU is the exact erf form; Y is rounded to bf16 before the second GEMM.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <string>
+#include <vector>
+
+namespace {
+
+constexpr int kMaxMesh = 8;
+constexpr int kMaxDev = 256;
+constexpr int kMaxDim = 8;
+
+}  // namespace
+
+extern "C" {
+
+// A layout in the ND-SBP form: a row-major mesh of device ids and one entry per
+// mesh dim: 'S' (split tensor axis `axis`), 'B' (broadcast) or 'P' (partial sum).
+struct OracleLayout {
+    int32_t mesh_ndim;
+    int64_t mesh_shape[kMaxMesh];
+    int32_t devices[kMaxDev];
+    int8_t kind[kMaxMesh];
+    int32_t axis[kMaxMesh];
+};
+
+}  // extern "C"
+
+namespace {
+
+int64_t num_devices(const OracleLayout& L)
+{
+    int64_t n = 1;
+    for (int d = 0; d < L.mesh_ndim; ++d) n *= L.mesh_shape[d];
+    return n;
+}
+
+// Mesh coordinates of device `dev`, or false if it is not on the mesh.
+bool coords_of(const OracleLayout& L, int dev, int64_t* c)
+{
+    int64_t n = num_devices(L);
+    for (int64_t p = 0; p < n; ++p) {
+        if (L.devices[p] != dev) continue;
+        int64_t rem = p;
+        for (int d = L.mesh_ndim - 1; d >= 0; --d) {
+            c[d] = rem % L.mesh_shape[d];
+            rem /= L.mesh_shape[d];
+        }
+        return true;
+    }
+    return false;
+}
+
+// The slice [lo, hi) of every tensor axis held by a device at mesh coords c.
+// For each axis, the mesh dims that split it are visited outer first; each
+// level cuts the current interval into num_shards pieces of width
+// ceil(len / num_shards) (the last piece is short, possibly empty).
+void slice_of(const OracleLayout& L, int ndim, const int64_t* shape, const int64_t* c, int64_t* lo,
+              int64_t* hi)
+{
+    for (int a = 0; a < ndim; ++a) {
+        lo[a] = 0;
+        hi[a] = shape[a];
+    }
+    for (int d = 0; d < L.mesh_ndim; ++d) {
+        if (L.kind[d] != 'S') continue;
+        int a = L.axis[d];
+        int64_t len = hi[a] - lo[a];
+        int64_t n = L.mesh_shape[d];
+        int64_t width = (len + n - 1) / n;
+        int64_t b = std::min(c[d] * width, len);
+        int64_t e = std::min((c[d] + 1) * width, len);
+        hi[a] = lo[a] + e;
+        lo[a] = lo[a] + b;
+    }
+}
+
+bool holds_partial_value(const OracleLayout& L, const int64_t* c)
+{
+    for (int d = 0; d < L.mesh_ndim; ++d)
+        if (L.kind[d] == 'P' && c[d] != 0) return false;
+    return true;
+}
+
+bool is_b_representative(const OracleLayout& L, const int64_t* c)
+{
+    for (int d = 0; d < L.mesh_ndim; ++d)
+        if (L.kind[d] == 'B' && c[d] != 0) return false;
+    return true;
+}
+
+int check_layout(const OracleLayout& L, int ndim)
+{
+    if (L.mesh_ndim < 1 || L.mesh_ndim > kMaxMesh || ndim < 0 || ndim > kMaxDim) return -1;
+    int64_t n = num_devices(L);
+    if (n < 1 || n > kMaxDev) return -1;
+    std::vector<int> seen(n, 0);
+    for (int64_t p = 0; p < n; ++p) {
+        int v = L.devices[p];
+        if (v < 0 || v >= n || seen[v]) return -1;
+        seen[v] = 1;
+    }
+    for (int d = 0; d < L.mesh_ndim; ++d) {
+        if (L.kind[d] != 'S' && L.kind[d] != 'B' && L.kind[d] != 'P') return -1;
+        if (L.kind[d] == 'S' && (L.axis[d] < 0 || L.axis[d] >= ndim)) return -1;
+    }
+    return 0;
+}
+
+// ---- scalar conversions -------------------------------------------------
+
+double bf16_bits_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    std::memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+// Round a double to the nearest bfloat16 (8 significant bits, float's exponent
+// range, subnormals down to 2^-133), ties to even.
+uint16_t double_to_bf16_bits(double x)
+{
+    if (std::isnan(x)) return 0x7FC0;
+    float f;
+    if (x == 0.0 || std::isinf(x)) {
+        f = (float)x;
+    } else {
+        int ex;
+        std::frexp(x, &ex);  // |x| in [2^(ex-1), 2^ex)
+        int qexp = std::max(ex - 8, -133);
+        double q = std::ldexp(1.0, qexp);
+        double r = std::nearbyint(x / q) * q;  // default rounding mode: ties to even
+        if (std::fabs(r) >= std::ldexp(1.0, 128)) r = std::copysign(INFINITY, x);
+        f = (float)r;  // exact: r has at most 8 significant bits
+    }
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    return (uint16_t)(u >> 16);
+}
+
+double load(int dtype, const void* p, int64_t i)
+{
+    if (dtype == 0) return (double)((const float*)p)[i];
+    return bf16_bits_to_double(((const uint16_t*)p)[i]);
+}
+
+void store(int dtype, void* p, int64_t i, double v)
+{
+    if (dtype == 0) ((float*)p)[i] = (float)v;
+    else ((uint16_t*)p)[i] = double_to_bf16_bits(v);
+}
+
+// Row-major successor of index idx within extents ext; false when done.
+bool next_index(int ndim, const int64_t* ext, int64_t* idx)
+{
+    for (int a = ndim - 1; a >= 0; --a) {
+        if (++idx[a] < ext[a]) return true;
+        idx[a] = 0;
+    }
+    return false;
+}
+
+int64_t linear(int ndim, const int64_t* ext, const int64_t* idx)
+{
+    int64_t off = 0;
+    for (int a = 0; a < ndim; ++a) off = off * ext[a] + idx[a];
+    return off;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Shape of the piece held by `device`; returns 0, or -1 on a malformed layout.
+int oracle_shard_box(int ndim, const int64_t* shape, const OracleLayout* L, int device, int64_t* lo, int64_t* hi,
+                     int32_t* holds_value)
+{
+    if (check_layout(*L, ndim)) return -1;
+    int64_t c[kMaxMesh];
+    if (!coords_of(*L, device, c)) return -1;
+    slice_of(*L, ndim, shape, c, lo, hi);
+    *holds_value = holds_partial_value(*L, c) ? 1 : 0;
+    return 0;
+}
+
+// shard: the per-device pieces of the logical tensor `full`.
+// out[dev] receives the row-major piece of device dev.
+int oracle_shard(int dtype, int ndim, const int64_t* shape, const void* full, const OracleLayout* L, void* const* out)
+{
+    if (check_layout(*L, ndim)) return -1;
+    int64_t n = num_devices(*L);
+    for (int dev = 0; dev < n; ++dev) {
+        int64_t c[kMaxMesh], lo[kMaxDim], hi[kMaxDim], ext[kMaxDim], e[kMaxDim], g[kMaxDim];
+        coords_of(*L, dev, c);
+        slice_of(*L, ndim, shape, c, lo, hi);
+        bool value = holds_partial_value(*L, c);
+        int64_t count = 1;
+        for (int a = 0; a < ndim; ++a) {
+            ext[a] = hi[a] - lo[a];
+            count *= ext[a];
+            e[a] = 0;
+        }
+        if (count == 0) continue;
+        int64_t k = 0;
+        do {
+            for (int a = 0; a < ndim; ++a) g[a] = lo[a] + e[a];
+            double v = value ? load(dtype, full, linear(ndim, shape, g)) : 0.0;
+            store(dtype, out[dev], k++, v);
+        } while (next_index(ndim, ext, e));
+    }
+    return 0;
+}
+
+// The logical tensor (in double) described by per-device pieces `in` laid out
+// by L: pieces of B replicas other than coordinate 0 are skipped, partial
+// pieces are added.
+int oracle_gather(int dtype, int ndim, const int64_t* shape, const void* const* in, const OracleLayout* L,
+                  double* logical)
+{
+    if (check_layout(*L, ndim)) return -1;
+    int64_t total = 1;
+    for (int a = 0; a < ndim; ++a) total *= shape[a];
+    for (int64_t i = 0; i < total; ++i) logical[i] = 0.0;
+    int64_t n = num_devices(*L);
+    for (int dev = 0; dev < n; ++dev) {
+        int64_t c[kMaxMesh], lo[kMaxDim], hi[kMaxDim], ext[kMaxDim], e[kMaxDim], g[kMaxDim];
+        coords_of(*L, dev, c);
+        if (!is_b_representative(*L, c)) continue;
+        slice_of(*L, ndim, shape, c, lo, hi);
+        int64_t count = 1;
+        for (int a = 0; a < ndim; ++a) {
+            ext[a] = hi[a] - lo[a];
+            count *= ext[a];
+            e[a] = 0;
+        }
+        if (count == 0) continue;
+        int64_t k = 0;
+        do {
+            for (int a = 0; a < ndim; ++a) g[a] = lo[a] + e[a];
+            logical[linear(ndim, shape, g)] += load(dtype, in[dev], k++);
+        } while (next_index(ndim, ext, e));
+    }
+    return 0;
+}
+
+// reshard: gather the logical tensor from the source pieces (summing partial
+// pieces in double), then cut it by the destination layout, rounding once to
+// the element type.
+int oracle_reshard(int dtype, int ndim, const int64_t* shape, const void* const* src, const OracleLayout* Ls,
+                   void* const* dst, const OracleLayout* Ld)
+{
+    if (check_layout(*Ls, ndim) || check_layout(*Ld, ndim)) return -1;
+    int64_t total = 1;
+    for (int a = 0; a < ndim; ++a) total *= shape[a];
+    std::vector<double> logical((size_t)std::max<int64_t>(total, 1));
+    oracle_gather(dtype, ndim, shape, src, Ls, logical.data());
+    int64_t n = num_devices(*Ld);
+    for (int dev = 0; dev < n; ++dev) {
+        int64_t c[kMaxMesh], lo[kMaxDim], hi[kMaxDim], ext[kMaxDim], e[kMaxDim], g[kMaxDim];
+        coords_of(*Ld, dev, c);
+        slice_of(*Ld, ndim, shape, c, lo, hi);
+        bool value = holds_partial_value(*Ld, c);
+        int64_t count = 1;
+        for (int a = 0; a < ndim; ++a) {
+            ext[a] = hi[a] - lo[a];
+            count *= ext[a];
+            e[a] = 0;
+        }
+        if (count == 0) continue;
+        int64_t k = 0;
+        do {
+            for (int a = 0; a < ndim; ++a) g[a] = lo[a] + e[a];
+            store(dtype, dst[dev], k++, value ? logical[linear(ndim, shape, g)] : 0.0);
+        } while (next_index(ndim, ext, e));
+    }
+    return 0;
+}
+
+// ---- front-ends -----------------------------------------------------------
+
+// Paddle dims_mapping: dims_mapping[i] = j splits tensor dim i along mesh dim j,
+// -1 leaves it whole. Mesh dims named by no tensor dim are broadcast, or
+// partial when their bit is set in partial_mask.
+int oracle_layout_from_dims_mapping(int ndim, const int32_t* dims_mapping, int mesh_ndim, const int64_t* mesh_shape,
+                                    const int32_t* devices, uint32_t partial_mask, OracleLayout* out)
+{
+    if (mesh_ndim < 1 || mesh_ndim > kMaxMesh || ndim < 0 || ndim > kMaxDim) return -1;
+    OracleLayout L;
+    std::memset(&L, 0, sizeof L);
+    L.mesh_ndim = mesh_ndim;
+    int64_t n = 1;
+    for (int d = 0; d < mesh_ndim; ++d) {
+        L.mesh_shape[d] = mesh_shape[d];
+        L.kind[d] = (partial_mask >> d) & 1u ? 'P' : 'B';
+        L.axis[d] = -1;
+        n *= mesh_shape[d];
+    }
+    if (n < 1 || n > kMaxDev) return -1;
+    for (int64_t p = 0; p < n; ++p) L.devices[p] = devices ? devices[p] : (int32_t)p;
+    for (int i = 0; i < ndim; ++i) {
+        int j = dims_mapping[i];
+        if (j == -1) continue;
+        if (j < 0 || j >= mesh_ndim) return -1;
+        if ((partial_mask >> j) & 1u) return -1;  // a mesh dim cannot both split and hold partials
+        if (L.kind[j] == 'S') return -1;         // two tensor dims on one mesh dim
+        L.kind[j] = 'S';
+        L.axis[j] = i;
+    }
+    if (check_layout(L, ndim)) return -1;
+    *out = L;
+    return 0;
+}
+
+// ONNX ShardingSpecProto: `device` lists device ids, or negative keys into
+// device_map (index_to_device_group_map). The sharded_dim entries split their
+// axes in the listed order (first = outer); split piece s goes to device[s],
+// or to every device of group device_map[device[s]]. The product of the
+// num_shards must equal the length of `device`; all groups must be the same
+// size. The result is a mesh [num_shards..., group size] whose last dim, when
+// the groups have more than one device, is broadcast.
+int oracle_layout_from_onnx(int ndim, int n_device, const int64_t* device, int n_groups, const int64_t* group_keys,
+                            const int32_t* group_sizes, const int64_t* group_devices, int n_sharded,
+                            const int64_t* axes, const int64_t* num_shards, OracleLayout* out)
+{
+    if (n_device < 1 || n_sharded < 0 || n_sharded + 1 > kMaxMesh) return -1;
+    // Expand each device entry into its list of devices.
+    std::vector<std::vector<int64_t>> members;
+    for (int s = 0; s < n_device; ++s) {
+        std::vector<int64_t> m;
+        if (device[s] >= 0) {
+            m.push_back(device[s]);
+        } else {
+            int64_t off = 0;
+            bool found = false;
+            for (int g = 0; g < n_groups; ++g) {
+                if (group_keys[g] == device[s]) {
+                    for (int t = 0; t < group_sizes[g]; ++t) m.push_back(group_devices[off + t]);
+                    found = true;
+                    break;
+                }
+                off += group_sizes[g];
+            }
+            if (!found || m.empty()) return -1;
+        }
+        if (!members.empty() && m.size() != members[0].size()) return -1;
+        members.push_back(m);
+    }
+    int64_t splits = 1;
+    for (int k = 0; k < n_sharded; ++k) {
+        if (num_shards[k] < 1) return -1;
+        splits *= num_shards[k];
+    }
+    if (splits != n_device) return -1;
+    OracleLayout L;
+    std::memset(&L, 0, sizeof L);
+    int md = 0;
+    for (int k = 0; k < n_sharded; ++k) {
+        int64_t a = axes[k];
+        if (a < -ndim || a >= ndim) return -1;
+        if (a < 0) a += ndim;
+        L.mesh_shape[md] = num_shards[k];
+        L.kind[md] = 'S';
+        L.axis[md] = (int32_t)a;
+        ++md;
+    }
+    int64_t gsize = (int64_t)members[0].size();
+    if (gsize > 1 || md == 0) {
+        L.mesh_shape[md] = gsize;
+        L.kind[md] = 'B';
+        L.axis[md] = -1;
+        ++md;
+    }
+    L.mesh_ndim = md;
+    int64_t n = splits * gsize;
+    if (n > kMaxDev) return -1;
+    for (int s = 0; s < n_device; ++s)
+        for (int64_t t = 0; t < gsize; ++t) L.devices[s * gsize + t] = (int32_t)members[s][t];
+    if (check_layout(L, ndim)) return -1;
+    *out = L;
+    return 0;
+}
+
+// ---- infer_spmd (einsum rule) ---------------------------------------------
+
+// Step 1: the einsum ("mk,kn->mn") names every axis of every input and of the
+// output by a letter. Step 2 (merge): each letter takes the first mesh dim that
+// some input gives it; an input that gives it another mesh dim conflicts and
+// must be resharded. A mesh dim may shard one letter only: the letter that
+// comes first in the einsum keeps it. Step 3: the output dims_mapping lists
+// the merged mesh dims of the output letters; a letter that is summed away
+// (present in the inputs, absent from the output) and sharded leaves the
+// output partial over that mesh dim.
+//   merged_in[j][i]: dims_mapping that input j must be resharded to.
+// Returns 0, or -1 on a malformed einsum / mapping.
+int oracle_infer_spmd(const char* einsum, int n_in, const int32_t* const* in_dims_mapping, int mesh_ndim,
+                      int32_t* out_dims_mapping, uint32_t* out_partial_mask, uint32_t* in_needs_reshard_mask,
+                      int32_t* const* merged_in)
+{
+    std::string s(einsum ? einsum : "");
+    size_t arrow = s.find("->");
+    if (arrow == std::string::npos || n_in < 1 || n_in > 8 || mesh_ndim < 1 || mesh_ndim > kMaxMesh) return -1;
+    std::vector<std::string> ins;
+    {
+        std::string lhs = s.substr(0, arrow), cur;
+        for (char ch : lhs) {
+            if (ch == ',') {
+                ins.push_back(cur);
+                cur.clear();
+            } else {
+                cur.push_back(ch);
+            }
+        }
+        ins.push_back(cur);
+    }
+    std::string outs = s.substr(arrow + 2);
+    if ((int)ins.size() != n_in) return -1;
+    for (auto& t : ins)
+        for (size_t i = 0; i < t.size(); ++i) {
+            if (t[i] < 'a' || t[i] > 'z' || t.find(t[i]) != i) return -1;
+        }
+    for (size_t i = 0; i < outs.size(); ++i) {
+        char ch = outs[i];
+        if (ch < 'a' || ch > 'z' || outs.find(ch) != i) return -1;
+        bool present = false;
+        for (auto& t : ins) present = present || t.find(ch) != std::string::npos;
+        if (!present) return -1;
+    }
+    for (int j = 0; j < n_in; ++j)
+        for (size_t i = 0; i < ins[j].size(); ++i) {
+            int v = in_dims_mapping[j][i];
+            if (v < -1 || v >= mesh_ndim) return -1;
+            for (size_t k = 0; k < i; ++k)
+                if (v != -1 && in_dims_mapping[j][k] == v) return -1;
+        }
+    // letters in order of first appearance in the einsum string
+    std::string order;
+    for (char ch : s)
+        if (ch >= 'a' && ch <= 'z' && order.find(ch) == std::string::npos) order.push_back(ch);
+    int letter_dim[26];
+    for (int i = 0; i < 26; ++i) letter_dim[i] = -1;
+    for (char ch : order)
+        for (int j = 0; j < n_in; ++j) {
+            size_t pos = ins[j].find(ch);
+            if (pos == std::string::npos) continue;
+            int v = in_dims_mapping[j][pos];
+            if (v != -1 && letter_dim[ch - 'a'] == -1) letter_dim[ch - 'a'] = v;
+        }
+    for (int d = 0; d < mesh_ndim; ++d) {
+        bool taken = false;
+        for (char ch : order) {
+            if (letter_dim[ch - 'a'] != d) continue;
+            if (taken) letter_dim[ch - 'a'] = -1;
+            taken = true;
+        }
+    }
+    uint32_t needs = 0;
+    for (int j = 0; j < n_in; ++j)
+        for (size_t i = 0; i < ins[j].size(); ++i) {
+            int m = letter_dim[ins[j][i] - 'a'];
+            if (merged_in && merged_in[j]) merged_in[j][i] = m;
+            if (in_dims_mapping[j][i] != m) needs |= 1u << j;
+        }
+    for (size_t i = 0; i < outs.size(); ++i) out_dims_mapping[i] = letter_dim[outs[i] - 'a'];
+    uint32_t partial = 0;
+    for (char ch : order)
+        if (outs.find(ch) == std::string::npos && letter_dim[ch - 'a'] != -1) partial |= 1u << letter_dim[ch - 'a'];
+    *out_partial_mask = partial;
+    *in_needs_reshard_mask = needs;
+    return 0;
+}
+
+// ---- reshape rule (DimTrans) ----------------------------------------------
+
+// Describes each output dim of a reshape by the Paddle DimTrans kinds:
+//   0 InputDim(i), 1 Flatten(dims), 2 Split(input dim, sizes, idx),
+//   3 Singleton, 4 Split(Flatten(dims), sizes, idx).
+// in_first/in_count: the input dims feeding the output dim; piece/npieces: its
+// index among the output dims cut from the same input group.
+// Then the sharding rule: in a group, only the leading member (first with
+// extent > 1) may carry a split, and it survives the reshape iff each device's
+// contiguous run of the flattened group is the same before and after (ceil
+// pieces of the leading input member scaled by the rest of the input group
+// equal ceil pieces of the leading output member scaled by the rest of the
+// output group). Otherwise the input must first be resharded to drop it.
+int oracle_reshape_spmd(int in_ndim, const int64_t* in_shape, const int32_t* in_dims_mapping, int out_ndim,
+                        const int64_t* out_shape, int mesh_ndim, const int64_t* mesh_shape, int32_t* in_dims_after,
+                        int32_t* out_dims_mapping, int32_t* dt_kind, int32_t* dt_in_first, int32_t* dt_in_count,
+                        int32_t* dt_piece, int32_t* dt_npieces)
+{
+    if (in_ndim < 0 || in_ndim > kMaxDim || out_ndim < 0 || out_ndim > kMaxDim || mesh_ndim < 1 ||
+        mesh_ndim > kMaxMesh)
+        return -1;
+    int64_t pi = 1, po = 1;
+    for (int i = 0; i < in_ndim; ++i) {
+        if (in_shape[i] < 1) return -1;
+        pi *= in_shape[i];
+        int v = in_dims_mapping[i];
+        if (v < -1 || v >= mesh_ndim) return -1;
+        in_dims_after[i] = v;
+    }
+    for (int o = 0; o < out_ndim; ++o) {
+        if (out_shape[o] < 1) return -1;
+        po *= out_shape[o];
+        out_dims_mapping[o] = -1;
+        dt_kind[o] = 3;
+        dt_in_first[o] = -1;
+        dt_in_count[o] = 0;
+        dt_piece[o] = 0;
+        dt_npieces[o] = 1;
+    }
+    if (pi != po) return -1;
+    int i = 0, o = 0;
+    while (i < in_ndim || o < out_ndim) {
+        if (o < out_ndim && out_shape[o] == 1 && (i >= in_ndim || in_shape[i] != 1)) {
+            ++o;  // Singleton
+            continue;
+        }
+        if (i < in_ndim && in_shape[i] == 1 && (o >= out_ndim || out_shape[o] != 1)) {
+            in_dims_after[i] = -1;  // a size-1 input dim vanishes; its split cannot survive
+            ++i;
+            continue;
+        }
+        int i0 = i, o0 = o;
+        int64_t a = in_shape[i++], b = out_shape[o++];
+        while (a != b) {
+            if (a < b) a *= in_shape[i++];
+            else b *= out_shape[o++];
+        }
+        int ni = i - i0, no = o - o0;
+        for (int k = 0; k < no; ++k) {
+            dt_kind[o0 + k] = ni == 1 && no == 1 ? 0 : (no == 1 ? 1 : (ni == 1 ? 2 : 4));
+            dt_in_first[o0 + k] = i0;
+            dt_in_count[o0 + k] = ni;
+            dt_piece[o0 + k] = k;
+            dt_npieces[o0 + k] = no;
+        }
+        // leading members
+        int li = i0, lo = o0;
+        while (li < i - 1 && in_shape[li] == 1) ++li;
+        while (lo < o - 1 && out_shape[lo] == 1) ++lo;
+        for (int k = i0; k < i; ++k)
+            if (k != li) in_dims_after[k] = -1;
+        int d = in_dims_after[li];
+        if (d == -1) continue;
+        int64_t n = mesh_shape[d];
+        int64_t L0 = in_shape[li], E0 = out_shape[lo], I = 1, J = 1;
+        for (int k = li + 1; k < i; ++k) I *= in_shape[k];
+        for (int k = lo + 1; k < o; ++k) J *= out_shape[k];
+        int64_t wi = (L0 + n - 1) / n, wo = (E0 + n - 1) / n;
+        bool same = true;
+        for (int64_t r = 0; r < n; ++r) {
+            int64_t b1 = std::min(r * wi, L0) * I, e1 = std::min((r + 1) * wi, L0) * I;
+            int64_t b2 = std::min(r * wo, E0) * J, e2 = std::min((r + 1) * wo, E0) * J;
+            if (b1 != b2 || e1 != e2) same = false;
+        }
+        if (same) out_dims_mapping[lo] = d;
+        else in_dims_after[li] = -1;
+    }
+    return 0;
+}
+
+// ---- scalar helpers exposed for pins -----------------------------------------
+
+uint16_t oracle_bf16_round(double x) { return double_to_bf16_bits(x); }
+
+double oracle_gelu(double x) { return 0.5 * x * (1.0 + std::erf(x / std::sqrt(2.0))); }
+
+// ---- TP-MLP -------------------------------------------------------------------
+
+// Megatron 1D tensor-parallel MLP on P virtual devices, for the listed rows of X:
+//   Y_i = act(X A_i)      (column-parallel: A = [A_1 ... A_P], A_i is [K, F/P])
+//   Z   = sum_i Y_i B_i   (row-parallel: B = [B_1; ...; B_P], B_i is [F/P, N])
+// X, A_i, B_i are bf16 bit patterns, row-major. Products are summed in double;
+// Y is rounded to bf16 before the second product (it is a bf16 tensor).
+// act: 0 identity, 1 GELU (exact erf form).
+// y_out (optional): [n_rows, F] with shard i in columns [i F/P, (i+1) F/P);
+// z_out: [n_rows, N].
+int oracle_tp_mlp(int64_t P, int64_t M, int64_t K, int64_t F, int64_t N, const uint16_t* X,
+                  const uint16_t* const* A, const uint16_t* const* B, int act, int round_y, int64_t n_rows,
+                  const int64_t* rows, double* y_out, double* z_out)
+{
+    if (P < 1 || F % P != 0 || M < 0 || K < 1 || N < 1) return -1;
+    int64_t Fp = F / P;
+    std::vector<double> x((size_t)K), y((size_t)Fp);
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t m = rows[r];
+        if (m < 0 || m >= M) return -1;
+        for (int64_t k = 0; k < K; ++k) x[k] = bf16_bits_to_double(X[m * K + k]);
+        double* z = z_out + r * N;
+        for (int64_t n = 0; n < N; ++n) z[n] = 0.0;
+        for (int64_t i = 0; i < P; ++i) {
+            for (int64_t f = 0; f < Fp; ++f) y[f] = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const uint16_t* arow = A[i] + k * Fp;
+                for (int64_t f = 0; f < Fp; ++f) y[f] += x[k] * bf16_bits_to_double(arow[f]);
+            }
+            for (int64_t f = 0; f < Fp; ++f) {
+                double v = act == 1 ? oracle_gelu(y[f]) : y[f];
+                if (round_y) v = bf16_bits_to_double(double_to_bf16_bits(v));
+                y[f] = v;
+                if (y_out) y_out[r * F + i * Fp + f] = v;
+            }
+            for (int64_t f = 0; f < Fp; ++f) {
+                const uint16_t* brow = B[i] + f * N;
+                for (int64_t n = 0; n < N; ++n) z[n] += y[f] * bf16_bits_to_double(brow[n]);
+            }
+        }
+    }
+    return 0;
+}
+
+}  // extern "C"
