@@ -1,0 +1,256 @@
+/*
+ * rtp.h - resharding and 1D tensor parallelism on a virtual device mesh held
+ * inside one GPU (NVIDIA GB300, sm_103a).
+ *
+ * The virtual "devices" (ranks) of a mesh are separate buffers in the memory
+ * of one GPU. Every rank buffer, and every other buffer passed here, is
+ * allocated and owned by the caller; the library never allocates memory that
+ * the caller sees and never frees a caller pointer.
+ *
+ * Conventions for every call:
+ *   - Return value: RTP_OK (0) or a negative rtp_status. On failure,
+ *     rtp_last_error() returns a text for the calling thread, and nothing
+ *     was launched (arguments are checked on the host before any launch).
+ *     RTP_ECUDA means that a CUDA call failed; its message names the call.
+ *   - Tensors are dense and row-major (C order). Shapes are int64 arrays of
+ *     length ndim (0 < ndim <= RTP_MAX_NDIM). Element types: rtp_dtype.
+ *   - "device pointer" means memory of the current CUDA device; calls that
+ *     take a stream are asynchronous with respect to the host and ordered on
+ *     that stream (NULL = the legacy default stream). Host-only calls (the
+ *     front-ends, shapes, inference) touch no GPU state.
+ *   - Source and destination buffers must not overlap.
+ *
+ * Readings of the pages that the semantics rely on (pages are cited by title
+ * and section):
+ *   - split order: "ONNX multi-device proposal", section on the index rule for
+ *     multi-axis splits: the first sharded axis is the outer loop, so shards
+ *     are produced in (a outer, b inner) order; for an ND-SBP on a mesh, mesh
+ *     dim 0 is the outer level (OneFlow 2D SBP example on ranks [[0,1],[2,3]]).
+ *   - uneven extents are left to the backend by the ONNX page (note on
+ *     divisibility). Here every split level cuts its interval into pieces of
+ *     ceil(len/n) with a short (possibly empty) last piece; two mesh dims
+ *     splitting one axis cut it level by level, outer mesh dim first.
+ *   - partial (OneFlow SBP definition): the logical tensor is the element-wise
+ *     sum of the rank tensors. When a logical tensor is *sharded* to a
+ *     partial layout, the rank whose partial coordinates are all zero holds
+ *     the value and the other ranks hold zeros.
+ */
+#ifndef RTP_H_
+#define RTP_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RTP_MAX_NDIM 8
+#define RTP_MAX_MESH_NDIM 4
+#define RTP_MAX_RANKS 64
+
+typedef enum { RTP_F32 = 0, RTP_BF16 = 1 } rtp_dtype;
+
+typedef enum {
+    RTP_OK = 0,
+    RTP_EINVAL = -1,       /* malformed argument (NULL pointer, bad spec, bad axis) */
+    RTP_ESHAPE = -2,       /* sizes that do not fit the operation (e.g. F % P != 0) */
+    RTP_EUNSUPPORTED = -3, /* legal-looking request outside what is implemented */
+    RTP_ECONFLICT = -4,    /* inference found no consistent result */
+    RTP_ECUDA = -5,        /* a CUDA runtime/driver call failed */
+    RTP_ENOMEM = -6        /* host-side allocation failed */
+} rtp_status;
+
+/* Per-mesh-dim distribution (OneFlow SBP page: split, broadcast, partial). */
+typedef enum { RTP_SBP_SPLIT = 0, RTP_SBP_BROADCAST = 1, RTP_SBP_PARTIAL_SUM = 2 } rtp_sbp;
+
+/* A CUDA stream (cudaStream_t) passed as an opaque pointer; NULL = default stream. */
+typedef void* rtp_stream;
+
+/*
+ * Canonical layout of a tensor on a virtual mesh (the ND-SBP form of the
+ * OneFlow page; the Paddle dims_mapping and ONNX ShardingSpec forms are
+ * converted to it by the front-ends below).
+ *   mesh_ndim     number of mesh dims, 1..RTP_MAX_MESH_NDIM
+ *   mesh_shape    size of each mesh dim (>= 1); R = product <= RTP_MAX_RANKS
+ *   rank_ids      the mesh, row-major: rank_ids[p] is the rank at flat mesh
+ *                 position p. Must be a permutation of 0..R-1; rank r's buffer
+ *                 is entry r of the buffer arrays passed to shard/reshard.
+ *   sbp_kind      per mesh dim, an rtp_sbp value
+ *   sbp_axis      per mesh dim with RTP_SBP_SPLIT: the tensor axis it splits,
+ *                 in [0, ndim); ignored otherwise
+ */
+typedef struct {
+    int32_t mesh_ndim;
+    int64_t mesh_shape[RTP_MAX_MESH_NDIM];
+    int32_t rank_ids[RTP_MAX_RANKS];
+    int32_t sbp_kind[RTP_MAX_MESH_NDIM];
+    int32_t sbp_axis[RTP_MAX_MESH_NDIM];
+} rtp_spec;
+
+/* ---- front-ends and geometry (host only) ----------------------------------- */
+
+/*
+ * Paddle form ("SPMD rules" design note, ProcessMesh and dims_mapping):
+ * dims_mapping[i] = j splits tensor dim i along mesh dim j; -1 keeps it whole.
+ * Mesh dims that no tensor dim names are broadcast, or partial-sum when their
+ * bit is set in partial_mask. rank_ids: the ProcessMesh ids, row-major (NULL
+ * means 0..R-1). Two tensor dims on one mesh dim, or a mesh dim both split
+ * and partial, give RTP_EINVAL.
+ */
+int rtp_spec_from_dims_mapping(int ndim, const int32_t* dims_mapping, int mesh_ndim, const int64_t* mesh_shape,
+                               const int32_t* rank_ids, uint32_t partial_mask, rtp_spec* out);
+
+/*
+ * ONNX form ("ONNX multi-device proposal", ShardingSpecProto, ShardedDimProto,
+ * SimpleShardedDimProto and device_map = index_to_device_group_map):
+ *   device[n_device]     rank ids, or negative keys into the group map
+ *   group_keys[n_groups] the negative keys; group k holds group_sizes[k]
+ *                        ranks, listed consecutively in group_devices
+ *   axes[n_sharded], num_shards[n_sharded]
+ *                        one simple_sharding per sharded_dim (axis may be
+ *                        negative, counted from the end)
+ * Split piece s (row-major over the sharded dims, first listed = outer) goes
+ * to device[s], or to every rank of its group. Requires the product of
+ * num_shards to equal n_device. Result: mesh [num_shards..., group size],
+ * the last dim broadcast when groups hold more than one rank.
+ * RTP_EUNSUPPORTED: groups of unequal size.
+ */
+int rtp_spec_from_onnx(int ndim, int n_device, const int64_t* device, int n_groups, const int64_t* group_keys,
+                       const int32_t* group_sizes, const int64_t* group_devices, int n_sharded, const int64_t* axes,
+                       const int64_t* num_shards, rtp_spec* out);
+
+/* Checks a spec against a tensor rank; RTP_OK if usable. */
+int rtp_spec_check(int ndim, const rtp_spec* spec);
+
+/* Shape of rank `rank`'s piece of a tensor of shape `shape` (out_shape[ndim]). */
+int rtp_shard_shape(int ndim, const int64_t* shape, const rtp_spec* spec, int rank, int64_t* out_shape);
+
+/*
+ * Box [lo, hi) of the logical tensor covered by rank `rank`, and whether the
+ * rank holds values (0 only for a non-zero partial coordinate when sharding).
+ */
+int rtp_shard_box(int ndim, const int64_t* shape, const rtp_spec* spec, int rank, int64_t* lo, int64_t* hi,
+                  int32_t* holds_value);
+
+/* ---- the four calls -------------------------------------------------------- */
+
+/*
+ * shard(tensor, spec): materialises every rank's piece of a logical tensor
+ * ("ONNX multi-device proposal": sharding as a split, as a broadcast, and
+ * split plus broadcast; OneFlow page: split, broadcast, partial).
+ *   full       device pointer, the logical tensor [shape]
+ *   shard_dev  R device pointers; shard_dev[r] receives rank r's piece, of
+ *              shape rtp_shard_shape(r) (empty pieces may pass NULL)
+ * Data movement is bit-exact.
+ */
+int rtp_shard(rtp_dtype dtype, int ndim, const int64_t* shape, const void* full, const rtp_spec* spec,
+              void* const* shard_dev, rtp_stream stream);
+
+/*
+ * reshard(shards, src_spec, dst_spec): converts rank pieces from one layout to
+ * another ("boxing" in the OneFlow page; "reshard inputs" step of the ONNX
+ * execution semantics): S(i)->S(j) (all-to-all), S->B (all-gather), B->S
+ * (slice), P->B (all-reduce), P->S (reduce-scatter), and any mix on an ND mesh.
+ *   src_dev  R_src device pointers laid out by `src`
+ *   dst_dev  R_dst device pointers laid out by `dst` (meshes may differ)
+ * Without partial sources the result is bit-exact. Partial sources are
+ * summed in float32 in a fixed order (partial coordinates row-major), then
+ * rounded once to the element type; results are identical run to run.
+ */
+int rtp_reshard(rtp_dtype dtype, int ndim, const int64_t* shape, const void* const* src_dev, const rtp_spec* src,
+                void* const* dst_dev, const rtp_spec* dst, rtp_stream stream);
+
+/*
+ * Algorithmic traffic of a reshard (host only): bytes read (each distinct
+ * source byte once; every partial read) and bytes written (every destination
+ * byte), and the number of copy tasks and kernel launches it plans.
+ */
+int rtp_reshard_cost(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_spec* src, const rtp_spec* dst,
+                     int64_t* bytes_read, int64_t* bytes_written, int32_t* n_tasks, int32_t* n_launches);
+
+/*
+ * infer_spmd(einsum, dims_mappings) (Paddle "SPMD rules" note, steps 1-3:
+ * einsum notation, ShardingMergeForTensors, GetDimsMappingForAxes; ONNX
+ * sharding formalism, reduction operators). Host only.
+ *   einsum            e.g. "mk,kn->mn": one letter per axis, inputs separated
+ *                     by ',', output after "->" (letters a-z, none repeated
+ *                     within one operand)
+ *   in_dims_mappings  n_in arrays, one entry per letter of that input
+ *   out_dims_mapping  receives one entry per output letter
+ *   out_partial_mask  bit d set: the output is a partial sum over mesh dim d
+ *                     (a sharded letter summed away)
+ *   in_needs_reshard_mask  bit j set: input j must be resharded to its
+ *                     inferred mapping (written to in_inferred[j] if given)
+ * Merge rule: a letter takes the first mesh dim any input gives it (inputs in
+ * order); a mesh dim shards one letter only, the one that comes first in the
+ * einsum string.
+ */
+int rtp_infer_spmd(const char* einsum, int n_in, const int32_t* const* in_dims_mappings, int mesh_ndim,
+                   int32_t* out_dims_mapping, uint32_t* out_partial_mask, uint32_t* in_needs_reshard_mask,
+                   int32_t* const* in_inferred);
+
+/*
+ * Reshape rule (Paddle note, DimTrans: InputDim, Flatten, Split, Singleton).
+ * Host only. A split survives a reshape only on the leading (first non-unit)
+ * member of a group of dims that map onto each other, and only if every
+ * rank's contiguous run of that group is the same before and after; other
+ * splits are dropped (in_after = the mapping the input must be resharded to).
+ */
+int rtp_infer_reshape(int in_ndim, const int64_t* in_shape, const int32_t* in_dims_mapping, int out_ndim,
+                      const int64_t* out_shape, int mesh_ndim, const int64_t* mesh_shape, int32_t* in_after,
+                      int32_t* out_dims_mapping);
+
+/*
+ * tp_mlp(X, A_shards, B_shards): the Megatron 1D tensor-parallel MLP on P
+ * virtual ranks (ColossalAI "1D tensor parallelism" page, sections 2 and 2.1:
+ * column-parallel Y_i = X A_i, row-parallel Z = sum_i Y_i B_i; GELU between
+ * the GEMMs as in the Domino page's "GeMM GeLU GeMM").
+ *   X         bf16 [M, K] device pointer
+ *   A_shards  P bf16 [K, F/P] device pointers (column blocks of A)
+ *   B_shards  P bf16 [F/P, N] device pointers (row blocks of B)
+ *   Y         P bf16 [M, F/P] device pointers; receives Y_i = GELU(X A_i)
+ *             (exact erf GELU on the float32 accumulator, rounded once)
+ *   partials  P float32 [M, N] device pointers for mode 0 (receive Y_i B_i);
+ *             may be NULL in mode 1
+ *   Z         float32 [M, N] device pointer; receives sum_i Y_i B_i
+ *   mode      0: row-parallel GEMM writes per-rank partials, a separate
+ *             kernel sums them (the all-reduce); 1: the row-parallel GEMM
+ *             walks all ranks' K ranges in one accumulator (fused reduction)
+ *   chunks    1, 2 or 4: Domino row split of X (and Z); in mode 0 the sum of
+ *             chunk c runs on s1 while chunk c+1's GEMMs run on s0
+ *   col_blocks 1 or 2: Domino column split of B_i (mode 0); the sum of
+ *             column block 0 overlaps the GEMM of block 1
+ *   s0, s1    streams; all work is ordered after prior work on s0 and the
+ *             call's completion is ordered on s0 (s1 is joined back)
+ * Requirements (else RTP_ESHAPE, like the ValueError on out_features %
+ * tp_size in ColossalAI's Linear1D_Col): F % P == 0, M % chunks == 0,
+ * M/chunks % 128 == 0, (F/P) % 256 == 0, K % 64 == 0, (F/P) % 64 == 0,
+ * N % (256 * col_blocks) == 0; all pointers 16-byte aligned.
+ * The first call on a device builds its kernels' tensor maps; no allocation.
+ */
+int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X, const void* const* A_shards,
+               const void* const* B_shards, void* const* Y, void* const* partials, float* Z, int mode, int chunks,
+               int col_blocks, rtp_stream s0, rtp_stream s1);
+
+/*
+ * Reads and clears the device word in which the tensor-core kernels of
+ * rtp_tp_mlp record a wait that gave up (no progress for about 4 seconds; the
+ * kernel then stops, frees its tensor memory and returns instead of hanging).
+ * Synchronises `stream`. *code == 0: no such event since the last check;
+ * otherwise the results of the launches since then are invalid
+ * (1 producer, 2 MMA waiting for operands, 3 MMA waiting for an accumulator,
+ * 4 epilogue).
+ */
+int rtp_device_error(rtp_stream stream, uint32_t* code);
+
+/* Text of the last error on the calling thread ("" if none). */
+const char* rtp_last_error(void);
+
+/* Library version string. */
+const char* rtp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RTP_H_ */

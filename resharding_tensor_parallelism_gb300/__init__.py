@@ -1,0 +1,347 @@
+"""Python binding of librtp (resharding and 1D tensor parallelism on a virtual
+mesh inside one GB300).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels. PyTorch supplies device memory and streams. Loading fails loudly if
+the compiled library is missing; there is no fallback.
+
+Names mirror the C ABI in ``include/rtp.h``:
+  spec_from_dims_mapping, spec_from_onnx, spec_nd_sbp (the ND-SBP form filled
+  directly), shard_shape, shard_box, shard, reshard, reshard_cost,
+  infer_spmd, infer_reshape, tp_mlp, last_error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence, Tuple, Union
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librtp.so")
+
+MAX_NDIM = 8
+MAX_MESH_NDIM = 4
+MAX_RANKS = 64
+F32, BF16 = 0, 1
+SPLIT, BROADCAST, PARTIAL = 0, 1, 2
+STATUS = {0: "RTP_OK", -1: "RTP_EINVAL", -2: "RTP_ESHAPE", -3: "RTP_EUNSUPPORTED", -4: "RTP_ECONFLICT",
+          -5: "RTP_ECUDA", -6: "RTP_ENOMEM"}
+
+
+class RtpError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (STATUS.get(status, status), message))
+        self.status = status
+
+
+class Spec(ctypes.Structure):
+    """rtp_spec: the canonical (ND-SBP) layout of a tensor on a virtual mesh."""
+
+    _fields_ = [
+        ("mesh_ndim", ctypes.c_int32),
+        ("mesh_shape", ctypes.c_int64 * MAX_MESH_NDIM),
+        ("rank_ids", ctypes.c_int32 * MAX_RANKS),
+        ("sbp_kind", ctypes.c_int32 * MAX_MESH_NDIM),
+        ("sbp_axis", ctypes.c_int32 * MAX_MESH_NDIM),
+    ]
+
+    @property
+    def num_ranks(self) -> int:
+        n = 1
+        for d in range(self.mesh_ndim):
+            n *= self.mesh_shape[d]
+        return n
+
+    def describe(self):
+        ents = []
+        for d in range(self.mesh_ndim):
+            k = self.sbp_kind[d]
+            ents.append(("S", self.sbp_axis[d]) if k == SPLIT else ("B" if k == BROADCAST else "P"))
+        mesh = tuple(self.mesh_shape[d] for d in range(self.mesh_ndim))
+        return mesh, tuple(ents), tuple(self.rank_ids[p] for p in range(self.num_ranks))
+
+    def __repr__(self):
+        mesh, ents, ranks = self.describe()
+        return "Spec(mesh=%s, sbp=%s, ranks=%s)" % (mesh, ents, ranks)
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("librtp.so is not built (%s); run `python -c \"import __graft_entry__ as g; g.build()\"`"
+                          % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER
+    i64p, i32p, u32p, vp = P(ctypes.c_int64), P(ctypes.c_int32), P(ctypes.c_uint32), ctypes.c_void_p
+    vpp = P(ctypes.c_void_p)
+    c_int = ctypes.c_int
+    sig = {
+        "rtp_spec_from_dims_mapping": [c_int, i32p, c_int, i64p, i32p, ctypes.c_uint32, P(Spec)],
+        "rtp_spec_from_onnx": [c_int, c_int, i64p, c_int, i64p, i32p, i64p, c_int, i64p, i64p, P(Spec)],
+        "rtp_spec_check": [c_int, P(Spec)],
+        "rtp_shard_shape": [c_int, i64p, P(Spec), c_int, i64p],
+        "rtp_shard_box": [c_int, i64p, P(Spec), c_int, i64p, i64p, i32p],
+        "rtp_shard": [c_int, c_int, i64p, vp, P(Spec), vpp, vp],
+        "rtp_reshard": [c_int, c_int, i64p, vpp, P(Spec), vpp, P(Spec), vp],
+        "rtp_reshard_cost": [c_int, c_int, i64p, P(Spec), P(Spec), i64p, i64p, i32p, i32p],
+        "rtp_infer_spmd": [ctypes.c_char_p, c_int, P(i32p), c_int, i32p, u32p, u32p, P(i32p)],
+        "rtp_infer_reshape": [c_int, i64p, i32p, c_int, i64p, c_int, i64p, i32p, i32p],
+        "rtp_device_error": [vp, u32p],
+        "rtp_tp_mlp": [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vpp, vpp, vpp,
+                       vpp, vp, c_int, c_int, c_int, vp, vp],
+    }
+    for name, args in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = c_int
+    lib.rtp_last_error.restype = ctypes.c_char_p
+    lib.rtp_last_error.argtypes = []
+    lib.rtp_version.restype = ctypes.c_char_p
+    lib.rtp_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def lib():
+    """The loaded ctypes library (loads it on first use)."""
+    return _load()
+
+
+def last_error() -> str:
+    return _load().rtp_last_error().decode()
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        raise RtpError(rc, last_error())
+
+
+def _i64(xs) -> ctypes.Array:
+    xs = [int(x) for x in xs]
+    return (ctypes.c_int64 * max(1, len(xs)))(*xs)
+
+
+def _i32(xs) -> ctypes.Array:
+    xs = [int(x) for x in xs]
+    return (ctypes.c_int32 * max(1, len(xs)))(*xs)
+
+
+def _ptrs(ptrs) -> ctypes.Array:
+    return (ctypes.c_void_p * max(1, len(ptrs)))(*[p if p else None for p in ptrs])
+
+
+# ---- specs ------------------------------------------------------------------------
+
+Entry = Union[str, Tuple[str, int]]
+
+
+def spec_nd_sbp(mesh: Sequence[int], entries: Sequence[Entry], rank_ids: Sequence[int] = ()) -> Spec:
+    """ND-SBP form: one entry per mesh dim, ("S", axis), "B" or "P" (OneFlow page)."""
+    s = Spec()
+    s.mesh_ndim = len(mesh)
+    n = 1
+    for d, m in enumerate(mesh):
+        s.mesh_shape[d] = int(m)
+        n *= int(m)
+    ranks = list(rank_ids) if rank_ids else list(range(n))
+    if len(ranks) > MAX_RANKS:
+        raise RtpError(-3, "more than %d ranks" % MAX_RANKS)
+    for p, r in enumerate(ranks):
+        s.rank_ids[p] = int(r)
+    for d, e in enumerate(entries):
+        if e == "B":
+            s.sbp_kind[d], s.sbp_axis[d] = BROADCAST, -1
+        elif e == "P":
+            s.sbp_kind[d], s.sbp_axis[d] = PARTIAL, -1
+        else:
+            s.sbp_kind[d], s.sbp_axis[d] = SPLIT, int(e[1])
+    return s
+
+
+def spec_from_dims_mapping(dims_mapping: Sequence[int], mesh: Sequence[int], rank_ids: Sequence[int] = (),
+                           partial: Sequence[int] = ()) -> Spec:
+    mask = 0
+    for d in partial:
+        mask |= 1 << int(d)
+    out = Spec()
+    _check(_load().rtp_spec_from_dims_mapping(len(dims_mapping), _i32(dims_mapping), len(mesh), _i64(mesh),
+                                              _i32(rank_ids) if rank_ids else None, mask, ctypes.byref(out)))
+    return out
+
+
+def spec_from_onnx(ndim: int, device: Sequence[int], device_map: dict, sharded_dim: Sequence[Tuple[int, int]]
+                   ) -> Spec:
+    """device: ids or negative keys; device_map: {key: [ids]}; sharded_dim: [(axis, num_shards)]."""
+    keys = list(device_map.keys())
+    sizes = [len(device_map[k]) for k in keys]
+    flat = [d for k in keys for d in device_map[k]]
+    out = Spec()
+    _check(_load().rtp_spec_from_onnx(ndim, len(device), _i64(device), len(keys), _i64(keys), _i32(sizes),
+                                      _i64(flat), len(sharded_dim), _i64([a for a, _ in sharded_dim]),
+                                      _i64([s for _, s in sharded_dim]), ctypes.byref(out)))
+    return out
+
+
+def spec_check(ndim: int, spec: Spec) -> None:
+    _check(_load().rtp_spec_check(ndim, ctypes.byref(spec)))
+
+
+def shard_shape(shape: Sequence[int], spec: Spec, rank: int) -> Tuple[int, ...]:
+    out = _i64([0] * len(shape))
+    _check(_load().rtp_shard_shape(len(shape), _i64(shape), ctypes.byref(spec), rank, out))
+    return tuple(out[a] for a in range(len(shape)))
+
+
+def shard_box(shape: Sequence[int], spec: Spec, rank: int):
+    nd = len(shape)
+    lo, hi, hv = _i64([0] * nd), _i64([0] * nd), ctypes.c_int32()
+    _check(_load().rtp_shard_box(nd, _i64(shape), ctypes.byref(spec), rank, lo, hi, ctypes.byref(hv)))
+    return tuple(lo[a] for a in range(nd)), tuple(hi[a] for a in range(nd)), bool(hv.value)
+
+
+# ---- data movement ----------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError("rtp tensors are float32 or bfloat16, got %s" % t.dtype)
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def _alloc_pieces(shape, spec: Spec, like, out):
+    torch = _torch()
+    if out is not None:
+        return list(out)
+    return [torch.empty(shard_shape(shape, spec, r), dtype=like.dtype, device=like.device)
+            for r in range(spec.num_ranks)]
+
+
+def _check_cuda(ts, what):
+    for t in ts:
+        if t is not None and t.numel() > 0:
+            if not t.is_cuda:
+                raise RtpError(-1, "%s: tensors must live on the GPU" % what)
+            if not t.is_contiguous():
+                raise RtpError(-1, "%s: tensors must be contiguous (row-major)" % what)
+
+
+def shard(full, spec: Spec, out=None, stream=None):
+    """Rank pieces of the logical tensor `full` (a CUDA tensor) under `spec`."""
+    shape = tuple(full.shape)
+    pieces = _alloc_pieces(shape, spec, full, out)
+    _check_cuda([full] + pieces, "shard")
+    _check(_load().rtp_shard(_dtype_code(full), len(shape), _i64(shape), full.data_ptr(), ctypes.byref(spec),
+                             _ptrs([p.data_ptr() for p in pieces]), _stream_ptr(stream)))
+    return pieces
+
+
+def reshard(pieces, shape: Sequence[int], src: Spec, dst: Spec, out=None, stream=None):
+    """Pieces laid out by `dst`, from `pieces` laid out by `src`."""
+    shape = tuple(int(s) for s in shape)
+    like = pieces[0]
+    outs = _alloc_pieces(shape, dst, like, out)
+    _check_cuda(list(pieces) + outs, "reshard")
+    _check(_load().rtp_reshard(_dtype_code(like), len(shape), _i64(shape), _ptrs([p.data_ptr() for p in pieces]),
+                               ctypes.byref(src), _ptrs([o.data_ptr() for o in outs]), ctypes.byref(dst),
+                               _stream_ptr(stream)))
+    return outs
+
+
+def reshard_cost(dtype_code: int, shape: Sequence[int], src: Spec, dst: Spec):
+    """(bytes_read, bytes_written, n_tasks, n_launches) planned for a reshard."""
+    rd, wr, nt, nl = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+    _check(_load().rtp_reshard_cost(dtype_code, len(shape), _i64(shape), ctypes.byref(src), ctypes.byref(dst),
+                                    ctypes.byref(rd), ctypes.byref(wr), ctypes.byref(nt), ctypes.byref(nl)))
+    return rd.value, wr.value, nt.value, nl.value
+
+
+# ---- inference --------------------------------------------------------------------
+
+def infer_spmd(einsum: str, dims_mappings: Sequence[Sequence[int]], mesh_ndim: int):
+    """(out_dims_mapping, partial_mesh_dims, inputs_needing_reshard, inferred_input_mappings)."""
+    lhs, rhs = einsum.split("->") if "->" in einsum else (einsum, "")
+    ins = lhs.split(",")
+    P = ctypes.POINTER(ctypes.c_int32)
+    arrs = [_i32(dm) for dm in dims_mappings]
+    merged = [_i32([0] * max(1, len(t))) for t in ins]
+    inp = (P * max(1, len(arrs)))(*[ctypes.cast(a, P) for a in arrs])
+    mp = (P * max(1, len(merged)))(*[ctypes.cast(a, P) for a in merged])
+    out = _i32([0] * max(1, len(rhs)))
+    pm, rm = ctypes.c_uint32(), ctypes.c_uint32()
+    _check(_load().rtp_infer_spmd(einsum.encode(), len(dims_mappings), inp, mesh_ndim, out, ctypes.byref(pm),
+                                  ctypes.byref(rm), mp))
+    return ([out[i] for i in range(len(rhs))], [d for d in range(32) if (pm.value >> d) & 1],
+            [j for j in range(len(ins)) if (rm.value >> j) & 1],
+            [[merged[j][i] for i in range(len(ins[j]))] for j in range(len(ins))])
+
+
+def infer_reshape(in_shape, in_dims_mapping, out_shape, mesh):
+    """(in_dims_after, out_dims_mapping) for a reshape."""
+    ni, no = len(in_shape), len(out_shape)
+    after, outm = _i32([0] * ni), _i32([0] * no)
+    _check(_load().rtp_infer_reshape(ni, _i64(in_shape), _i32(in_dims_mapping), no, _i64(out_shape), len(mesh),
+                                     _i64(mesh), after, outm))
+    return [after[i] for i in range(ni)], [outm[o] for o in range(no)]
+
+
+# ---- tensor-parallel MLP ------------------------------------------------------------
+
+def tp_mlp(X, A_shards, B_shards, Y=None, partials=None, Z=None, mode: int = 1, chunks: int = 1,
+           col_blocks: int = 1, s0=None, s1=None):
+    """Z = sum_i GELU(X A_i) B_i on P = len(A_shards) virtual ranks (bf16 in, float32 Z).
+    Returns (Z, Y). Buffers not given are allocated with torch."""
+    torch = _torch()
+    P = len(A_shards)
+    M, K = X.shape
+    Fp = A_shards[0].shape[1]
+    N = B_shards[0].shape[1]
+    F = Fp * P
+    dev = X.device
+    if Y is None:
+        Y = [torch.empty((M, Fp), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    if Z is None:
+        Z = torch.empty((M, N), dtype=torch.float32, device=dev)
+    if mode == 0 and partials is None:
+        partials = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in range(P)]
+    _check_cuda([X, Z] + list(A_shards) + list(B_shards) + list(Y) + list(partials or []), "tp_mlp")
+    if s0 is None:
+        s0 = torch.cuda.current_stream()
+    if s1 is None:
+        s1 = s0
+    pp = _ptrs([p.data_ptr() for p in partials]) if partials is not None else None
+    _check(_load().rtp_tp_mlp(P, M, K, F, N, X.data_ptr(), _ptrs([a.data_ptr() for a in A_shards]),
+                              _ptrs([b.data_ptr() for b in B_shards]), _ptrs([y.data_ptr() for y in Y]), pp,
+                              Z.data_ptr(), mode, chunks, col_blocks, _stream_ptr(s0), _stream_ptr(s1)))
+    return Z, Y
+
+
+def device_error(stream=None) -> int:
+    """Reads and clears the device word set when a tensor-core kernel's bounded wait gave up."""
+    code = ctypes.c_uint32()
+    _check(_load().rtp_device_error(_stream_ptr(stream), ctypes.byref(code)))
+    return code.value
+
+
+def version() -> str:
+    return _load().rtp_version().decode()

@@ -1,0 +1,187 @@
+// Host-side sharding inference.
+//
+// infer_spmd follows the einsum-based rule of the Paddle "SPMD rules" design
+// note: (1) the op as an einsum, (2) merge the inputs' dims_mappings per
+// einsum letter (ShardingMergeForTensors), (3) read the output's mapping off
+// the merged letters (GetDimsMappingForAxes). A letter that is summed away
+// while sharded leaves the output partial over that mesh dim (ONNX sharding
+// formalism, reduction operators: a local reduction followed by a
+// cross-device one).
+//
+// The reshape rule follows the same note's DimTrans table (InputDim, Flatten,
+// Split, Singleton).
+#include <cstring>
+#include <string>
+
+#include "rtp_internal.h"
+
+using namespace rtp;
+
+namespace {
+
+struct Parsed {
+    int n_in = 0;
+    std::string in[8];
+    std::string out;
+};
+
+int parse_einsum(const char* s, int n_in, Parsed* p)
+{
+    if (!s) return fail(RTP_EINVAL, "rtp_infer_spmd: einsum is NULL");
+    const char* arrow = std::strstr(s, "->");
+    if (!arrow) return fail(RTP_EINVAL, "rtp_infer_spmd: einsum \"%s\" has no \"->\"", s);
+    int k = 0;
+    for (const char* c = s; c < arrow; ++c) {
+        if (*c == ',') {
+            if (++k >= 8) return fail(RTP_EUNSUPPORTED, "rtp_infer_spmd: more than 8 inputs");
+            continue;
+        }
+        if (*c < 'a' || *c > 'z') return fail(RTP_EINVAL, "rtp_infer_spmd: bad character '%c' in \"%s\"", *c, s);
+        if (p->in[k].find(*c) != std::string::npos)
+            return fail(RTP_EUNSUPPORTED, "rtp_infer_spmd: letter '%c' repeated within one operand", *c);
+        p->in[k].push_back(*c);
+    }
+    p->n_in = k + 1;
+    if (p->n_in != n_in) return fail(RTP_EINVAL, "rtp_infer_spmd: einsum has %d inputs, %d mappings given", p->n_in, n_in);
+    for (const char* c = arrow + 2; *c; ++c) {
+        if (*c < 'a' || *c > 'z') return fail(RTP_EINVAL, "rtp_infer_spmd: bad character '%c' in \"%s\"", *c, s);
+        if (p->out.find(*c) != std::string::npos) return fail(RTP_EINVAL, "rtp_infer_spmd: output letter '%c' repeated", *c);
+        bool found = false;
+        for (int j = 0; j < p->n_in; ++j) found = found || p->in[j].find(*c) != std::string::npos;
+        if (!found) return fail(RTP_EINVAL, "rtp_infer_spmd: output letter '%c' is in no input", *c);
+        p->out.push_back(*c);
+    }
+    return RTP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int rtp_infer_spmd(const char* einsum, int n_in, const int32_t* const* in_dims_mappings, int mesh_ndim,
+                   int32_t* out_dims_mapping, uint32_t* out_partial_mask, uint32_t* in_needs_reshard_mask,
+                   int32_t* const* in_inferred)
+{
+    if (!in_dims_mappings || !out_dims_mapping || !out_partial_mask || !in_needs_reshard_mask)
+        return fail(RTP_EINVAL, "rtp_infer_spmd: NULL argument");
+    if (mesh_ndim < 1 || mesh_ndim > 32) return fail(RTP_EINVAL, "rtp_infer_spmd: mesh_ndim %d", mesh_ndim);
+    Parsed p;
+    int st = parse_einsum(einsum, n_in, &p);
+    if (st) return st;
+    for (int j = 0; j < n_in; ++j) {
+        if (!in_dims_mappings[j] && !p.in[j].empty()) return fail(RTP_EINVAL, "rtp_infer_spmd: mapping %d is NULL", j);
+        uint32_t used = 0;
+        for (size_t i = 0; i < p.in[j].size(); ++i) {
+            int v = in_dims_mappings[j][i];
+            if (v < -1 || v >= mesh_ndim) return fail(RTP_EINVAL, "rtp_infer_spmd: input %d dim %zu maps to mesh dim %d", j, i, v);
+            if (v >= 0 && ((used >> v) & 1u)) return fail(RTP_EINVAL, "rtp_infer_spmd: input %d uses mesh dim %d twice", j, v);
+            if (v >= 0) used |= 1u << v;
+        }
+    }
+    // Letters in the order they first appear in the einsum string.
+    std::string order;
+    for (const char* c = einsum; *c; ++c)
+        if (*c >= 'a' && *c <= 'z' && order.find(*c) == std::string::npos) order.push_back(*c);
+    int dim_of[26];
+    for (int& d : dim_of) d = -1;
+    // Step 2: merge. First sharded occurrence wins; later disagreeing inputs reshard.
+    for (char L : order)
+        for (int j = 0; j < n_in && dim_of[L - 'a'] == -1; ++j) {
+            size_t pos = p.in[j].find(L);
+            if (pos != std::string::npos) dim_of[L - 'a'] = in_dims_mappings[j][pos];
+        }
+    // A mesh dim shards one letter only: the earliest letter keeps it.
+    uint32_t claimed = 0;
+    for (char L : order) {
+        int d = dim_of[L - 'a'];
+        if (d < 0) continue;
+        if ((claimed >> d) & 1u) dim_of[L - 'a'] = -1;
+        else claimed |= 1u << d;
+    }
+    uint32_t needs = 0;
+    for (int j = 0; j < n_in; ++j)
+        for (size_t i = 0; i < p.in[j].size(); ++i) {
+            int m = dim_of[p.in[j][i] - 'a'];
+            if (in_dims_mappings[j][i] != m) needs |= 1u << j;
+            if (in_inferred && in_inferred[j]) in_inferred[j][i] = m;
+        }
+    // Step 3: output mapping; contracted sharded letters leave partial sums.
+    for (size_t i = 0; i < p.out.size(); ++i) out_dims_mapping[i] = dim_of[p.out[i] - 'a'];
+    uint32_t partial = 0;
+    for (char L : order)
+        if (p.out.find(L) == std::string::npos && dim_of[L - 'a'] >= 0) partial |= 1u << dim_of[L - 'a'];
+    *out_partial_mask = partial;
+    *in_needs_reshard_mask = needs;
+    return RTP_OK;
+}
+
+int rtp_infer_reshape(int in_ndim, const int64_t* in_shape, const int32_t* in_dims_mapping, int out_ndim,
+                      const int64_t* out_shape, int mesh_ndim, const int64_t* mesh_shape, int32_t* in_after,
+                      int32_t* out_dims_mapping)
+{
+    const char* fn = "rtp_infer_reshape";
+    if (!in_shape || !in_dims_mapping || !out_shape || !mesh_shape || !in_after || !out_dims_mapping)
+        return fail(RTP_EINVAL, "%s: NULL argument", fn);
+    if (in_ndim < 1 || in_ndim > RTP_MAX_NDIM || out_ndim < 1 || out_ndim > RTP_MAX_NDIM)
+        return fail(RTP_EINVAL, "%s: ranks %d -> %d", fn, in_ndim, out_ndim);
+    if (mesh_ndim < 1 || mesh_ndim > RTP_MAX_MESH_NDIM) return fail(RTP_EINVAL, "%s: mesh_ndim %d", fn, mesh_ndim);
+    int64_t ni = 1, no = 1;
+    for (int i = 0; i < in_ndim; ++i) {
+        if (in_shape[i] < 1) return fail(RTP_ESHAPE, "%s: input extent %d is %lld", fn, i, (long long)in_shape[i]);
+        int v = in_dims_mapping[i];
+        if (v < -1 || v >= mesh_ndim) return fail(RTP_EINVAL, "%s: dims_mapping[%d] = %d", fn, i, v);
+        ni *= in_shape[i];
+        in_after[i] = v;
+    }
+    for (int o = 0; o < out_ndim; ++o) {
+        if (out_shape[o] < 1) return fail(RTP_ESHAPE, "%s: output extent %d is %lld", fn, o, (long long)out_shape[o]);
+        no *= out_shape[o];
+        out_dims_mapping[o] = -1;
+    }
+    if (ni != no) return fail(RTP_ESHAPE, "%s: %lld elements cannot become %lld", fn, (long long)ni, (long long)no);
+    int i = 0, o = 0;
+    while (i < in_ndim || o < out_ndim) {
+        const bool out_unit = o < out_ndim && out_shape[o] == 1;
+        const bool in_unit = i < in_ndim && in_shape[i] == 1;
+        if (out_unit && !in_unit) {  // Singleton output dim
+            ++o;
+            continue;
+        }
+        if (in_unit && !out_unit) {  // unit input dim disappears with its split
+            in_after[i++] = -1;
+            continue;
+        }
+        // A group of input dims and output dims with equal products.
+        const int gi = i, go = o;
+        int64_t a = in_shape[i++], b = out_shape[o++];
+        while (a != b) {
+            if (a < b) a *= in_shape[i++];
+            else b *= out_shape[o++];
+        }
+        int lead_in = gi, lead_out = go;
+        while (lead_in + 1 < i && in_shape[lead_in] == 1) ++lead_in;
+        while (lead_out + 1 < o && out_shape[lead_out] == 1) ++lead_out;
+        for (int k = gi; k < i; ++k)
+            if (k != lead_in) in_after[k] = -1;
+        const int d = in_after[lead_in];
+        if (d < 0) continue;
+        const int64_t n = mesh_shape[d];
+        int64_t inner_in = 1, inner_out = 1;
+        for (int k = lead_in + 1; k < i; ++k) inner_in *= in_shape[k];
+        for (int k = lead_out + 1; k < o; ++k) inner_out *= out_shape[k];
+        // Each rank's run of the flattened group, before and after.
+        const int64_t L = in_shape[lead_in], E = out_shape[lead_out];
+        const int64_t wl = (L + n - 1) / n, we = (E + n - 1) / n;
+        bool keep = true;
+        for (int64_t r = 0; r < n && keep; ++r) {
+            const int64_t x0 = (r * wl < L ? r * wl : L) * inner_in, x1 = ((r + 1) * wl < L ? (r + 1) * wl : L) * inner_in;
+            const int64_t y0 = (r * we < E ? r * we : E) * inner_out, y1 = ((r + 1) * we < E ? (r + 1) * we : E) * inner_out;
+            keep = x0 == y0 && x1 == y1;
+        }
+        if (keep) out_dims_mapping[lead_out] = d;
+        else in_after[lead_in] = -1;
+    }
+    return RTP_OK;
+}
+
+}  // extern "C"

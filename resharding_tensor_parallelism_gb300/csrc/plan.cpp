@@ -1,0 +1,262 @@
+// Reshard planning ("boxing"): from a source layout and a destination layout,
+// the list of rectangular regions to move. Every destination piece is the
+// union of its intersections with the source pieces (OneFlow page: boxing
+// inserted between mismatched SBPs; ONNX page: execution semantics, "reshard
+// inputs"). Partial sources (OneFlow SBP definition of partial sum) become
+// regions read from every member of a partial group and summed.
+//
+// Each source byte is planned to be read once per destination group of equal
+// pieces: broadcast destinations with the same box are written from the same
+// registers (one read, many writes), which keeps all-gather and all-reduce
+// traffic at its algorithmic minimum.
+#include <algorithm>
+#include <cstring>
+#include <map>
+
+#include "rtp_internal.h"
+
+namespace rtp {
+
+namespace {
+
+struct SrcGroup {
+    Box box;
+    std::vector<std::pair<int64_t, int>> members;  // (partial index, rank)
+};
+
+struct DstGroup {
+    Box box;
+    std::vector<int> ranks;
+};
+
+bool same_box(int ndim, const Box& a, const Box& b)
+{
+    for (int d = 0; d < ndim; ++d)
+        if (a.lo[d] != b.lo[d] || a.hi[d] != b.hi[d]) return false;
+    return true;
+}
+
+void row_major_strides(int ndim, const Box& b, int64_t* st)
+{
+    int64_t s = 1;
+    for (int a = ndim - 1; a >= 0; --a) {
+        st[a] = s;
+        s *= b.hi[a] - b.lo[a];
+    }
+}
+
+// Region [lo, hi) of the logical tensor, read from pieces with box sbox and
+// written to pieces with box dbox.
+int make_task(int ndim, const int64_t* lo, const int64_t* hi, const Box& sbox, const Box& dbox, PlanTask* t,
+              int64_t* soff, int64_t* doff)
+{
+    int64_t e[RTP_MAX_NDIM] = {}, ss[RTP_MAX_NDIM] = {}, ds[RTP_MAX_NDIM] = {};
+    row_major_strides(ndim, sbox, ss);
+    row_major_strides(ndim, dbox, ds);
+    *soff = 0;
+    *doff = 0;
+    for (int a = 0; a < ndim; ++a) {
+        e[a] = hi[a] - lo[a];
+        *soff += (lo[a] - sbox.lo[a]) * ss[a];
+        *doff += (lo[a] - dbox.lo[a]) * ds[a];
+    }
+    // innermost run: the last axis, grown outward while the region covers
+    // whole rows of both pieces
+    int a = ndim - 1;
+    int64_t cols = e[a];
+    while (a > 0 && ss[a - 1] == cols && ds[a - 1] == cols) {
+        --a;
+        cols *= e[a];
+    }
+    // outer dims, unit extents dropped, contiguous neighbours merged
+    int64_t oe[RTP_MAX_NDIM], os[RTP_MAX_NDIM], od[RTP_MAX_NDIM];
+    int n = 0;
+    for (int b = 0; b < a; ++b) {
+        if (e[b] == 1) continue;
+        if (n > 0 && os[n - 1] == e[b] * ss[b] && od[n - 1] == e[b] * ds[b]) {
+            oe[n - 1] *= e[b];
+            os[n - 1] = ss[b];
+            od[n - 1] = ds[b];
+            continue;
+        }
+        oe[n] = e[b];
+        os[n] = ss[b];
+        od[n] = ds[b];
+        ++n;
+    }
+    if (n > kMaxOuter) return fail(RTP_EUNSUPPORTED, "reshard: region needs %d outer dims (max %d)", n, kMaxOuter);
+    t->cols = cols;
+    t->n_outer = n;
+    t->rows = 1;
+    for (int k = 0; k < n; ++k) {
+        t->ext[k] = oe[k];
+        t->sstr[k] = os[k];
+        t->dstr[k] = od[k];
+        t->rows *= oe[k];
+    }
+    return RTP_OK;
+}
+
+}  // namespace
+
+int plan_reshard(int ndim, const int64_t* shape, const rtp_spec& src, const rtp_spec& dst,
+                 std::vector<PlanTask>* tasks)
+{
+    tasks->clear();
+    int64_t sc[RTP_MAX_RANKS * RTP_MAX_MESH_NDIM], dc[RTP_MAX_RANKS * RTP_MAX_MESH_NDIM];
+    rank_coords(src, sc);
+    rank_coords(dst, dc);
+    int64_t nsrc = num_ranks(src), ndst = num_ranks(dst);
+
+    // Source pieces grouped by box; within a group, one member per partial index.
+    std::vector<SrcGroup> sg;
+    for (int r = 0; r < nsrc; ++r) {
+        Box b = rank_box(ndim, shape, src, sc + r * RTP_MAX_MESH_NDIM);
+        if (!b.b_rep || box_volume(ndim, b) == 0) continue;
+        auto it = std::find_if(sg.begin(), sg.end(), [&](const SrcGroup& g) { return same_box(ndim, g.box, b); });
+        if (it == sg.end()) {
+            sg.push_back(SrcGroup{b, {}});
+            it = sg.end() - 1;
+        }
+        it->members.emplace_back(b.pidx, r);
+    }
+    for (auto& g : sg) std::sort(g.members.begin(), g.members.end());
+
+    // Destination pieces grouped by box and by whether they hold values.
+    std::vector<DstGroup> dval, dzero;
+    for (int r = 0; r < ndst; ++r) {
+        Box b = rank_box(ndim, shape, dst, dc + r * RTP_MAX_MESH_NDIM);
+        if (box_volume(ndim, b) == 0) continue;
+        auto& list = b.holds_value ? dval : dzero;
+        auto it = std::find_if(list.begin(), list.end(), [&](const DstGroup& g) { return same_box(ndim, g.box, b); });
+        if (it == list.end()) {
+            list.push_back(DstGroup{b, {}});
+            it = list.end() - 1;
+        }
+        it->ranks.push_back(r);
+    }
+
+    for (const auto& dg : dval) {
+        for (const auto& g : sg) {
+            int64_t lo[RTP_MAX_NDIM], hi[RTP_MAX_NDIM];
+            bool empty = false;
+            for (int a = 0; a < ndim; ++a) {
+                lo[a] = std::max(dg.box.lo[a], g.box.lo[a]);
+                hi[a] = std::min(dg.box.hi[a], g.box.hi[a]);
+                if (hi[a] <= lo[a]) empty = true;
+            }
+            if (empty) continue;
+            PlanTask t;
+            int64_t so, dof;
+            int st = make_task(ndim, lo, hi, g.box, dg.box, &t, &so, &dof);
+            if (st) return st;
+            for (auto& m : g.members) t.src.push_back(Ref{m.second, so});
+            for (int r : dg.ranks) t.dst.push_back(Ref{r, dof});
+            tasks->push_back(std::move(t));
+        }
+    }
+    for (const auto& dg : dzero) {
+        PlanTask t;
+        int64_t so, dof;
+        int st = make_task(ndim, dg.box.lo, dg.box.hi, dg.box, dg.box, &t, &so, &dof);
+        if (st) return st;
+        for (int r : dg.ranks) t.dst.push_back(Ref{r, dof});
+        tasks->push_back(std::move(t));
+    }
+    return RTP_OK;
+}
+
+}  // namespace rtp
+
+using namespace rtp;
+
+namespace {
+
+int element_size(int dtype) { return dtype == RTP_F32 ? 4 : 2; }
+
+int check_common(const char* fn, int dtype, int ndim, const int64_t* shape)
+{
+    if (dtype != RTP_F32 && dtype != RTP_BF16) return fail(RTP_EINVAL, "%s: unknown dtype %d", fn, dtype);
+    if (!shape) return fail(RTP_EINVAL, "%s: shape is NULL", fn);
+    if (ndim < 1 || ndim > RTP_MAX_NDIM) return fail(RTP_EINVAL, "%s: ndim %d outside [1, %d]", fn, ndim, RTP_MAX_NDIM);
+    for (int a = 0; a < ndim; ++a)
+        if (shape[a] < 0) return fail(RTP_ESHAPE, "%s: extent %d is negative", fn, a);
+    return RTP_OK;
+}
+
+int check_pointers(const char* fn, const char* which, const std::vector<PlanTask>& tasks, const void* const* bufs,
+                   bool src, int es)
+{
+    for (const auto& t : tasks)
+        for (const auto& r : (src ? t.src : t.dst)) {
+            const void* p = bufs[r.rank];
+            if (!p) return fail(RTP_EINVAL, "%s: %s buffer of rank %d is NULL", fn, which, r.rank);
+            if ((uintptr_t)p % es) return fail(RTP_EINVAL, "%s: %s buffer of rank %d is not %d-byte aligned", fn, which, r.rank, es);
+        }
+    return RTP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int rtp_reshard(rtp_dtype dtype, int ndim, const int64_t* shape, const void* const* src_dev, const rtp_spec* src,
+                void* const* dst_dev, const rtp_spec* dst, rtp_stream stream)
+{
+    const char* fn = "rtp_reshard";
+    int st = check_common(fn, dtype, ndim, shape);
+    if (st) return st;
+    if (!src || !dst || !src_dev || !dst_dev) return fail(RTP_EINVAL, "%s: NULL spec or buffer array", fn);
+    if ((st = check_spec(ndim, *src, "rtp_reshard (src)"))) return st;
+    if ((st = check_spec(ndim, *dst, "rtp_reshard (dst)"))) return st;
+    std::vector<PlanTask> tasks;
+    if ((st = plan_reshard(ndim, shape, *src, *dst, &tasks))) return st;
+    int es = element_size(dtype);
+    if ((st = check_pointers(fn, "source", tasks, src_dev, true, es))) return st;
+    if ((st = check_pointers(fn, "destination", tasks, (const void* const*)dst_dev, false, es))) return st;
+    return launch_tasks(dtype, tasks, src_dev, dst_dev, stream, nullptr);
+}
+
+int rtp_shard(rtp_dtype dtype, int ndim, const int64_t* shape, const void* full, const rtp_spec* spec,
+              void* const* shard_dev, rtp_stream stream)
+{
+    const char* fn = "rtp_shard";
+    int st = check_common(fn, dtype, ndim, shape);
+    if (st) return st;
+    if (!spec || !shard_dev) return fail(RTP_EINVAL, "%s: NULL spec or buffer array", fn);
+    if ((st = check_spec(ndim, *spec, fn))) return st;
+    rtp_spec whole = whole_tensor_spec();
+    std::vector<PlanTask> tasks;
+    if ((st = plan_reshard(ndim, shape, whole, *spec, &tasks))) return st;
+    const void* srcs[1] = {full};
+    int es = element_size(dtype);
+    if ((st = check_pointers(fn, "full-tensor", tasks, srcs, true, es))) return st;
+    if ((st = check_pointers(fn, "shard", tasks, (const void* const*)shard_dev, false, es))) return st;
+    return launch_tasks(dtype, tasks, srcs, shard_dev, stream, nullptr);
+}
+
+int rtp_reshard_cost(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_spec* src, const rtp_spec* dst,
+                     int64_t* bytes_read, int64_t* bytes_written, int32_t* n_tasks, int32_t* n_launches)
+{
+    const char* fn = "rtp_reshard_cost";
+    int st = check_common(fn, dtype, ndim, shape);
+    if (st) return st;
+    if (!src || !dst) return fail(RTP_EINVAL, "%s: NULL spec", fn);
+    if ((st = check_spec(ndim, *src, "rtp_reshard_cost (src)"))) return st;
+    if ((st = check_spec(ndim, *dst, "rtp_reshard_cost (dst)"))) return st;
+    std::vector<PlanTask> tasks;
+    if ((st = plan_reshard(ndim, shape, *src, *dst, &tasks))) return st;
+    int64_t rd = 0, wr = 0, es = element_size(dtype);
+    for (const auto& t : tasks) {
+        int64_t v = t.rows * t.cols * es;
+        rd += v * (int64_t)t.src.size();
+        wr += v * (int64_t)t.dst.size();
+    }
+    if (bytes_read) *bytes_read = rd;
+    if (bytes_written) *bytes_written = wr;
+    if (n_tasks) *n_tasks = (int32_t)tasks.size();
+    if (n_launches) *n_launches = count_launches(tasks);
+    return RTP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// Internal declarations of the rtp library (host side). Not installed.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "rtp.h"
+
+namespace rtp {
+
+// ---- errors ------------------------------------------------------------------
+// Records a message for rtp_last_error() on this thread and returns `status`.
+int fail(int status, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+void clear_error();
+
+// ---- spec geometry -------------------------------------------------------------
+int64_t num_ranks(const rtp_spec& s);
+// RTP_OK or an error (message recorded) if the spec cannot describe a tensor of rank ndim.
+int check_spec(int ndim, const rtp_spec& s, const char* what);
+// Mesh coordinates of every rank: coords[r * RTP_MAX_MESH_NDIM + d].
+void rank_coords(const rtp_spec& s, int64_t* coords);
+
+struct Box {
+    int64_t lo[RTP_MAX_NDIM];
+    int64_t hi[RTP_MAX_NDIM];
+    bool holds_value;  // false: zero-filled member of a partial group
+    bool b_rep;        // coordinate 0 on every broadcast mesh dim
+    int64_t pidx;      // index of the partial coordinates (row-major), 0 if no P dim
+};
+// Piece of rank r (caller validated the spec).
+Box rank_box(int ndim, const int64_t* shape, const rtp_spec& s, const int64_t* coords_of_r);
+int64_t box_volume(int ndim, const Box& b);
+
+// ---- copy plan -------------------------------------------------------------------
+// One rectangular region moved from n_src source pieces (summed when n_src > 1,
+// zeros when n_src == 0) to n_dst destination pieces. After merging, the region
+// is rows x cols: `cols` consecutive elements in every buffer, rows indexed by
+// the mixed radix ext[0..n_outer) with per-buffer element strides.
+constexpr int kMaxOuter = 7;
+struct Ref {
+    int rank;        // buffer index
+    int64_t offset;  // element offset of the region's first element
+};
+struct PlanTask {
+    int64_t rows = 1, cols = 1;
+    int n_outer = 0;
+    int64_t ext[kMaxOuter] = {};
+    int64_t sstr[kMaxOuter] = {};
+    int64_t dstr[kMaxOuter] = {};
+    std::vector<Ref> src;
+    std::vector<Ref> dst;
+};
+// Plans moving a tensor laid out by `src` into the layout `dst`.
+int plan_reshard(int ndim, const int64_t* shape, const rtp_spec& src, const rtp_spec& dst,
+                 std::vector<PlanTask>* tasks);
+
+// The single-rank, broadcast spec of an unsharded tensor.
+rtp_spec whole_tensor_spec();
+
+// ---- launches (boxing.cu) --------------------------------------------------------------
+// Executes planned tasks on `stream`; src/dst buffer arrays are indexed by Ref::rank.
+int launch_tasks(int dtype, const std::vector<PlanTask>& tasks, const void* const* src, void* const* dst,
+                 void* stream, int* n_launches_out);
+// Number of launches the tasks need (host only).
+int count_launches(const std::vector<PlanTask>& tasks);
+
+}  // namespace rtp

@@ -1,0 +1,635 @@
+// Megatron 1D tensor-parallel MLP on a virtual mesh of P ranks held in one GPU
+// (ColossalAI "1D tensor parallelism" page, sections 2 and 2.1; GELU between
+// the GEMMs from the Domino page, forward section).
+//
+//   column-parallel:  Y_i = GELU(X A_i)          X [M,K], A_i [K,F/P]
+//   row-parallel:     Z   = sum_i Y_i B_i        Y_i [M,F/P], B_i [F/P,N]
+//
+// Both GEMMs run on one persistent, warp-specialised tcgen05 kernel:
+//   warp 0     TMA producer: 128x64 tiles of the K-major operand (X or Y_i)
+//              and 4 boxes of 64x64 of the N-major operand (A_i or B_i), all
+//              128-byte swizzled, into a 4-stage shared-memory ring;
+//   warp 1     one thread issues tcgen05.mma (M=128, N=256, K=16, bf16 in,
+//              float32 accumulate in TMEM); 2 accumulators of 256 columns
+//              let the epilogue of one tile overlap the next tile's K loop;
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator rows, GELU and bf16
+//              rounding (GEMM1) or float32 (GEMM2), stored to global memory.
+// Tiles are walked in groups of 16 M-tiles so that the CTAs running at one
+// time share operand panels in L2.
+//
+// The row-parallel GEMM has two forms. Separate: each rank's Y_i B_i is a
+// float32 partial, and a multi-source kernel sums the partials (the
+// all-reduce of the pages). Fused: the K loop of one output tile walks every
+// rank's K range in turn, so the sum of ranks happens in the TMEM accumulator
+// and no partial is ever written.
+//
+// The Domino schedule (Domino page, row split of X and column split of B)
+// cuts X into row chunks (and B_i into column blocks): the reduction of
+// chunk c runs on a second stream while the GEMMs of chunk c+1 run.
+//
+// Every mbarrier wait is bounded: after a few seconds without progress the
+// waiting thread records an error code in a device word, raises a CTA-wide
+// abort flag and every role leaves its loop; the CTA then frees its TMEM and
+// exits. rtp_device_error() reads and clears that word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <vector>
+
+#include "rtp_internal.h"
+
+namespace rtp {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KB
+constexpr uint32_t B_SUB = 64 * BK * 2;    // one 64(N) x 64(K) box, 8 KB
+constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr int GROUP_M = 16;
+constexpr int MAX_GROUPS = 8;
+constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /* barriers */ + 1024 /* alignment */;
+constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;
+
+enum : uint32_t { ERR_PRODUCER = 1, ERR_MMA_STAGE = 2, ERR_MMA_ACC = 3, ERR_EPILOGUE = 4 };
+enum { EPI_GELU_BF16 = 0, EPI_F32 = 1 };
+
+// Instruction descriptor of tcgen05.mma kind::f16: D float32 (bits 4-5 = 1),
+// A and B bf16 (bits 7-9 = 1, 10-12 = 1), A K-major (bit 15 = 0), B N-major
+// (bit 16 = 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
+                           ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+struct GemmArgs {
+    CUtensorMap ta[MAX_GROUPS];  // K-major operand of each group: rows x K
+    CUtensorMap tb[MAX_GROUPS];  // N-major operand of each group: K x N
+    void* out[MAX_GROUPS];       // output of each group (out[0] when fused)
+    int64_t ldo;                 // output row stride, elements
+    int32_t groups, fused, epi;
+    int32_t m_tiles, n_tiles, kb_per_group;
+    int32_t m0, n0;              // window of the problem (Domino chunk / column block)
+    int32_t total_tiles;
+};
+
+__device__ unsigned int g_tp_error;
+
+// ---- PTX wrappers ------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait. False: this wait gave up, or another role already did.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, uint32_t code)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > WAIT_LIMIT_NS) {
+                *abort_flag = 1;
+                atomicCAS(&g_tp_error, 0u, code);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait used only while tearing down after an abort: it ignores the
+// abort flag so that copies and MMAs already in flight can land.
+__device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > 200000000ull) break;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor (tcgen05): start >> 4 (bits 0-13), leading
+// byte offset >> 4 (16-29), stride byte offset >> 4 (32-45), version 1 (46-48),
+// base offset 0, swizzle mode 2 = 128-byte swizzle (61-63).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(IDESC), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tile_coords(const GemmArgs& a, int tile, int& g, int& mt, int& nt)
+{
+    const int per_group = a.m_tiles * a.n_tiles;
+    g = a.fused ? 0 : tile / per_group;
+    const int r = tile - (a.fused ? 0 : g * per_group);
+    const int span = GROUP_M * a.n_tiles;
+    const int first_m = (r / span) * GROUP_M;
+    const int rows = min(a.m_tiles - first_m, GROUP_M);
+    const int w = r % span;
+    mt = first_m + w % rows;
+    nt = w / rows;
+}
+
+__device__ __forceinline__ float gelu(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752440f)); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+
+// ---- the kernel ----------------------------------------------------------------------
+
+__global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_constant__ GemmArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    // bars: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(STAGES + s); };
+    auto acc_full = [&](int x) { return bar0 + 8u * (uint32_t)(2 * STAGES + x); };
+    auto acc_empty = [&](int x) { return bar0 + 8u * (uint32_t)(2 * STAGES + 2 + x); };
+    const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(acc_full(x), 1);
+            mbar_init(acc_empty(x), 4);  // one arrival per epilogue warp
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        for (int g = 0; g < a.groups; ++g) {
+            prefetch_map(&a.ta[g]);
+            prefetch_map(&a.tb[g]);
+        }
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int kbs = a.fused ? a.groups * a.kb_per_group : a.kb_per_group;
+
+    if (warp == 0) {
+        // ---------------- TMA producer (one lane) ----------------
+        if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued = 0, issued_parity = 0;  // per stage: last load and its phase parity
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < a.total_tiles; tile += gridDim.x) {
+            int g, mt, nt;
+            tile_coords(a, tile, g, mt, nt);
+            const int row = a.m0 + mt * BM, col = a.n0 + nt * BN;
+            for (int kb = 0; kb < kbs; ++kb) {
+                if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, ERR_PRODUCER)) {
+                    ok = false;
+                    break;
+                }
+                const int gg = a.fused ? kb / a.kb_per_group : g;
+                const int kk = a.fused ? kb - gg * a.kb_per_group : kb;
+                const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                const uint32_t sb = sa + A_BYTES;
+                mbar_expect_tx(full_bar(stage), STAGE_BYTES);
+                tma_load_2d(sa, &a.ta[gg], full_bar(stage), kk * BK, row);
+#pragma unroll
+                for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * B_SUB, &a.tb[gg], full_bar(stage), col + 64 * j, kk * BK);
+                issued |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            // let the loads already issued land before the CTA can exit
+            for (int s = 0; s < STAGES; ++s)
+                if ((issued >> s) & 1u) drain_wait(full_bar(s), (issued_parity >> s) & 1u);
+        }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (one lane) ----------------
+        if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < a.total_tiles; tile += gridDim.x) {
+            if (!wait_bar(acc_empty(acc), acc_phase ^ 1u, abort_flag, ERR_MMA_ACC)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            for (int kb = 0; kb < kbs; ++kb) {
+                if (!wait_bar(full_bar(stage), phase, abort_flag, ERR_MMA_STAGE)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k) {
+                    // K-major A: advance 32 bytes (16 bf16) inside the 128-byte swizzle row;
+                    // 8-row groups are 1024 bytes apart.
+                    const uint64_t da = smem_desc(sa + 32u * k, 16u, 1024u);
+                    // N-major B: 16 K-rows = 2 groups of 8 rows of 128 bytes; the four
+                    // 64-wide N boxes are B_SUB bytes apart.
+                    const uint64_t db = smem_desc(sb + 2048u * k, B_SUB, 1024u);
+                    mma_bf16(d_tmem, da, db, (kb > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(empty_bar(stage));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            mma_commit(acc_full(acc));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        if (!ok || *abort_flag) {
+            // MMAs already issued must finish before TMEM is freed
+            mma_commit(drain_bar);
+            drain_wait(drain_bar, 0);
+        }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue ----------------
+        const int quarter = warp & 3;  // TMEM lanes this warp may read
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < a.total_tiles; tile += gridDim.x) {
+            int g, mt, nt;
+            tile_coords(a, tile, g, mt, nt);
+            // one lane waits; the warp follows its verdict so that the
+            // .sync.aligned TMEM loads below always run on a converged warp
+            int ok = 1;
+            if (lane == 0) ok = wait_bar(acc_full(acc), acc_phase, abort_flag, ERR_EPILOGUE) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const int64_t row = a.m0 + mt * BM + quarter * 32 + lane;
+            const int64_t col = a.n0 + nt * BN;
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32cols(taddr + 32u * c, r);
+                tmem_ld_wait();
+                if (a.epi == EPI_GELU_BF16) {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out[g]) + row * a.ldo + col + 32 * c);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 v;
+                        v.x = pack_bf16(gelu(__uint_as_float(r[8 * q + 0])), gelu(__uint_as_float(r[8 * q + 1])));
+                        v.y = pack_bf16(gelu(__uint_as_float(r[8 * q + 2])), gelu(__uint_as_float(r[8 * q + 3])));
+                        v.z = pack_bf16(gelu(__uint_as_float(r[8 * q + 4])), gelu(__uint_as_float(r[8 * q + 5])));
+                        v.w = pack_bf16(gelu(__uint_as_float(r[8 * q + 6])), gelu(__uint_as_float(r[8 * q + 7])));
+                        dst[q] = v;
+                    }
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out[g]) + row * a.ldo + col + 32 * c);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        __stcs(dst + q, make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
+                                                    __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty(acc));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+}
+
+// ---- host side --------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2D bf16 tensor map over a row-major [rows, cols] matrix, box [box_rows, 64],
+// 128-byte swizzle (64 bf16 per box row).
+int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return fail(RTP_ECUDA, "tp_mlp: cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(cols * 2)};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(RTP_ECUDA, "tp_mlp: cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return RTP_OK;
+}
+
+int sm_count_now()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+int launch_gemm(GemmArgs& args, cudaStream_t stream)
+{
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(tp_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (e != cudaSuccess) return fail(RTP_ECUDA, "tp_mlp: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        configured[dev] = true;
+    }
+    const int sms = sm_count_now();
+    if (sms <= 0) return fail(RTP_ECUDA, "tp_mlp: no CUDA device");
+    args.total_tiles = (args.fused ? 1 : args.groups) * args.m_tiles * args.n_tiles;
+    const int grid = args.total_tiles < sms ? args.total_tiles : sms;
+    if (grid <= 0) return RTP_OK;
+    tp_gemm_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(args);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(RTP_ECUDA, "tp_mlp: GEMM launch failed: %s", cudaGetErrorString(e));
+    return RTP_OK;
+}
+
+struct Events {
+    cudaEvent_t fwd = nullptr, back = nullptr;
+};
+
+int events(Events** out)
+{
+    static Events ev[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(RTP_ECUDA, "tp_mlp: no CUDA device");
+    Events& e = ev[dev];
+    if (!e.fwd) {
+        if (cudaEventCreateWithFlags(&e.fwd, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&e.back, cudaEventDisableTiming) != cudaSuccess)
+            return fail(RTP_ECUDA, "tp_mlp: cudaEventCreate failed");
+    }
+    *out = &e;
+    return RTP_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace
+
+}  // namespace rtp
+
+using namespace rtp;
+
+extern "C" {
+
+int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X, const void* const* A_shards,
+               const void* const* B_shards, void* const* Y, void* const* partials, float* Z, int mode, int chunks,
+               int col_blocks, rtp_stream s0_, rtp_stream s1_)
+{
+    const char* fn = "rtp_tp_mlp";
+    if (P < 1 || P > MAX_GROUPS) return fail(RTP_EUNSUPPORTED, "%s: P = %d outside [1, %d]", fn, P, MAX_GROUPS);
+    if (!X || !A_shards || !B_shards || !Y || !Z) return fail(RTP_EINVAL, "%s: NULL argument", fn);
+    if (mode != 0 && mode != 1) return fail(RTP_EINVAL, "%s: mode %d", fn, mode);
+    if (mode == 0 && !partials) return fail(RTP_EINVAL, "%s: mode 0 needs partial buffers", fn);
+    if (chunks != 1 && chunks != 2 && chunks != 4) return fail(RTP_EINVAL, "%s: chunks %d not in {1,2,4}", fn, chunks);
+    if (col_blocks != 1 && col_blocks != 2) return fail(RTP_EINVAL, "%s: col_blocks %d not in {1,2}", fn, col_blocks);
+    if (mode == 1 && col_blocks != 1) return fail(RTP_EINVAL, "%s: column blocks apply to mode 0", fn);
+    if (M < 0 || K < 1 || F < 1 || N < 1) return fail(RTP_ESHAPE, "%s: sizes M=%lld K=%lld F=%lld N=%lld", fn, (long long)M,
+                                                      (long long)K, (long long)F, (long long)N);
+    if (F % P) return fail(RTP_ESHAPE, "%s: F=%lld is not divisible by P=%d", fn, (long long)F, P);
+    const int64_t Fp = F / P;
+    if (M % chunks || (M / chunks) % BM) return fail(RTP_ESHAPE, "%s: M/chunks must be a multiple of %d", fn, BM);
+    if (K % BK) return fail(RTP_ESHAPE, "%s: K must be a multiple of %d", fn, BK);
+    if (Fp % BN) return fail(RTP_ESHAPE, "%s: F/P must be a multiple of %d", fn, BN);
+    if (N % (BN * col_blocks)) return fail(RTP_ESHAPE, "%s: N must be a multiple of %d", fn, BN * col_blocks);
+    if (M >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 31) || Fp >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31))
+        return fail(RTP_ESHAPE, "%s: extents must stay below 2^31", fn);
+    if (!aligned16(X) || !aligned16(Z)) return fail(RTP_EINVAL, "%s: X and Z must be 16-byte aligned", fn);
+    for (int i = 0; i < P; ++i) {
+        if (!A_shards[i] || !B_shards[i] || !Y[i] || (mode == 0 && !partials[i]))
+            return fail(RTP_EINVAL, "%s: NULL buffer for rank %d", fn, i);
+        if (!aligned16(A_shards[i]) || !aligned16(B_shards[i]) || !aligned16(Y[i]) || (mode == 0 && !aligned16(partials[i])))
+            return fail(RTP_EINVAL, "%s: buffers of rank %d must be 16-byte aligned", fn, i);
+    }
+    if (M == 0) return RTP_OK;
+    cudaStream_t s0 = static_cast<cudaStream_t>(s0_), s1 = static_cast<cudaStream_t>(s1_);
+    const bool two_streams = s1 != s0;
+    Events* ev = nullptr;
+    if (mode == 0 && two_streams) {
+        int st = events(&ev);
+        if (st) return st;
+    }
+    const int64_t Mc = M / chunks;
+    const int64_t Nb = N / col_blocks;
+
+    // GEMM1 arguments (tensor maps shared by every chunk)
+    static thread_local GemmArgs g1, g2;
+    std::memset(&g1, 0, sizeof g1);
+    std::memset(&g2, 0, sizeof g2);
+    int st;
+    for (int i = 0; i < P; ++i) {
+        if ((st = make_map(&g1.ta[i], X, M, K, BM))) return st;
+        if ((st = make_map(&g1.tb[i], A_shards[i], K, Fp, BK))) return st;
+        g1.out[i] = Y[i];
+        if ((st = make_map(&g2.ta[i], Y[i], M, Fp, BM))) return st;
+        if ((st = make_map(&g2.tb[i], B_shards[i], Fp, N, BK))) return st;
+        g2.out[i] = mode == 0 ? partials[i] : (void*)Z;
+    }
+    g1.ldo = Fp;
+    g1.groups = P;
+    g1.fused = 0;
+    g1.epi = EPI_GELU_BF16;
+    g1.m_tiles = (int)(Mc / BM);
+    g1.n_tiles = (int)(Fp / BN);
+    g1.kb_per_group = (int)(K / BK);
+    g1.n0 = 0;
+    g2.ldo = N;
+    g2.groups = P;
+    g2.fused = mode == 1;
+    g2.epi = EPI_F32;
+    g2.m_tiles = (int)(Mc / BM);
+    g2.n_tiles = (int)(Nb / BN);
+    g2.kb_per_group = (int)(Fp / BK);
+
+    for (int c = 0; c < chunks; ++c) {
+        g1.m0 = (int)(c * Mc);
+        if ((st = launch_gemm(g1, s0))) return st;
+        for (int b = 0; b < (mode == 0 ? col_blocks : 1); ++b) {
+            g2.m0 = (int)(c * Mc);
+            g2.n0 = (int)(b * Nb);
+            if ((st = launch_gemm(g2, s0))) return st;
+            if (mode == 1) continue;
+            // sum of the P partials over this window: Z[rows, cols] = sum_i partial_i[rows, cols]
+            PlanTask t;
+            t.cols = Nb;
+            t.rows = Mc;
+            t.n_outer = 1;
+            t.ext[0] = Mc;
+            t.sstr[0] = N;
+            t.dstr[0] = N;
+            if (col_blocks == 1) {  // whole rows: one contiguous run
+                t.cols = Mc * N;
+                t.rows = 1;
+                t.n_outer = 0;
+            }
+            const int64_t off = c * Mc * N + b * Nb;
+            for (int i = 0; i < P; ++i) t.src.push_back(Ref{i, off});
+            t.dst.push_back(Ref{0, off});
+            std::vector<PlanTask> tasks{t};
+            void* zdst[1] = {Z};
+            cudaStream_t rs = s0;
+            if (two_streams) {
+                if (cudaEventRecord(ev->fwd, s0) != cudaSuccess || cudaStreamWaitEvent(s1, ev->fwd, 0) != cudaSuccess)
+                    return fail(RTP_ECUDA, "tp_mlp: event ordering failed");
+                rs = s1;
+            }
+            if ((st = launch_tasks(RTP_F32, tasks, (const void* const*)partials, zdst, rs, nullptr))) return st;
+        }
+    }
+    if (mode == 0 && two_streams) {
+        if (cudaEventRecord(ev->back, s1) != cudaSuccess || cudaStreamWaitEvent(s0, ev->back, 0) != cudaSuccess)
+            return fail(RTP_ECUDA, "tp_mlp: event ordering failed");
+    }
+    return RTP_OK;
+}
+
+int rtp_device_error(rtp_stream stream, uint32_t* code)
+{
+    if (!code) return fail(RTP_EINVAL, "rtp_device_error: NULL argument");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_tp_error, sizeof v, 0, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_tp_error, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return fail(RTP_ECUDA, "rtp_device_error: %s", cudaGetErrorString(cudaGetLastError()));
+    *code = v;
+    return RTP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,183 @@
+"""The C-ABI library loads, exports what include/rtp.h declares, and its
+host-only logic (front-ends, shard geometry, inference, reshape rule, planned
+traffic) agrees with the oracle. No GPU needed: nothing here launches work."""
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import resharding_tensor_parallelism_gb300 as rtp
+from resharding_tensor_parallelism_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    _build.build()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "rtp.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(rtp_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol():
+    names = _declared()
+    assert len(names) >= 13
+    lib = rtp.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+    out = os.popen("nm -D --defined-only %s" % rtp.LIB_PATH).read()
+    for n in names:
+        assert re.search(r"\bT %s\b" % n, out), n
+
+
+def test_version_and_errors():
+    assert "sm_103a" in rtp.version()
+    with pytest.raises(rtp.RtpError) as e:
+        rtp.spec_from_dims_mapping([0, 0], [2])
+    assert e.value.status == -1 and "mesh dim 0" in rtp.last_error()
+    with pytest.raises(rtp.RtpError) as e:
+        rtp.spec_from_onnx(2, [-1, -2], {-1: [0, 1], -2: [2]}, [(0, 2)])
+    assert e.value.status == -3  # unequal groups
+    with pytest.raises(rtp.RtpError):
+        rtp.spec_from_onnx(2, [0, 1, 2], {}, [(0, 2)])  # 2 pieces, 3 devices
+    with pytest.raises(rtp.RtpError):
+        rtp.spec_from_onnx(2, [0, 1], {}, [(2, 2)])  # axis out of range
+    with pytest.raises(rtp.RtpError):
+        rtp.spec_check(2, rtp.spec_nd_sbp((2,), (("S", 2),)))
+    with pytest.raises(rtp.RtpError):
+        rtp.spec_check(2, rtp.spec_nd_sbp((2,), ("B",), (0, 0)))
+    with pytest.raises(rtp.RtpError):
+        rtp.infer_spmd("mk,kn->mz", [[0, -1], [-1, -1]], 1)
+    with pytest.raises(rtp.RtpError):
+        rtp.infer_reshape([2, 3], [0, -1], [7], [2])
+
+
+def _same_layout(spec, lay, shape):
+    for r in range(spec.num_ranks):
+        assert rtp.shard_box(shape, spec, r) == oracle.shard_box(shape, lay, r)
+
+
+def test_front_ends_match_oracle():
+    shape = (5, 7, 3)
+    rng = np.random.default_rng(0)
+    for mesh in [(2,), (3,), (2, 2), (2, 3), (1, 4)]:
+        n = int(np.prod(mesh))
+        for _ in range(20):
+            dm = [-1] * 3
+            for d in range(len(mesh)):
+                if rng.random() < 0.7:
+                    i = int(rng.integers(3))
+                    if dm[i] == -1:
+                        dm[i] = d
+            free = [d for d in range(len(mesh)) if d not in dm]
+            partial = [d for d in free if rng.random() < 0.5]
+            ranks = list(rng.permutation(n))
+            s = rtp.spec_from_dims_mapping(dm, mesh, ranks, partial)
+            L = oracle.layout_from_dims_mapping(dm, mesh, ranks, partial)
+            _same_layout(s, L, shape)
+    cases = [
+        ([0, 1], {}, [(0, 2)]), ([0, 1], {}, [(1, 2)]), ([0, 1, 2, 3], {}, [(0, 2), (1, 2)]),
+        ([-1], {-1: [0, 1]}, []), ([-1, -2], {-1: [0, 1], -2: [2, 3]}, [(0, 2)]),
+        ([-1, -2], {-1: [0, 2], -2: [1, 3]}, [(-1, 2)]), ([3, 1, 0, 2], {}, [(1, 4)]),
+    ]
+    for device, dmap, sd in cases:
+        s = rtp.spec_from_onnx(2, device, dmap, sd)
+        L = oracle.layout_from_onnx(2, device, dmap, sd)
+        _same_layout(s, L, (4, 6))
+        _same_layout(s, L, (3, 5))
+
+
+def test_nd_sbp_geometry_matches_oracle():
+    opts = lambda nd: [("S", a) for a in range(nd)] + ["B", "P"]
+    for shape in [(7,), (5, 4), (3, 1, 9)]:
+        for mesh in [(2,), (4,), (2, 2), (2, 3), (3, 2)]:
+            for ents in itertools.product(opts(len(shape)), repeat=len(mesh)):
+                _same_layout(rtp.spec_nd_sbp(mesh, ents), oracle.Layout(mesh, ents), shape)
+
+
+EINSUMS = ["mk,kn->mn", "mn,mn->mn", "bmk,bkn->bmn", "mn->mn", "mk,k->m", "ij,jk,kl->il", "mn->m"]
+
+
+def test_infer_spmd_matches_oracle():
+    rng = np.random.default_rng(2)
+    for einsum in EINSUMS:
+        ins = einsum.split("->")[0].split(",")
+        for mesh_ndim in (1, 2, 3):
+            for _ in range(60):
+                dms = []
+                for t in ins:
+                    dm = [-1] * len(t)
+                    for d in range(mesh_ndim):
+                        if rng.random() < 0.6:
+                            i = int(rng.integers(len(t)))
+                            if dm[i] == -1:
+                                dm[i] = d
+                    dms.append(dm)
+                assert rtp.infer_spmd(einsum, dms, mesh_ndim) == oracle.infer_spmd(einsum, dms, mesh_ndim), (einsum, dms)
+
+
+def test_infer_spmd_page_examples():
+    assert rtp.infer_spmd("mk,kn->mn", [[0, -1], [-1, 1]], 2)[:3] == ([0, 1], [], [])
+    assert rtp.infer_spmd("mn,mn->mn", [[0, -1], [-1, 0]], 1)[:3] == ([0, -1], [], [1])
+    assert rtp.infer_spmd("mk,kn->mn", [[-1, 0], [0, -1]], 1)[:3] == ([-1, -1], [0], [])
+
+
+def test_infer_reshape_matches_oracle():
+    shapes = {6: [(6,), (2, 3), (3, 2), (1, 6), (6, 1), (2, 1, 3)], 12: [(12,), (2, 6), (6, 2), (3, 4), (2, 2, 3),
+                                                                           (4, 3), (2, 3, 2)]}
+    for total, group in shapes.items():
+        for a in group:
+            for b in group:
+                for mesh in [(2,), (3,), (2, 2)]:
+                    for dm in itertools.product(range(-1, len(mesh)), repeat=len(a)):
+                        used = [d for d in dm if d >= 0]
+                        if len(used) != len(set(used)):
+                            continue
+                        got = rtp.infer_reshape(a, list(dm), b, mesh)
+                        want = oracle.reshape_spmd(a, list(dm), b, mesh)[:2]
+                        assert got == (want[0], want[1]), (a, dm, b, mesh)
+    assert rtp.infer_reshape([2, 3, 4096], [0, -1, -1], [6, 4096], [2]) == ([0, -1, -1], [0, -1])
+    assert rtp.infer_reshape([6144, 4096], [0, -1], [2, 3072, 4096], [2]) == ([0, -1], [0, -1, -1])
+
+
+def _dm(dm, mesh, partial=()):
+    return rtp.spec_from_dims_mapping(dm, mesh, partial=partial)
+
+
+def test_planned_traffic_matches_algorithmic_bytes():
+    """Bytes planned for the resharding sweep on [8,2048,4096] (each source
+    byte read once, every destination byte written)."""
+    shape = (8, 2048, 4096)
+    N = int(np.prod(shape))
+    for es, code in ((4, rtp.F32), (2, rtp.BF16)):
+        m1, m2 = (8,), (2, 4)
+        cases = [
+            (_dm([0, -1, -1], m1), _dm([-1, -1, 0], m1), 2),
+            (_dm([-1, -1, 0], m1), _dm([-1, 0, -1], m1), 2),
+            (_dm([0, -1, 1], (1, 8)), _dm([-1, -1, -1], (1, 8)), 9),
+            (_dm([-1, -1, -1], m1, [0]), _dm([-1, -1, -1], m1), 16),
+            (_dm([-1, -1, -1], m1, [0]), _dm([-1, -1, 0], m1), 9),
+            (_dm([-1, -1, -1], m1), _dm([0, -1, -1], m1), 2),
+            (_dm([0, -1, -1], m2), _dm([-1, -1, 0], m2), 5),
+            (_dm([-1, -1, 0], m2), _dm([-1, 0, -1], m2), 5),
+            (_dm([0, -1, 1], m2), _dm([-1, -1, -1], m2), 9),
+            (_dm([-1, -1, -1], m2, [0, 1]), _dm([-1, -1, -1], m2), 16),
+            (rtp.spec_nd_sbp(m2, ("P", "P")), rtp.spec_nd_sbp(m2, (("S", 2), ("S", 2))), 9),
+            (rtp.spec_nd_sbp(m2, ("B", "B")), rtp.spec_nd_sbp(m2, (("S", 0), ("S", 0))), 2),
+        ]
+        for src, dst, mult in cases:
+            rd, wr, nt, nl = rtp.reshard_cost(code, shape, src, dst)
+            assert rd + wr == mult * N * es, (src, dst, rd, wr)
+            assert nl == 1
+    # the uneven configuration
+    shape = (12289, 6143)
+    N = 12289 * 6143
+    s01 = rtp.spec_nd_sbp((2, 2), (("S", 0), ("S", 1)))
+    assert sum(rtp.reshard_cost(rtp.F32, shape, s01, rtp.spec_nd_sbp((2, 2), (("S", 1), ("S", 0))))[:2]) == 2 * N * 4
+    assert sum(rtp.reshard_cost(rtp.F32, shape, s01, rtp.spec_nd_sbp((2, 2), ("B", ("S", 1))))[:2]) == 3 * N * 4
