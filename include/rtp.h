@@ -223,10 +223,12 @@ int rtp_infer_reshape(int in_ndim, const int64_t* in_shape, const int32_t* in_di
  *   s0, s1    streams; all work is ordered after prior work on s0 and the
  *             call's completion is ordered on s0 (s1 is joined back)
  * Requirements (else RTP_ESHAPE, like the ValueError on out_features %
- * tp_size in ColossalAI's Linear1D_Col): F % P == 0, M % chunks == 0,
- * M/chunks % 128 == 0, (F/P) % 256 == 0, K % 64 == 0, (F/P) % 64 == 0,
- * N % (256 * col_blocks) == 0; all pointers 16-byte aligned.
- * The first call on a device builds its kernels' tensor maps; no allocation.
+ * tp_size in ColossalAI's Linear1D_Col): F % P == 0, M % chunks == 0, K, F/P
+ * and N / col_blocks multiples of 8 (16-byte rows); P <= 8 (else
+ * RTP_EUNSUPPORTED); all pointers 16-byte aligned (else RTP_EINVAL).
+ * Errors leave nothing launched. The kernels allocate nothing; the first call
+ * on a device sets the GEMM kernel's shared-memory limit and creates two
+ * events used to order s0 and s1.
  */
 int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X, const void* const* A_shards,
                const void* const* B_shards, void* const* Y, void* const* partials, float* Z, int mode, int chunks,

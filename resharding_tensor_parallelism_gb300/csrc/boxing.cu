@@ -5,9 +5,11 @@
 //   * the task table travels in the kernel parameters (up to ~26 KB per
 //     launch, __grid_constant__), so no device memory is allocated or copied
 //     per call and the launch can be captured in a CUDA graph;
-//   * a persistent grid (8 blocks of 256 threads per SM, a multiple of the SM
-//     count) walks ~32 KB chunks of work; long rows are cut into segments
-//     that a whole block streams, short rows are handed one per warp;
+//   * a persistent grid (4 blocks of 256 threads per SM, a multiple of the SM
+//     count) walks ~32 KB chunks: a chunk is a segment of one long row or a
+//     group of up to 256 short rows; the block stages each row's offsets in
+//     shared memory once and spreads the (row, vector) items over its threads,
+//     so every thread keeps several loads in flight even for 1 KB rows;
 //   * loads and stores are 16-byte vectors whenever every pointer, stride and
 //     run length allows it (else 8, 4 or 2 bytes), with streaming cache hints
 //     since every byte is touched once;
@@ -28,9 +30,7 @@ namespace rtp {
 namespace {
 
 constexpr int kBlock = 256;
-constexpr int kWarps = kBlock / 32;
 constexpr int kUnroll = 4;
-constexpr int kBlocksPerSm = 8;
 constexpr int64_t kChunkBytes = 32 * 1024;
 constexpr int kMaxTasks = 96;
 constexpr int kMaxPtrs = 640;
@@ -38,9 +38,8 @@ constexpr int kMaxPtrs = 640;
 struct KTask {
     int64_t chunk_begin;  // first chunk index of this task within the launch
     int64_t rows, cols;   // region: rows runs of cols contiguous elements
-    int64_t seg, nseg;    // block mode: elements per segment, segments per row
-    int64_t rpc;          // warp mode: rows per chunk
-    int32_t mode;         // 1: block streams one row segment; 0: one row per warp
+    int64_t seg, nseg;    // column segment (elements) and segments per row
+    int32_t rpc;          // rows per chunk (1 when rows are cut into segments)
     int32_t vec;          // bytes per vector access
     int32_t n_outer, n_src, n_dst, ptr0;
     int32_t ext[kMaxOuter];
@@ -109,153 +108,136 @@ __device__ __forceinline__ void row_offsets(const KTask& t, int64_t row, int64_t
     }
 }
 
-// One contiguous run of nvec vectors: source(s) at element offset so, every
-// destination at element offset dof. `lane`/`stride` split it among threads.
-template <int VB>
-__device__ __forceinline__ void run_copy(const KParams& p, const KTask& t, int es, int64_t so, int64_t dof,
-                                         int64_t nvec, int lane, int stride)
+// jj = q * nv + r with 0 <= r < nv, for jj < 2^24: a float estimate, then one correction.
+__device__ __forceinline__ void divmod(int jj, int nv, float inv, int& q, int& r)
 {
-    using V = typename Raw<VB>::T;
-    const V* s = reinterpret_cast<const V*>(static_cast<const char*>(p.ptrs[t.ptr0]) + so * es);
-    const int nd = t.n_dst;
-    const void* const* dp = p.ptrs + t.ptr0 + 1;
-    int64_t i = lane;
-    for (; i + (int64_t)(kUnroll - 1) * stride < nvec; i += (int64_t)kUnroll * stride) {
-        V v[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) v[u] = __ldcs(s + i + u * stride);
-        for (int j = 0; j < nd; ++j) {
-            V* d = reinterpret_cast<V*>(static_cast<char*>(const_cast<void*>(dp[j])) + dof * es);
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) __stcs(d + i + u * stride, v[u]);
-        }
-    }
-    for (; i < nvec; i += stride) {
-        V v = __ldcs(s + i);
-        for (int j = 0; j < nd; ++j) {
-            V* d = reinterpret_cast<V*>(static_cast<char*>(const_cast<void*>(dp[j])) + dof * es);
-            __stcs(d + i, v);
-        }
+    q = (int)((float)jj * inv);
+    r = jj - q * nv;
+    if (r < 0) {
+        --q;
+        r += nv;
+    } else if (r >= nv) {
+        ++q;
+        r -= nv;
     }
 }
 
-template <int VB>
-__device__ __forceinline__ void run_zero(const KParams& p, const KTask& t, int es, int64_t dof, int64_t nvec,
-                                         int lane, int stride)
+// One chunk: nr rows (element offsets of each row's first element in s_off /
+// d_off, relative to the task's buffers) of nv vectors each. Items (row,
+// vector) are spread over the block, U per thread per pass. ES: element size.
+template <int VB, int ES, bool SUM>
+__device__ __forceinline__ void run_chunk(const KParams& p, const KTask& t, int nr, int nv, const int64_t* s_off,
+                                          const int64_t* d_off)
 {
     using V = typename Raw<VB>::T;
-    Lanes<VB> z;
-#pragma unroll
-    for (int k = 0; k < VB / 2; ++k) z.h[k] = 0;
-    const void* const* dp = p.ptrs + t.ptr0;
-    for (int j = 0; j < t.n_dst; ++j) {
-        V* d = reinterpret_cast<V*>(static_cast<char*>(const_cast<void*>(dp[j])) + dof * es);
-        for (int64_t i = lane; i < nvec; i += stride) __stcs(d + i, z.v);
-    }
-}
-
-// Sum of n_src sources. ES: element size (4 = float32, 2 = bf16).
-template <int VB, int ES>
-__device__ __forceinline__ void run_sum(const KParams& p, const KTask& t, int64_t so, int64_t dof, int64_t nvec,
-                                        int lane, int stride)
-{
-    using V = typename Raw<VB>::T;
-    constexpr int NE = VB / ES;  // elements per vector
+    constexpr int U = SUM ? 2 : 4;
+    const int total = nr * nv;
+    const float inv = 1.0f / (float)nv;
     const int ns = t.n_src, nd = t.n_dst;
     const void* const* sp = p.ptrs + t.ptr0;
     const void* const* dp = sp + ns;
-    for (int64_t i0 = lane; i0 < nvec; i0 += (int64_t)kUnroll * stride) {
-        float acc[kUnroll][NE];
-        bool live[kUnroll];
+    for (int j0 = threadIdx.x; j0 < total; j0 += kBlock * U) {
+        int q[U], r[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            live[u] = i0 + (int64_t)u * stride < nvec;
-#pragma unroll
-            for (int e = 0; e < NE; ++e) acc[u][e] = 0.f;
+        for (int u = 0; u < U; ++u) {
+            const int jj = j0 + u * kBlock;
+            q[u] = 0;
+            r[u] = -1;  // r < 0 marks a dead item
+            if (jj < total) divmod(jj, nv, inv, q[u], r[u]);
         }
-        for (int j = 0; j < ns; ++j) {
-            const V* s = reinterpret_cast<const V*>(static_cast<const char*>(sp[j]) + so * ES);
-            Lanes<VB> in[kUnroll];
+        auto saddr = [&](const void* base, int u) {
+            return reinterpret_cast<const V*>(static_cast<const char*>(base) + s_off[q[u]] * ES) + r[u];
+        };
+        auto daddr = [&](const void* base, int u) {
+            return reinterpret_cast<V*>(static_cast<char*>(const_cast<void*>(base)) + d_off[q[u]] * ES) + r[u];
+        };
+        if (ns == 0) {
+            Lanes<VB> z;
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u)
-                if (live[u]) in[u].v = __ldcs(s + i0 + u * stride);
+            for (int k = 0; k < VB / 2; ++k) z.h[k] = 0;
+            for (int j = 0; j < nd; ++j)
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
+                for (int u = 0; u < U; ++u)
+                    if (r[u] >= 0) __stcs(daddr(dp[j], u), z.v);
+        } else if (!SUM || ns == 1) {
+            V x[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (r[u] >= 0) x[u] = __ldcs(saddr(sp[0], u));
+            for (int j = 0; j < nd; ++j)
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (r[u] >= 0) __stcs(daddr(dp[j], u), x[u]);
+        } else if constexpr (SUM) {
+            constexpr int NE = VB / ES;  // elements per vector
+            float acc[U][NE];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int e = 0; e < NE; ++e) acc[u][e] = 0.f;
+#pragma unroll 4
+            for (int j = 0; j < ns; ++j) {
+                Lanes<VB> in[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (r[u] >= 0) in[u].v = __ldcs(saddr(sp[j], u));
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int e = 0; e < NE; ++e) {
+                        float x;
+                        if constexpr (ES == 4) x = __uint_as_float(in[u].w[e]);
+                        else x = __uint_as_float((uint32_t)in[u].h[e] << 16);
+                        acc[u][e] = j == 0 ? x : acc[u][e] + x;
+                    }
+            }
+            Lanes<VB> out[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
 #pragma unroll
                 for (int e = 0; e < NE; ++e) {
-                    float x;
-                    if (ES == 4) x = __uint_as_float(in[u].w[e]);
-                    else x = __uint_as_float((uint32_t)in[u].h[e] << 16);
-                    acc[u][e] = j == 0 ? x : acc[u][e] + x;
+                    if constexpr (ES == 4) out[u].w[e] = __float_as_uint(acc[u][e]);
+                    else out[u].h[e] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[u][e]));
                 }
-            }
-        }
-        Lanes<VB> out[kUnroll];
+            for (int j = 0; j < nd; ++j)
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-#pragma unroll
-            for (int e = 0; e < NE; ++e) {
-                if (ES == 4) out[u].w[e] = __float_as_uint(acc[u][e]);
-                else out[u].h[e] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[u][e]));
-            }
-        for (int j = 0; j < nd; ++j) {
-            V* d = reinterpret_cast<V*>(static_cast<char*>(const_cast<void*>(dp[j])) + dof * ES);
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u)
-                if (live[u]) __stcs(d + i0 + u * stride, out[u].v);
+                for (int u = 0; u < U; ++u)
+                    if (r[u] >= 0) __stcs(daddr(dp[j], u), out[u].v);
         }
     }
 }
 
-template <int VB>
-__device__ __forceinline__ void run_any(const KParams& p, const KTask& t, int64_t so, int64_t dof, int64_t n,
-                                        int lane, int stride)
+// SUM = false: copies and zero fills only; SUM = true: also multi-source
+// sums. ES: element size in bytes.
+template <bool SUM, int ES>
+__global__ void __launch_bounds__(kBlock, 4) boxing_kernel(const __grid_constant__ KParams p)
 {
-    const int es = p.dtype == RTP_F32 ? 4 : 2;
-    const int64_t nvec = n * es / VB;
-    if (t.n_src == 1) {
-        run_copy<VB>(p, t, es, so, dof, nvec, lane, stride);
-    } else if (t.n_src == 0) {
-        run_zero<VB>(p, t, es, dof, nvec, lane, stride);
-    } else if (p.dtype == RTP_F32) {
-        if constexpr (VB >= 4) run_sum<VB, 4>(p, t, so, dof, nvec, lane, stride);
-    } else {
-        run_sum<VB, 2>(p, t, so, dof, nvec, lane, stride);
-    }
-}
-
-__device__ __forceinline__ void run(const KParams& p, const KTask& t, int64_t so, int64_t dof, int64_t n, int lane,
-                                    int stride)
-{
-    switch (t.vec) {
-    case 16: run_any<16>(p, t, so, dof, n, lane, stride); break;
-    case 8: run_any<8>(p, t, so, dof, n, lane, stride); break;
-    case 4: run_any<4>(p, t, so, dof, n, lane, stride); break;
-    default: run_any<2>(p, t, so, dof, n, lane, stride); break;
-    }
-}
-
-__global__ void __launch_bounds__(kBlock) boxing_kernel(const __grid_constant__ KParams p)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __shared__ int64_t s_off[kBlock], d_off[kBlock];
     for (int64_t c = blockIdx.x; c < p.total_chunks; c += gridDim.x) {
         const KTask& t = p.tasks[find_task(p, c)];
         const int64_t lc = c - t.chunk_begin;
-        int64_t so, dof;
-        if (t.mode == 1) {
-            const int64_t row = lc / t.nseg;
-            const int64_t c0 = (lc - row * t.nseg) * t.seg;
-            const int64_t n = min(t.seg, t.cols - c0);
-            row_offsets(t, row, so, dof);
-            run(p, t, so + c0, dof + c0, n, threadIdx.x, kBlock);
-        } else {
-            const int64_t r0 = lc * t.rpc;
-            const int64_t r1 = min(r0 + t.rpc, t.rows);
-            for (int64_t row = r0 + warp; row < r1; row += kWarps) {
-                row_offsets(t, row, so, dof);
-                run(p, t, so, dof, t.cols, lane, 32);
-            }
+        const int64_t rb = lc / t.nseg;
+        const int64_t c0 = (lc - rb * t.nseg) * t.seg;
+        const int64_t r0 = rb * t.rpc;
+        const int nr = (int)min((int64_t)t.rpc, t.rows - r0);
+        const int64_t len = min(t.seg, t.cols - c0);
+        if ((int)threadIdx.x < nr) {
+            int64_t so, dof;
+            row_offsets(t, r0 + threadIdx.x, so, dof);
+            s_off[threadIdx.x] = so + c0;
+            d_off[threadIdx.x] = dof + c0;
         }
+        __syncthreads();
+        const int nv = (int)(len * ES / t.vec);
+        switch (t.vec) {
+        case 16: run_chunk<16, ES, SUM>(p, t, nr, nv, s_off, d_off); break;
+        case 8: run_chunk<8, ES, SUM>(p, t, nr, nv, s_off, d_off); break;
+        case 4: run_chunk<4, ES, SUM>(p, t, nr, nv, s_off, d_off); break;
+        default:
+            if constexpr (ES == 2) run_chunk<2, ES, SUM>(p, t, nr, nv, s_off, d_off);
+            break;
+        }
+        __syncthreads();
     }
 }
 
@@ -285,6 +267,8 @@ int pick_vec(const PlanTask& t, const void* const* src, void* const* dst, int es
     return es;
 }
 
+// Chunking: rows longer than a chunk are cut into segments (one row per
+// chunk); shorter rows are grouped, up to one row per thread of the block.
 int64_t fill_task(KTask& k, const PlanTask& t, int vec, int es)
 {
     std::memset(&k, 0, sizeof k);
@@ -300,20 +284,19 @@ int64_t fill_task(KTask& k, const PlanTask& t, int vec, int es)
     k.n_src = (int32_t)t.src.size();
     k.n_dst = (int32_t)t.dst.size();
     const int64_t row_bytes = t.cols * es;
-    if (row_bytes >= (int64_t)kBlock * vec) {
-        const int64_t epv = vec / es;
-        int64_t seg = std::max<int64_t>(epv, (kChunkBytes / es) / epv * epv);
-        seg = std::min(seg, t.cols);
-        k.mode = 1;
+    const int64_t epv = vec / es;
+    if (row_bytes >= kChunkBytes) {
+        const int64_t seg = std::min(t.cols, std::max<int64_t>(epv, (kChunkBytes / es) / epv * epv));
         k.seg = seg;
         k.nseg = (t.cols + seg - 1) / seg;
-        return t.rows * k.nseg;
+        k.rpc = 1;
+    } else {
+        k.seg = t.cols;
+        k.nseg = 1;
+        k.rpc = (int32_t)std::min<int64_t>({(int64_t)kBlock, std::max<int64_t>(1, kChunkBytes / std::max<int64_t>(row_bytes, 1)),
+                                            t.rows});
     }
-    k.mode = 0;
-    int64_t rpc = std::max<int64_t>(kWarps, kChunkBytes / std::max<int64_t>(row_bytes, 1));
-    rpc = std::min(rpc, t.rows);
-    k.rpc = rpc;
-    return (t.rows + rpc - 1) / rpc;
+    return (t.rows + k.rpc - 1) / k.rpc * k.nseg;
 }
 
 }  // namespace
@@ -345,7 +328,7 @@ int launch_tasks(int dtype, const std::vector<PlanTask>& tasks, const void* cons
         if (t.src.size() + t.dst.size() > (size_t)kMaxPtrs) return fail(RTP_EUNSUPPORTED, "reshard: too many buffers");
     }
     static thread_local KParams prm;  // large: keep it off the stack
-    const int max_grid = sm_count() * kBlocksPerSm;
+    const int max_grid = sm_count() * 4;
     int launches = 0;
     size_t i = 0;
     while (i < tasks.size()) {
@@ -369,9 +352,18 @@ int launch_tasks(int dtype, const std::vector<PlanTask>& tasks, const void* cons
         }
         prm.n_tasks = nt;
         prm.total_chunks = chunks;
+        bool any_sum = false;
+        for (int k = 0; k < nt; ++k) any_sum = any_sum || prm.tasks[k].n_src > 1;
         if (chunks == 0) continue;
         const int grid = (int)std::min<int64_t>(chunks, max_grid);
-        boxing_kernel<<<grid, kBlock, 0, static_cast<cudaStream_t>(stream)>>>(prm);
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        if (es == 4) {
+            if (any_sum) boxing_kernel<true, 4><<<grid, kBlock, 0, st>>>(prm);
+            else boxing_kernel<false, 4><<<grid, kBlock, 0, st>>>(prm);
+        } else {
+            if (any_sum) boxing_kernel<true, 2><<<grid, kBlock, 0, st>>>(prm);
+            else boxing_kernel<false, 2><<<grid, kBlock, 0, st>>>(prm);
+        }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return fail(RTP_ECUDA, "boxing kernel launch failed: %s", cudaGetErrorString(e));
         ++launches;

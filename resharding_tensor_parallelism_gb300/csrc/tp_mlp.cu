@@ -74,6 +74,7 @@ struct GemmArgs {
     int32_t groups, fused, epi;
     int32_t m_tiles, n_tiles, kb_per_group;
     int32_t m0, n0;              // window of the problem (Domino chunk / column block)
+    int32_t m_end, n_end;        // exclusive bounds of the output window
     int32_t total_tiles;
 };
 
@@ -379,15 +380,21 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
             tc_fence_after();
             const int64_t row = a.m0 + mt * BM + quarter * 32 + lane;
             const int64_t col = a.n0 + nt * BN;
+            const bool row_ok = row < a.m_end;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld_32cols(taddr + 32u * c, r);
                 tmem_ld_wait();
+                const int64_t c0 = col + 32 * c;
+                if (!row_ok || c0 >= a.n_end) continue;
+                // 16-byte pieces; a piece is stored only if it lies inside the window
+                // (window edges are multiples of 8 columns)
                 if (a.epi == EPI_GELU_BF16) {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out[g]) + row * a.ldo + col + 32 * c);
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out[g]) + row * a.ldo + c0);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
+                        if (c0 + 8 * q >= a.n_end) break;
                         uint4 v;
                         v.x = pack_bf16(gelu(__uint_as_float(r[8 * q + 0])), gelu(__uint_as_float(r[8 * q + 1])));
                         v.y = pack_bf16(gelu(__uint_as_float(r[8 * q + 2])), gelu(__uint_as_float(r[8 * q + 3])));
@@ -396,11 +403,13 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
                         dst[q] = v;
                     }
                 } else {
-                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out[g]) + row * a.ldo + col + 32 * c);
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out[g]) + row * a.ldo + c0);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
+                    for (int q = 0; q < 8; ++q) {
+                        if (c0 + 4 * q >= a.n_end) break;
                         __stcs(dst + q, make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
                                                     __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
+                    }
                 }
             }
             tc_fence_before();
@@ -524,10 +533,9 @@ int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
                                                       (long long)K, (long long)F, (long long)N);
     if (F % P) return fail(RTP_ESHAPE, "%s: F=%lld is not divisible by P=%d", fn, (long long)F, P);
     const int64_t Fp = F / P;
-    if (M % chunks || (M / chunks) % BM) return fail(RTP_ESHAPE, "%s: M/chunks must be a multiple of %d", fn, BM);
-    if (K % BK) return fail(RTP_ESHAPE, "%s: K must be a multiple of %d", fn, BK);
-    if (Fp % BN) return fail(RTP_ESHAPE, "%s: F/P must be a multiple of %d", fn, BN);
-    if (N % (BN * col_blocks)) return fail(RTP_ESHAPE, "%s: N must be a multiple of %d", fn, BN * col_blocks);
+    if (M % chunks) return fail(RTP_ESHAPE, "%s: M=%lld is not divisible by chunks=%d", fn, (long long)M, chunks);
+    if (K % 8 || Fp % 8) return fail(RTP_ESHAPE, "%s: K and F/P must be multiples of 8 (16-byte rows)", fn);
+    if (N % (8 * col_blocks)) return fail(RTP_ESHAPE, "%s: N must be a multiple of %d", fn, 8 * col_blocks);
     if (M >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 31) || Fp >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31))
         return fail(RTP_ESHAPE, "%s: extents must stay below 2^31", fn);
     if (!aligned16(X) || !aligned16(Z)) return fail(RTP_EINVAL, "%s: X and Z must be 16-byte aligned", fn);
@@ -565,24 +573,28 @@ int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
     g1.groups = P;
     g1.fused = 0;
     g1.epi = EPI_GELU_BF16;
-    g1.m_tiles = (int)(Mc / BM);
-    g1.n_tiles = (int)(Fp / BN);
-    g1.kb_per_group = (int)(K / BK);
+    g1.m_tiles = (int)((Mc + BM - 1) / BM);
+    g1.n_tiles = (int)((Fp + BN - 1) / BN);
+    g1.kb_per_group = (int)((K + BK - 1) / BK);
     g1.n0 = 0;
+    g1.n_end = (int)Fp;
     g2.ldo = N;
     g2.groups = P;
     g2.fused = mode == 1;
     g2.epi = EPI_F32;
-    g2.m_tiles = (int)(Mc / BM);
-    g2.n_tiles = (int)(Nb / BN);
-    g2.kb_per_group = (int)(Fp / BK);
+    g2.m_tiles = (int)((Mc + BM - 1) / BM);
+    g2.n_tiles = (int)((Nb + BN - 1) / BN);
+    g2.kb_per_group = (int)((Fp + BK - 1) / BK);
 
     for (int c = 0; c < chunks; ++c) {
         g1.m0 = (int)(c * Mc);
+        g1.m_end = (int)((c + 1) * Mc);
         if ((st = launch_gemm(g1, s0))) return st;
         for (int b = 0; b < (mode == 0 ? col_blocks : 1); ++b) {
             g2.m0 = (int)(c * Mc);
+            g2.m_end = (int)((c + 1) * Mc);
             g2.n0 = (int)(b * Nb);
+            g2.n_end = (int)((b + 1) * Nb);
             if ((st = launch_gemm(g2, s0))) return st;
             if (mode == 1) continue;
             // sum of the P partials over this window: Z[rows, cols] = sum_i partial_i[rows, cols]

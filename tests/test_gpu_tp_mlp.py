@@ -1,0 +1,161 @@
+"""GPU parity of the tensor-parallel MLP (tcgen05 GEMMs) against the CPU oracle.
+
+Bounds (bf16 inputs, float32 accumulation):
+  * Z: max |Z - Z_ref| <= 2e-2 * sqrt(F / 4096) * RMS(Z_ref)   (K_eff = F)
+  * Y: max |Y - Y_ref| <= 2e-2 * sqrt(K / 4096) * RMS(Y_ref) on the rounded
+    values, and per element |Y - y| <= ulp_bf16(y) + 1.2 K 2^-24 sum_k |x_k a_k|
+    against the unrounded float64 y (one rounding plus float32 accumulation).
+The same seeded inputs feed both sides; Y_ref and Z_ref come from the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import as_f64, bf16_ulp, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+rtp = None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    global rtp
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from resharding_tensor_parallelism_gb300 import _build
+    _build.build()
+    import resharding_tensor_parallelism_gb300 as m
+    rtp = m
+    yield
+    assert m.device_error() == 0
+
+
+def _inputs(M, K, F, N, P, seed=0, wstd=0.02):
+    X = synth.normal(seed, (M, K), "bf16")
+    A = synth.normal(seed + 1, (K, F), "bf16", std=wstd)
+    B = synth.normal(seed + 2, (F, N), "bf16", std=wstd)
+    As = [np.ascontiguousarray(a) for a in np.split(A, P, axis=1)]
+    Bs = [np.ascontiguousarray(b) for b in np.split(B, P, axis=0)]
+    return X, As, Bs
+
+
+def _gpu(X, As, Bs, mode, chunks=1, col_blocks=1, second_stream=False):
+    s1 = torch.cuda.Stream() if second_stream else None
+    Z, Y = rtp.tp_mlp(to_dev(X), [to_dev(a) for a in As], [to_dev(b) for b in Bs], mode=mode, chunks=chunks,
+                      col_blocks=col_blocks, s1=s1)
+    torch.cuda.synchronize()
+    return to_host(Z), [to_host(y) for y in Y]
+
+
+def _check(X, As, Bs, Z, Ys, rows, what=""):
+    P = len(As)
+    K = X.shape[1]
+    F = sum(a.shape[1] for a in As)
+    z_ref, y_ref = oracle.tp_mlp(X, As, Bs, rows=rows)
+    # unrounded y and sum_k |x a| for the per-element bound
+    _, y64 = oracle.tp_mlp(X, As, Bs, rows=rows, round_y=False)
+    absX = X & np.uint16(0x7FFF)
+    _, s_abs = oracle.tp_mlp(absX, [a & np.uint16(0x7FFF) for a in As], [b & np.uint16(0x7FFF) for b in Bs],
+                             rows=rows, act="identity", round_y=False)
+    y_gpu = np.concatenate([as_f64(y[rows]) for y in Ys], axis=1)
+    z_gpu = Z[rows].astype(np.float64)
+    z_err = np.abs(z_gpu - z_ref).max()
+    z_tol = 2e-2 * np.sqrt(F / 4096) * np.sqrt(np.mean(z_ref ** 2))
+    assert z_err <= z_tol, "%s: Z error %.3g > %.3g" % (what, z_err, z_tol)
+    y_err = np.abs(y_gpu - y_ref).max()
+    y_tol = 2e-2 * np.sqrt(K / 4096) * np.sqrt(np.mean(y_ref ** 2))
+    bound = bf16_ulp(y64) + 1.2 * K * 2.0 ** -24 * s_abs
+    bad = np.abs(y_gpu - y64) > bound
+    assert not bad.any(), "%s: %d Y elements outside the per-element bound" % (what, bad.sum())
+    assert y_err <= max(y_tol, np.max(bound)), "%s: Y error %.3g > %.3g" % (what, y_err, y_tol)
+    return z_err / np.sqrt(np.mean(z_ref ** 2))
+
+
+def test_tiny_configuration():
+    """X[4,8] @ A[8,16] in 2 column shards, GELU, @ B[16,8] in 2 row shards; seed 0, N(0,1)."""
+    X, As, Bs = _inputs(4, 8, 16, 8, 2, seed=0, wstd=1.0)
+    for mode in (0, 1):
+        Z, Ys = _gpu(X, As, Bs, mode)
+        _check(X, As, Bs, Z, Ys, np.arange(4), "tiny mode %d" % mode)
+
+
+@pytest.mark.parametrize("M,K,F,N,P", [(300, 200, 528, 520, 2), (128, 64, 2048, 256, 8), (384, 136, 288, 264, 3),
+                                       (257, 1024, 1024, 512, 4)])
+def test_ragged_multi_tile(M, K, F, N, P):
+    X, As, Bs = _inputs(M, K, F, N, P, seed=M + K)
+    rows = np.arange(M)
+    for mode in (0, 1):
+        Z, Ys = _gpu(X, As, Bs, mode)
+        _check(X, As, Bs, Z, Ys, rows, "mode %d" % mode)
+    if M % 2 == 0 and N % 16 == 0:
+        Z, Ys = _gpu(X, As, Bs, 0, chunks=2, col_blocks=2, second_stream=True)
+        _check(X, As, Bs, Z, Ys, rows, "domino 2x2")
+
+
+def _sample_rows(M, n):
+    base = [0, 1, 127, 128, 129, M // 2, M - 129, M - 128, M - 1]
+    rng = np.random.default_rng(M)
+    extra = list(rng.integers(0, M, size=max(0, n - len(base))))
+    return np.array(sorted(set(int(r) for r in base + extra)))
+
+
+@pytest.fixture(scope="module")
+def cfg4():
+    return _inputs(8192, 4096, 16384, 4096, 8, seed=40)
+
+
+def test_tp_mlp_configuration_full_size(cfg4):
+    """X [8192,4096], A [4096,16384] and B [16384,4096] N(0,0.02), P = 8."""
+    X, As, Bs = cfg4
+    rows = _sample_rows(8192, 16)
+    Zs = {}
+    for mode in (1, 0):
+        Z, Ys = _gpu(X, As, Bs, mode)
+        _check(X, As, Bs, Z, Ys, rows, "full mode %d" % mode)
+        Zs[mode] = Z
+    # the Domino schedules sum the same partials in the same order: same bits
+    for chunks, cb in ((2, 1), (4, 2)):
+        Z, _ = _gpu(X, As, Bs, 0, chunks=chunks, col_blocks=cb, second_stream=True)
+        np.testing.assert_array_equal(Z, Zs[0])
+    # deterministic
+    Z, _ = _gpu(X, As, Bs, 1)
+    np.testing.assert_array_equal(Z, Zs[1])
+
+
+def test_domino_configuration_full_size():
+    """Llama-70B MLP shape: tokens 4096, hidden 8192, ffn 28672, P = 8; fused, and
+    the Domino row split (2 and 4 chunks) with the 2D column split."""
+    X, As, Bs = _inputs(4096, 8192, 28672, 8192, 8, seed=50)
+    rows = _sample_rows(4096, 10)
+    Z1, Ys = _gpu(X, As, Bs, 1)
+    _check(X, As, Bs, Z1, Ys, rows, "fused")
+    Z2, Ys2 = _gpu(X, As, Bs, 0, chunks=2, col_blocks=2, second_stream=True)
+    _check(X, As, Bs, Z2, Ys2, rows, "domino 2 chunks, 2 column blocks")
+    Z4, _ = _gpu(X, As, Bs, 0, chunks=4, col_blocks=1, second_stream=True)
+    np.testing.assert_array_equal(Z4, Z2)
+
+
+def test_argument_errors():
+    dev = lambda *s: torch.zeros(s, dtype=torch.bfloat16, device="cuda")
+    X = dev(256, 64)
+    As = [dev(64, 128) for _ in range(2)]
+    Bs = [dev(128, 64) for _ in range(2)]
+    with pytest.raises(rtp.RtpError) as e:  # M not divisible by chunks
+        rtp.tp_mlp(dev(255, 64), As, Bs, mode=0, chunks=2)
+    assert e.value.status == -2
+    with pytest.raises(rtp.RtpError) as e:  # K not a multiple of 8
+        rtp.tp_mlp(dev(256, 60), [dev(60, 128)] * 2, Bs)
+    assert e.value.status == -2
+    with pytest.raises(rtp.RtpError) as e:  # misaligned X
+        rtp.tp_mlp(dev(256 * 64 + 1)[1:].view(256, 64), As, Bs)
+    assert e.value.status == -1
+    with pytest.raises(rtp.RtpError):  # 9 ranks
+        rtp.tp_mlp(X, [dev(64, 8)] * 9, [dev(8, 64)] * 9)
+    with pytest.raises(rtp.RtpError):  # column blocks need mode 0
+        rtp.tp_mlp(X, As, Bs, mode=1, col_blocks=2)
+    Z, _ = rtp.tp_mlp(X, As, Bs)
+    torch.cuda.synchronize()
+    assert float(Z.abs().max()) == 0.0
