@@ -1,0 +1,555 @@
+#!/usr/bin/env python3
+"""Benchmark of the resharding engine and the 1D tensor-parallel MLP on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  * the resharding sweep on an activation tensor [B=8, S=2048, H=4096] in
+    float32 and bf16, on virtual meshes 1x8 and 2x4, six transitions each
+    (dims_mapping [0,-1,-1]->[-1,-1,0], [-1,-1,0]->[-1,0,-1],
+    [0,-1,1]->[-1,-1,-1], P-sum of 8->B, P-sum of 8->S(2), B->S(0)): 24
+    reshard calls, L2 flushed before each;
+  * the tensor-parallel MLP X[8192,4096] . A[4096,16384] -> GELU ->
+    . B[16384,4096], P = 8, bf16 in / float32 accumulate, fused reduction;
+  * the Domino schedule on the Llama-70B MLP shape (tokens 4096, hidden 8192,
+    ffn 28672, P = 8): row split into 2 chunks with the reduction of one chunk
+    on a second stream, next to the serial (one stream) schedule.
+
+`value` is the resharding throughput (algorithmic bytes of the 24 calls over
+their device time); the MLP and Domino figures are reported beside it.
+Inputs are seeded (torch's Philox generator on the device), resident in HBM
+when the timed region starts. `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "reshard GB/s (% of HBM peak); TP-MLP TFLOP/s (% of bf16 peak), 1 GB300"
+SWEEP_SHAPE = (8, 2048, 4096)
+MLP = dict(M=8192, K=4096, F=16384, N=4096, P=8)
+DOMINO = dict(M=4096, K=8192, F=28672, N=8192, P=8)
+L2_FLUSH_BYTES = 512 * 1024 * 1024
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), \
+            "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---- the sweep -----------------------------------------------------------------------
+
+TRANSITIONS = [
+    ("[0,-1,-1]->[-1,-1,0]", [0, -1, -1], [-1, -1, 0], False),
+    ("[-1,-1,0]->[-1,0,-1]", [-1, -1, 0], [-1, 0, -1], False),
+    ("[0,-1,1]->[-1,-1,-1]", [0, -1, 1], [-1, -1, -1], False),
+    ("P8->B", None, [-1, -1, -1], True),
+    ("P8->S(2)", None, [-1, -1, 0], True),
+    ("B->S(0)", [-1, -1, -1], [0, -1, -1], False),
+]
+
+
+def sweep_specs(rtp, mesh_name):
+    """(name, src spec, dst spec) of the six transitions on mesh '1x8' or '2x4'.
+    On 1x8, mappings naming only mesh dim 0 use the 1-D mesh [8]; [0,-1,1]
+    uses [1,8]. On 2x4, P-sum of 8 is partial over both mesh dims, and a
+    destination split or a broadcast source over 'all 8' nests both mesh dims."""
+    out = []
+    for name, sdm, ddm, partial in TRANSITIONS:
+        if mesh_name == "1x8":
+            m = (1, 8) if (sdm and 1 in sdm) else (8,)
+            if partial:
+                src = rtp.spec_nd_sbp(m, ("P",))
+            else:
+                src = rtp.spec_from_dims_mapping(sdm, m)
+            dst = rtp.spec_from_dims_mapping(ddm, m)
+        else:
+            m = (2, 4)
+            full8 = partial or sdm == [-1, -1, -1]
+            if partial:
+                src = rtp.spec_nd_sbp(m, ("P", "P"))
+            elif sdm == [-1, -1, -1]:
+                src = rtp.spec_nd_sbp(m, ("B", "B"))
+            else:
+                src = rtp.spec_from_dims_mapping(sdm, m)
+            ax = [i for i, v in enumerate(ddm) if v >= 0]
+            if full8 and ax:
+                dst = rtp.spec_nd_sbp(m, (("S", ax[0]), ("S", ax[0])))
+            else:
+                dst = rtp.spec_from_dims_mapping(ddm, m)
+        out.append((name, src, dst, partial))
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.file,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    source has not changed since the counters were taken (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = {"boxing_kernel": "boxing.cu", "tp_gemm_kernel": "tp_mlp.cu"}[kernel]
+    with open(os.path.join(ROOT, "resharding_tensor_parallelism_gb300", "csrc", src), "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            p = line.split()
+            if len(p) >= 4 and not line.startswith("#") and p[0] == kernel and p[1] == workload and p[2] == digest:
+                return float(p[3])
+    return None
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import resharding_tensor_parallelism_gb300 as rtp
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist_mod.init_process_group("nccl", device_id=dev)
+        dist = dist_mod
+    rtp.lib()
+    hbm_peak, bf16_peak, bf16_sust, peak_src = _peaks()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234 + 7919 * rank)
+
+    def randn(shape, dtype, std=1.0):
+        return (torch.randn(shape, generator=gen, device=dev, dtype=torch.float32) * std).to(dtype)
+
+    # ---- sweep inputs: pieces resident in HBM ----
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    sweep = []  # (label, dtype_code, src pieces, src, dst pieces, dst, bytes, launches)
+    for dtype, code in ((torch.float32, rtp.F32), (torch.bfloat16, rtp.BF16)):
+        T = randn(SWEEP_SHAPE, dtype)
+        partials = [randn(SWEEP_SHAPE, dtype) for _ in range(8)]
+        for mesh_name in ("1x8", "2x4"):
+            for name, src, dst, partial in sweep_specs(rtp, mesh_name):
+                ins = partials if partial else rtp.shard(T, src)
+                outs = [torch.empty(rtp.shard_shape(SWEEP_SHAPE, dst, r), dtype=dtype, device=dev)
+                        for r in range(dst.num_ranks)]
+                rd, wr, nt, nl = rtp.reshard_cost(code, SWEEP_SHAPE, src, dst)
+                sweep.append(("%s %s %s" % (str(dtype).split(".")[-1], mesh_name, name), code, ins, src, outs, dst,
+                              rd + wr, nl))
+        del T
+    torch.cuda.synchronize()
+
+    # ---- MLP inputs ----
+    def mlp_buffers(c, extra_partials):
+        M, K, F, N, P = c["M"], c["K"], c["F"], c["N"], c["P"]
+        X = randn((M, K), torch.bfloat16)
+        A = [randn((K, F // P), torch.bfloat16, 0.02) for _ in range(P)]
+        B = [randn((F // P, N), torch.bfloat16, 0.02) for _ in range(P)]
+        Y = [torch.empty((M, F // P), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+        Z = torch.empty((M, N), dtype=torch.float32, device=dev)
+        parts = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in range(P)] if extra_partials else None
+        return dict(X=X, A=A, B=B, Y=Y, Z=Z, parts=parts, flops=2 * M * K * F + 2 * M * F * N)
+
+    mlp = mlp_buffers(MLP, False)
+    dom = mlp_buffers(DOMINO, True)
+    s1 = torch.cuda.Stream(device=dev)
+    # the reduction alone: P-sum of the 8 float32 partials into one buffer
+    dom_red_src = rtp.spec_nd_sbp((8,), ("P",))
+    dom_red_dst = rtp.spec_nd_sbp((1,), ("B",))
+    dom_shape = (DOMINO["M"], DOMINO["N"])
+
+    def run_mlp():
+        rtp.tp_mlp(mlp["X"], mlp["A"], mlp["B"], Y=mlp["Y"], Z=mlp["Z"], mode=1)
+
+    def run_domino():
+        rtp.tp_mlp(dom["X"], dom["A"], dom["B"], Y=dom["Y"], partials=dom["parts"], Z=dom["Z"], mode=0, chunks=2,
+                   s1=s1)
+
+    def run_serial():
+        rtp.tp_mlp(dom["X"], dom["A"], dom["B"], Y=dom["Y"], partials=dom["parts"], Z=dom["Z"], mode=0, chunks=1)
+
+    def run_reduce():
+        rtp.reshard(dom["parts"], dom_shape, dom_red_src, dom_red_dst, out=[dom["Z"]])
+
+    ops = [(label, (lambda c=c, i=i, s=s, o=o, d=d: rtp.reshard(i, SWEEP_SHAPE, s, d, out=o)), nbytes, nl)
+           for (label, c, i, s, o, d, nbytes, nl) in sweep]
+    launches_per_step = sum(x[3] for x in ops) + 2 + 6 + 3 + 1  # mlp 2, domino 2x3, serial 3, reduce 1
+    E = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step(record):
+        for label, fn, nbytes, nl in ops:
+            flush.zero_()
+            e0, e1 = E(), E()
+            e0.record()
+            fn()
+            e1.record()
+            record.append(("reshard", label, e0, e1, nbytes))
+        for kind, fn in (("mlp", run_mlp), ("domino", run_domino), ("serial", run_serial), ("reduce", run_reduce)):
+            flush.zero_()
+            e0, e1 = E(), E()
+            e0.record()
+            fn()
+            e1.record()
+            record.append((kind, kind, e0, e1, 0))
+
+    for _ in range(args.warmup):
+        step([])
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    records = []
+    with ClockSampler(local_rank) as clocks:
+        t0 = E()
+        t1 = E()
+        t0.record()
+        for _ in range(args.steps):
+            step(records)
+        t1.record()
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall_ms = t0.elapsed_time(t1)
+    per = {}
+    for kind, label, e0, e1, nbytes in records:
+        ms = e0.elapsed_time(e1)
+        d = per.setdefault((kind, label), [0.0, 0, nbytes])
+        d[0] += ms
+        d[1] += 1
+    reshard_ms = sum(v[0] for (k, _), v in per.items() if k == "reshard")
+    reshard_bytes = sum(v[2] * v[1] for (k, _), v in per.items() if k == "reshard")
+    mlp_ms = per[("mlp", "mlp")][0]
+    dom_ms = per[("domino", "domino")][0] / args.steps
+    ser_ms = per[("serial", "serial")][0] / args.steps
+    red_ms = per[("reduce", "reduce")][0] / args.steps
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    reshard_ms = max_over_ranks(reshard_ms)
+    mlp_ms = max_over_ranks(mlp_ms)
+    wall_ms = max_over_ranks(wall_ms)
+    gbs = reshard_bytes * world / (reshard_ms * 1e-3) / 1e9
+    tflops = MLP_FLOPS * args.steps * world / (mlp_ms * 1e-3) / 1e12
+    per_launch_gbs = reshard_bytes / (reshard_ms * 1e-3) / 1e9
+
+    result = {
+        "metric": METRIC,
+        "value": round(gbs, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(wall_ms / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32+bf16",
+        "data": "synthetic (seeded Philox normals on the device)",
+        "config": {"workload": "resharding sweep [8,2048,4096] f32+bf16 on virtual meshes 1x8 and 2x4 (6 transitions "
+                               "each) + TP-MLP 8192x4096x16384x4096 P=8 + Domino 4096x8192x28672x8192 P=8",
+                   "parallelism": "virtual mesh of 8 ranks inside each GPU; GPUs run independent replicas",
+                   "l2": "flushed (512 MiB write) before every timed call"},
+        "roofline": {"bound": "hbm", "kernel": "boxing_kernel", "achieved": round(per_launch_gbs, 1),
+                     "peak": hbm_peak, "unit": "GB/s", "frac": round(per_launch_gbs / hbm_peak, 4),
+                     "peak_source": peak_src, "traffic": _traffic("boxing_kernel", "sweep")},
+        "tp_mlp": {"value": round(tflops, 1), "unit": "TFLOP/s", "mode": "fused reduction",
+                   "ms_per_call": round(mlp_ms / args.steps, 4),
+                   "roofline": {"bound": "tensor", "kernel": "tp_gemm_kernel", "achieved": round(tflops / world, 1),
+                                "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(tflops / world / bf16_peak, 4),
+                                "frac_of_sustained": round(tflops / world / bf16_sust, 4), "peak_source": peak_src,
+                                "traffic": _traffic("tp_gemm_kernel", "mlp")}},
+        "domino": {"ms_serial": round(ser_ms, 4), "ms_overlap_2_chunks": round(dom_ms, 4),
+                   "ms_reduce_alone": round(red_ms, 4),
+                   "hiding": round((ser_ms - dom_ms) / red_ms, 3) if red_ms > 0 else None,
+                   "tflops_overlap": round(DOMINO_FLOPS / (dom_ms * 1e-3) / 1e12, 1)},
+        "per_transition_gbs": {label: round(v[2] * v[1] / (v[0] * 1e-3) / 1e9, 1)
+                               for (k, label), v in per.items() if k == "reshard"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_e2e:
+        result["e2e"] = e2e_sweep(rtp, torch, dev, sweep)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(max_seconds=args.cpu_seconds)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+MLP_FLOPS = 2 * MLP["M"] * MLP["K"] * MLP["F"] + 2 * MLP["M"] * MLP["F"] * MLP["N"]
+DOMINO_FLOPS = 2 * DOMINO["M"] * DOMINO["K"] * DOMINO["F"] + 2 * DOMINO["M"] * DOMINO["F"] * DOMINO["N"]
+
+
+def e2e_sweep(rtp, torch, dev, sweep):
+    """The sweep's bf16 1x8 transitions through the public API with host
+    buffers: pinned host -> device copy of the source pieces, reshard, device
+    -> pinned host copy of the destination pieces, all inside the timed
+    region (2 timed passes after 1 warm-up)."""
+    sel = [s for s in sweep if s[0].startswith("bfloat16 1x8")]
+    host_in = [[torch.empty(p.shape, dtype=p.dtype, pin_memory=True).copy_(p) for p in s[2]] for s in sel]
+    host_out = [[torch.empty(p.shape, dtype=p.dtype, pin_memory=True) for p in s[4]] for s in sel]
+    h2d = sum(p.numel() * p.element_size() for hs in host_in for p in hs)
+    d2h = sum(p.numel() * p.element_size() for hs in host_out for p in hs)
+    nbytes = sum(s[6] for s in sel)
+
+    def one():
+        for s, hi, ho in zip(sel, host_in, host_out):
+            dev_in = [h.to(dev, non_blocking=True) for h in hi]
+            outs = rtp.reshard(dev_in, SWEEP_SHAPE, s[3], s[5])
+            for o, h in zip(outs, ho):
+                h.copy_(o, non_blocking=True)
+        torch.cuda.synchronize()
+
+    one()
+    t = time.perf_counter()
+    for _ in range(2):
+        one()
+    dt = (time.perf_counter() - t) / 2
+    return {"value": round(nbytes / dt / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "workload": "the six bf16 transitions on the 1x8 mesh, host pinned buffers in and out"}
+
+
+# ---- CPU oracle (baseline and reference arm) ---------------------------------------------
+
+CPU_SAMPLE_SHAPE = (8, 64, 4096)
+
+
+def cpu_baseline(max_seconds: float = 20.0, steps: int = 1):
+    """The oracle (single-threaded C++) on a bounded sample of the sweep: the
+    twelve float32 transitions on a [8,64,4096] slice of the activation
+    tensor (same meshes and specs), GB/s of algorithmic bytes."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    shape = CPU_SAMPLE_SHAPE
+    T = synth.normal(11, shape, "f32")
+    parts = [synth.normal(20 + k, shape, "f32") for k in range(8)]
+    cases = []
+    for mesh_name in ("1x8", "2x4"):
+        for name, sdm, ddm, partial in TRANSITIONS:
+            src, dst = _oracle_specs(oracle, mesh_name, sdm, ddm, partial)
+            pieces = parts if partial else oracle.shard(T, src)
+            cases.append((mesh_name + " " + name, pieces, src, dst))
+    total_bytes, total_s, done = 0, 0.0, 0
+    t_start = time.perf_counter()
+    for _ in range(steps):
+        for label, pieces, src, dst in cases:
+            t = time.perf_counter()
+            outs = oracle.reshard(pieces, shape, src, dst)
+            total_s += time.perf_counter() - t
+            total_bytes += sum(p.nbytes for p in _distinct_reads(pieces, src, oracle, shape)) + sum(o.nbytes for o in outs)
+            done += 1
+            if time.perf_counter() - t_start > max_seconds:
+                break
+    return {"value": round(total_bytes / total_s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d float32 reshard calls of the sweep on a [8,64,4096] slice (meshes 1x8 and 2x4)" % done,
+            "seconds": round(total_s, 2), "host_cores": os.cpu_count()}
+
+
+def _distinct_reads(pieces, layout, oracle, shape):
+    """Source pieces counted once per distinct piece (broadcast replicas read once)."""
+    seen, out = set(), []
+    for r, p in enumerate(pieces):
+        lo, hi, hv = oracle.shard_box(shape, layout, r)
+        key = (lo, hi) if "P" not in layout.entries else r
+        if key in seen or p.size == 0:
+            continue
+        seen.add(key)
+        out.append(p)
+    return out
+
+
+def _oracle_specs(oracle, mesh_name, sdm, ddm, partial):
+    if mesh_name == "1x8":
+        m = (1, 8) if (sdm and 1 in sdm) else (8,)
+        src = oracle.Layout(m, ("P",)) if partial else oracle.layout_from_dims_mapping(sdm, m)
+        dst = oracle.layout_from_dims_mapping(ddm, m)
+        return src, dst
+    m = (2, 4)
+    full8 = partial or sdm == [-1, -1, -1]
+    if partial:
+        src = oracle.Layout(m, ("P", "P"))
+    elif sdm == [-1, -1, -1]:
+        src = oracle.Layout(m, ("B", "B"))
+    else:
+        src = oracle.layout_from_dims_mapping(sdm, m)
+    ax = [i for i, v in enumerate(ddm) if v >= 0]
+    dst = oracle.Layout(m, (("S", ax[0]), ("S", ax[0]))) if (full8 and ax) else oracle.layout_from_dims_mapping(ddm, m)
+    return src, dst
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle as it stands, on the host cores, rank 0 only."""
+    if rank != 0:
+        return
+    per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(max_seconds=per_step)
+    t = time.perf_counter()
+    vals = [cpu_baseline(max_seconds=per_step) for _ in range(args.steps)]
+    wall = time.perf_counter() - t
+    v = statistics.median(x["value"] for x in vals)
+    cb = dict(vals[-1])
+    cb["value"] = v
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(wall / args.steps * 1e3, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded generator)",
+        "config": {"workload": "resharding sweep transitions on a [8,64,4096] float32 slice, meshes 1x8 and 2x4, "
+                               "by the single-threaded CPU oracle"},
+        "cpu_baseline": cb, "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+PROFILE_CASES = {
+    # name: (kind, details)
+    "reshard_f32_s0s2": ("reshard", ("1x8", 0, "f32")),
+    "reshard_bf16_s0s2": ("reshard", ("1x8", 0, "bf16")),
+    "reshard_f32_p8b": ("reshard", ("1x8", 3, "f32")),
+    "reshard_f32_p8s2": ("reshard", ("1x8", 4, "f32")),
+    "reshard_f32_s0s2b": ("reshard", ("1x8", 2, "f32")),
+    "mlp_fused": ("mlp", MLP),
+    "domino_fused": ("mlp", DOMINO),
+}
+
+
+def run_profile_case(name: str, repeats: int = 2):
+    """A small, fixed workload for an ncu capture: `repeats` calls of one
+    operation on inputs generated on the device (no other library launches)."""
+    import torch
+    import resharding_tensor_parallelism_gb300 as rtp
+
+    torch.cuda.set_device(0)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(5)
+    kind, det = PROFILE_CASES[name]
+    if kind == "reshard":
+        mesh_name, idx, dt = det
+        dtype, code = (torch.float32, rtp.F32) if dt == "f32" else (torch.bfloat16, rtp.BF16)
+        _, src, dst, _ = sweep_specs(rtp, mesh_name)[idx]
+        ins = [torch.randn(rtp.shard_shape(SWEEP_SHAPE, src, r), generator=gen, device="cuda").to(dtype)
+               for r in range(src.num_ranks)]
+        outs = [torch.empty(rtp.shard_shape(SWEEP_SHAPE, dst, r), dtype=dtype, device="cuda")
+                for r in range(dst.num_ranks)]
+        rd, wr, nt, nl = rtp.reshard_cost(code, SWEEP_SHAPE, src, dst)
+        torch.cuda.synchronize()
+        for _ in range(repeats):
+            rtp.reshard(ins, SWEEP_SHAPE, src, dst, out=outs)
+        torch.cuda.synchronize()
+        print(json.dumps({"case": name, "algorithmic_bytes_per_launch": rd + wr, "launches_per_call": nl}))
+    else:
+        c = det
+        M, K, F, N, P = c["M"], c["K"], c["F"], c["N"], c["P"]
+        X = torch.randn((M, K), generator=gen, device="cuda").bfloat16()
+        A = [(torch.randn((K, F // P), generator=gen, device="cuda") * 0.02).bfloat16() for _ in range(P)]
+        B = [(torch.randn((F // P, N), generator=gen, device="cuda") * 0.02).bfloat16() for _ in range(P)]
+        Y = [torch.empty((M, F // P), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+        Z = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        for _ in range(repeats):
+            rtp.tp_mlp(X, A, B, Y=Y, Z=Z, mode=1)
+        torch.cuda.synchronize()
+        print(json.dumps({"case": name, "flops_gemm1": 2 * M * K * F, "flops_gemm2": 2 * M * F * N}))
+    assert rtp.device_error() == 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
+                    help="run one small fixed workload for an ncu capture and exit")
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case)
+        return
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()
