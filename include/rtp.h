@@ -235,6 +235,27 @@ int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
                int col_blocks, rtp_stream s0, rtp_stream s1);
 
 /*
+ * tp_mlp for callers that cannot allocate device memory (code running inside
+ * another runtime's memory pool, or a serving loop whose memory plan is fixed
+ * at start-up). The pages have no counterpart to this call; it is a service
+ * of this library.
+ *   X, A_shards, B_shards, Z: as in rtp_tp_mlp (caller-owned, 16-byte aligned)
+ *   stream: the stream that orders the work
+ * Computes Z = sum_i GELU(X A_i) B_i with the reduction fused into the
+ * row-parallel GEMM. The activations Y live in a static device array of the
+ * library (16 MiB), so the call allocates nothing. It returns RTP_ESHAPE when
+ * P * round_up(M * F/P * 2 bytes, 256) exceeds 16 MiB (about M * F <= 8 Mi
+ * elements), and the other errors of rtp_tp_mlp.
+ * The first call on a device finds the array's device address (with that
+ * device current); make that first call before any stream capture.
+ * Every call uses the same array: calls that overlap on the GPU (on several
+ * streams, or from several threads) race on it and must be ordered by the
+ * caller.
+ */
+int rtp_tp_mlp_noalloc(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X, const void* const* A_shards,
+                       const void* const* B_shards, float* Z, rtp_stream stream);
+
+/*
  * Reads and clears the device word in which the tensor-core kernels of
  * rtp_tp_mlp record a wait that gave up (no progress for about 4 seconds; the
  * kernel then stops, frees its tensor memory and returns instead of hanging).

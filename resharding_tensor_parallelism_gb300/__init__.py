@@ -92,6 +92,8 @@ def _load():
         "rtp_infer_spmd": [ctypes.c_char_p, c_int, P(i32p), c_int, i32p, u32p, u32p, P(i32p)],
         "rtp_infer_reshape": [c_int, i64p, i32p, c_int, i64p, c_int, i64p, i32p, i32p],
         "rtp_device_error": [vp, u32p],
+        "rtp_tp_mlp_noalloc": [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vpp, vpp,
+                               vp, vp],
         "rtp_tp_mlp": [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vpp, vpp, vpp,
                        vpp, vp, c_int, c_int, c_int, vp, vp],
     }
@@ -334,6 +336,22 @@ def tp_mlp(X, A_shards, B_shards, Y=None, partials=None, Z=None, mode: int = 1, 
                               _ptrs([b.data_ptr() for b in B_shards]), _ptrs([y.data_ptr() for y in Y]), pp,
                               Z.data_ptr(), mode, chunks, col_blocks, _stream_ptr(s0), _stream_ptr(s1)))
     return Z, Y
+
+
+def tp_mlp_noalloc(X, A_shards, B_shards, Z=None, stream=None):
+    """Z = sum_i GELU(X A_i) B_i with the activations in the library's static
+    device scratch (for callers that cannot allocate). Returns Z."""
+    torch = _torch()
+    P = len(A_shards)
+    M, K = X.shape
+    Fp = A_shards[0].shape[1]
+    N = B_shards[0].shape[1]
+    if Z is None:
+        Z = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    _check_cuda([X, Z] + list(A_shards) + list(B_shards), "tp_mlp_noalloc")
+    _check(_load().rtp_tp_mlp_noalloc(P, M, K, Fp * P, N, X.data_ptr(), _ptrs([a.data_ptr() for a in A_shards]),
+                                      _ptrs([b.data_ptr() for b in B_shards]), Z.data_ptr(), _stream_ptr(stream)))
+    return Z
 
 
 def device_error(stream=None) -> int:

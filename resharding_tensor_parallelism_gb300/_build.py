@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librtp.so")
 
 HOST_SOURCES = ["spec.cpp", "plan.cpp", "infer.cpp"]
-CUDA_SOURCES = ["boxing.cu", "tp_mlp.cu"]
+CUDA_SOURCES = ["boxing.cu", "tp_mlp.cu", "tp_mlp_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
