@@ -480,6 +480,7 @@ PROFILE_CASES = {
     "reshard_f32_p8b": ("reshard", ("1x8", 3, "f32")),
     "reshard_f32_p8s2": ("reshard", ("1x8", 4, "f32")),
     "reshard_f32_s0s2b": ("reshard", ("1x8", 2, "f32")),
+    "sweep": ("sweep", None),
     "mlp_fused": ("mlp", MLP),
     "domino_fused": ("mlp", DOMINO),
 }
@@ -495,7 +496,26 @@ def run_profile_case(name: str, repeats: int = 2):
     gen = torch.Generator(device="cuda")
     gen.manual_seed(5)
     kind, det = PROFILE_CASES[name]
-    if kind == "reshard":
+    if kind == "sweep":
+        # the 24 reshard calls of one bench step, in bench order, one launch each
+        order = []
+        for dtype, code in ((torch.float32, rtp.F32), (torch.bfloat16, rtp.BF16)):
+            for mesh_name in ("1x8", "2x4"):
+                for tname, src, dst, partial in sweep_specs(rtp, mesh_name):
+                    ins = [torch.randn(rtp.shard_shape(SWEEP_SHAPE, src, r), generator=gen, device="cuda").to(dtype)
+                           for r in range(src.num_ranks)]
+                    outs = [torch.empty(rtp.shard_shape(SWEEP_SHAPE, dst, r), dtype=dtype, device="cuda")
+                            for r in range(dst.num_ranks)]
+                    rd, wr, nt, nl = rtp.reshard_cost(code, SWEEP_SHAPE, src, dst)
+                    torch.cuda.synchronize()
+                    rtp.reshard(ins, SWEEP_SHAPE, src, dst, out=outs)
+                    torch.cuda.synchronize()
+                    order.append({"call": "%s %s %s" % (str(dtype).split(".")[-1], mesh_name, tname),
+                                  "algorithmic_bytes": rd + wr, "launches": nl})
+                    del ins, outs
+                    torch.cuda.empty_cache()
+        print(json.dumps({"case": name, "calls": order}))
+    elif kind == "reshard":
         mesh_name, idx, dt = det
         dtype, code = (torch.float32, rtp.F32) if dt == "f32" else (torch.bfloat16, rtp.BF16)
         _, src, dst, _ = sweep_specs(rtp, mesh_name)[idx]

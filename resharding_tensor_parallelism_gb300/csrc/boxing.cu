@@ -30,7 +30,6 @@ namespace rtp {
 namespace {
 
 constexpr int kBlock = 256;
-constexpr int kUnroll = 4;
 constexpr int64_t kChunkBytes = 32 * 1024;
 constexpr int kMaxTasks = 96;
 constexpr int kMaxPtrs = 640;
@@ -318,7 +317,7 @@ int count_launches(const std::vector<PlanTask>& tasks)
 }
 
 int launch_tasks(int dtype, const std::vector<PlanTask>& tasks, const void* const* src, void* const* dst,
-                 void* stream, int* n_launches_out)
+                 void* stream, int* n_launches_out, int blocks_per_sm)
 {
     const int es = dtype == RTP_F32 ? 4 : 2;
     for (const auto& t : tasks) {
@@ -328,7 +327,7 @@ int launch_tasks(int dtype, const std::vector<PlanTask>& tasks, const void* cons
         if (t.src.size() + t.dst.size() > (size_t)kMaxPtrs) return fail(RTP_EUNSUPPORTED, "reshard: too many buffers");
     }
     static thread_local KParams prm;  // large: keep it off the stack
-    const int max_grid = sm_count() * 4;
+    const int max_grid = sm_count() * (blocks_per_sm < 1 ? 1 : blocks_per_sm > 4 ? 4 : blocks_per_sm);
     int launches = 0;
     size_t i = 0;
     while (i < tasks.size()) {

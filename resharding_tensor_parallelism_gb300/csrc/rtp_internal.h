@@ -60,8 +60,10 @@ rtp_spec whole_tensor_spec();
 
 // ---- launches (boxing.cu) --------------------------------------------------------------
 // Executes planned tasks on `stream`; src/dst buffer arrays are indexed by Ref::rank.
+// blocks_per_sm caps the persistent grid (default 4 = full occupancy); a
+// reduction that should run beside another kernel uses 1.
 int launch_tasks(int dtype, const std::vector<PlanTask>& tasks, const void* const* src, void* const* dst,
-                 void* stream, int* n_launches_out);
+                 void* stream, int* n_launches_out, int blocks_per_sm = 4);
 // Number of launches the tasks need (host only).
 int count_launches(const std::vector<PlanTask>& tasks);
 

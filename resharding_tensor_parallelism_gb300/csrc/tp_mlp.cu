@@ -5,17 +5,23 @@
 //   column-parallel:  Y_i = GELU(X A_i)          X [M,K], A_i [K,F/P]
 //   row-parallel:     Z   = sum_i Y_i B_i        Y_i [M,F/P], B_i [F/P,N]
 //
-// Both GEMMs run on one persistent, warp-specialised tcgen05 kernel:
-//   warp 0     TMA producer: 128x64 tiles of the K-major operand (X or Y_i)
-//              and 4 boxes of 64x64 of the N-major operand (A_i or B_i), all
-//              128-byte swizzled, into a 4-stage shared-memory ring;
-//   warp 1     one thread issues tcgen05.mma (M=128, N=256, K=16, bf16 in,
-//              float32 accumulate in TMEM); 2 accumulators of 256 columns
-//              let the epilogue of one tile overlap the next tile's K loop;
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator rows, GELU and bf16
-//              rounding (GEMM1) or float32 (GEMM2), stored to global memory.
-// Tiles are walked in groups of 16 M-tiles so that the CTAs running at one
-// time share operand panels in L2.
+// Both GEMMs run on one persistent, warp-specialised tcgen05 kernel in which a
+// cluster of 2 CTAs (2 SMs) computes one 256x256 output tile per step:
+//   warp 0     TMA producer, in each CTA: its 128 rows of the K-major operand
+//              (X or Y_i, 128x64 per stage) and its 128 columns of the N-major
+//              operand (A_i or B_i, two 64x64 boxes), 128-byte swizzled, into
+//              a 6-stage ring of 32 KB stages;
+//   warp 1     one thread of the leader CTA issues tcgen05.mma.cta_group::2
+//              (M=256, N=256, K=16, bf16 in, float32 accumulate in TMEM), which
+//              reads both CTAs' operands and writes each CTA's 128 rows to that
+//              CTA's TMEM; 2 accumulators of 256 columns let the epilogue of one
+//              tile overlap the next tile's K loop;
+//   warps 2-5  epilogue, in each CTA: tcgen05.ld of its accumulator rows, GELU
+//              and bf16 rounding (GEMM1) or float32 (GEMM2), streaming stores.
+// Per SM the pair tile halves the operand bytes fetched from L2 and staged in
+// shared memory per FLOP compared with a 128x256 single-SM tile. Tiles are
+// walked in groups of 16 M-tiles so that the pairs running at one time share
+// operand panels in L2.
 //
 // The row-parallel GEMM has two forms. Separate: each rank's Y_i B_i is a
 // float32 partial, and a multi-source kernel sums the partials (the
@@ -45,26 +51,18 @@ namespace rtp {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KB
-constexpr uint32_t B_SUB = 64 * BK * 2;    // one 64(N) x 64(K) box, 8 KB
-constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KB
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BN = 256, BK = 64;
+constexpr uint32_t B_SUB = 64 * BK * 2;  // one 64(N) x 64(K) box, 8 KB
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int GROUP_M = 16;
+constexpr int kOverlapBlocksPerSm = 1;  // reduction blocks per SM while a GEMM runs beside it
 constexpr int MAX_GROUPS = 8;
-constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /* barriers */ + 1024 /* alignment */;
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;
 
 enum : uint32_t { ERR_PRODUCER = 1, ERR_MMA_STAGE = 2, ERR_MMA_ACC = 3, ERR_EPILOGUE = 4 };
 enum { EPI_GELU_BF16 = 0, EPI_F32 = 1 };
 
-// Instruction descriptor of tcgen05.mma kind::f16: D float32 (bits 4-5 = 1),
-// A and B bf16 (bits 7-9 = 1, 10-12 = 1), A K-major (bit 15 = 0), B N-major
-// (bit 16 = 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
-                           ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 
 struct GemmArgs {
     CUtensorMap ta[MAX_GROUPS];  // K-major operand of each group: rows x K
@@ -92,11 +90,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
@@ -146,14 +139,6 @@ __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity)
         if (global_ns() - t0 > 200000000ull) break;
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-        : "memory");
-}
-
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -169,21 +154,6 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 {
     return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(IDESC), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32])
@@ -223,31 +193,113 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
 }
 
 // ---- the kernel ----------------------------------------------------------------------
+//
+// CTA r of the pair holds rows [128r, 128r+128) of the K-major operand and
+// columns [128r, 128r+128) of the N-major operand. Barriers:
+//   full[s]      in the leader: expects both CTAs' TMA bytes (one arrival, the
+//                leader's expect_tx); each CTA's loads signal it (cta_group::2)
+//   empty[s]     in both CTAs: one arrival from the leader's commit (multicast)
+//   acc_full[x]  in both CTAs: the leader's commit after a tile's last MMA
+//   acc_empty[x] in the leader: 8 arrivals, the 4 epilogue warps of each CTA
+
+constexpr int BM2 = 256;
+constexpr int STAGES2 = 6;
+constexpr uint32_t A2_BYTES = 128 * BK * 2;           // 16 KB
+constexpr uint32_t B2_BYTES = 128 * BK * 2;           // 16 KB: 2 boxes of 64(N) x 64(K)
+constexpr uint32_t STAGE2_BYTES = A2_BYTES + B2_BYTES;  // 32 KB
+constexpr size_t SMEM2_BYTES = STAGES2 * STAGE2_BYTES + 1024 + 1024;
+// Instruction descriptor of tcgen05.mma kind::f16: D float32 (bits 4-5 = 1),
+// A and B bf16 (bits 7-9 = 1, 10-12 = 1), A K-major (bit 15 = 0), B N-major
+// (bit 16 = 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28 (M = 256 for the pair).
+constexpr uint32_t IDESC2 = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) | ((uint32_t)(256 >> 3) << 17) |
+                            ((uint32_t)(BM2 >> 4) << 24);
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t num_clusters()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// Address in the shared::cluster window of the same variable in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int x, int y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(IDESC2), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar)
+{
+    const uint16_t both = 3;
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+                 "h"(both)
+                 : "memory");
+}
+__device__ __forceinline__ void mma_commit_pair_local(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
 
 __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_constant__ GemmArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-    // bars: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES2 * STAGE2_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES2 + 5);
     volatile uint32_t* abort_flag = tmem_slot + 1;
     const uint32_t bar0 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(STAGES + s); };
-    auto acc_full = [&](int x) { return bar0 + 8u * (uint32_t)(2 * STAGES + x); };
-    auto acc_empty = [&](int x) { return bar0 + 8u * (uint32_t)(2 * STAGES + 2 + x); };
-    const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 4);
+    auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(STAGES2 + s); };
+    auto acc_full = [&](int x) { return bar0 + 8u * (uint32_t)(2 * STAGES2 + x); };
+    auto acc_empty = [&](int x) { return bar0 + 8u * (uint32_t)(2 * STAGES2 + 2 + x); };
+    const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES2 + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t cta = cluster_rank();
+    const int pair = (int)cluster_id(), npairs = (int)num_clusters();
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < STAGES2; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(acc_full(x), 1);
-            mbar_init(acc_empty(x), 4);  // one arrival per epilogue warp
+            mbar_init(acc_empty(x), 8);  // 4 epilogue warps in each CTA of the pair
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -260,126 +312,129 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
         }
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+        // one warp in each CTA of the pair allocates collectively
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(TMEM_COLS)
                      : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // the peer's barriers are initialised before any remote use
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int kbs = a.fused ? a.groups * a.kb_per_group : a.kb_per_group;
 
     if (warp == 0) {
-        // ---------------- TMA producer (one lane) ----------------
+        // ---------------- TMA producer (one lane per CTA) ----------------
         if (lane == 0) {
-        int stage = 0;
-        uint32_t phase = 0;
-        uint32_t issued = 0, issued_parity = 0;  // per stage: last load and its phase parity
-        bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < a.total_tiles; tile += gridDim.x) {
-            int g, mt, nt;
-            tile_coords(a, tile, g, mt, nt);
-            const int row = a.m0 + mt * BM, col = a.n0 + nt * BN;
-            for (int kb = 0; kb < kbs; ++kb) {
-                if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, ERR_PRODUCER)) {
-                    ok = false;
-                    break;
-                }
-                const int gg = a.fused ? kb / a.kb_per_group : g;
-                const int kk = a.fused ? kb - gg * a.kb_per_group : kb;
-                const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-                const uint32_t sb = sa + A_BYTES;
-                mbar_expect_tx(full_bar(stage), STAGE_BYTES);
-                tma_load_2d(sa, &a.ta[gg], full_bar(stage), kk * BK, row);
-#pragma unroll
-                for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * B_SUB, &a.tb[gg], full_bar(stage), col + 64 * j, kk * BK);
-                issued |= 1u << stage;
-                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued = 0, issued_parity = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < a.total_tiles; tile += npairs) {
+                int g, mt, nt;
+                tile_coords(a, tile, g, mt, nt);
+                const int row = a.m0 + mt * BM2 + (int)cta * 128, col = a.n0 + nt * BN + (int)cta * 128;
+                for (int kb = 0; kb < kbs; ++kb) {
+                    if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, ERR_PRODUCER)) {
+                        ok = false;
+                        break;
+                    }
+                    const int gg = a.fused ? kb / a.kb_per_group : g;
+                    const int kk = a.fused ? kb - gg * a.kb_per_group : kb;
+                    const uint32_t sa = smem_u32(smem + stage * STAGE2_BYTES);
+                    const uint32_t sb = sa + A2_BYTES;
+                    const uint32_t fb = map_to_rank(full_bar(stage), 0);
+                    if (cta == 0) mbar_expect_tx(full_bar(stage), 2 * STAGE2_BYTES);
+                    tma_load_2d_pair(sa, &a.ta[gg], fb, kk * BK, row);
+                    tma_load_2d_pair(sb, &a.tb[gg], fb, col, kk * BK);
+                    tma_load_2d_pair(sb + B_SUB, &a.tb[gg], fb, col + 64, kk * BK);
+                    issued |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES2) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
-        }
-        if (!ok) {
-            // let the loads already issued land before the CTA can exit
-            for (int s = 0; s < STAGES; ++s)
-                if ((issued >> s) & 1u) drain_wait(full_bar(s), (issued_parity >> s) & 1u);
-        }
+            if (!ok) {
+                if (cta == 0) {
+                    for (int s = 0; s < STAGES2; ++s)
+                        if ((issued >> s) & 1u) drain_wait(full_bar(s), (issued_parity >> s) & 1u);
+                } else {
+                    // the follower cannot wait on the leader's barrier: give its
+                    // last loads (microseconds) time to land
+                    const uint64_t t0 = global_ns();
+                    while (global_ns() - t0 < 2000000ull) {
+                    }
+                }
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ---------------- MMA issuer (one lane) ----------------
-        if (lane == 0) {
-        int stage = 0;
-        uint32_t phase = 0;
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < a.total_tiles; tile += gridDim.x) {
-            if (!wait_bar(acc_empty(acc), acc_phase ^ 1u, abort_flag, ERR_MMA_ACC)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-            for (int kb = 0; kb < kbs; ++kb) {
-                if (!wait_bar(full_bar(stage), phase, abort_flag, ERR_MMA_STAGE)) {
+        // ---------------- MMA issuer (one lane of the leader) ----------------
+        if (lane == 0 && cta == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < a.total_tiles; tile += npairs) {
+                if (!wait_bar(acc_empty(acc), acc_phase ^ 1u, abort_flag, ERR_MMA_ACC)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-                const uint32_t sb = sa + A_BYTES;
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < kbs; ++kb) {
+                    if (!wait_bar(full_bar(stage), phase, abort_flag, ERR_MMA_STAGE)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * STAGE2_BYTES);
+                    const uint32_t sb = sa + A2_BYTES;
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k) {
-                    // K-major A: advance 32 bytes (16 bf16) inside the 128-byte swizzle row;
-                    // 8-row groups are 1024 bytes apart.
-                    const uint64_t da = smem_desc(sa + 32u * k, 16u, 1024u);
-                    // N-major B: 16 K-rows = 2 groups of 8 rows of 128 bytes; the four
-                    // 64-wide N boxes are B_SUB bytes apart.
-                    const uint64_t db = smem_desc(sb + 2048u * k, B_SUB, 1024u);
-                    mma_bf16(d_tmem, da, db, (kb > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint64_t da = smem_desc(sa + 32u * k, 16u, 1024u);
+                        const uint64_t db = smem_desc(sb + 2048u * k, B_SUB, 1024u);
+                        mma_bf16_pair(d_tmem, da, db, (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit_pair(empty_bar(stage));
+                    if (++stage == STAGES2) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
-                mma_commit(empty_bar(stage));
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
+                if (!ok) break;
+                mma_commit_pair(acc_full(acc));
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
                 }
             }
-            if (!ok) break;
-            mma_commit(acc_full(acc));
-            if (++acc == 2) {
-                acc = 0;
-                acc_phase ^= 1u;
+            if (!ok || *abort_flag) {
+                mma_commit_pair_local(drain_bar);
+                drain_wait(drain_bar, 0);
             }
-        }
-        if (!ok || *abort_flag) {
-            // MMAs already issued must finish before TMEM is freed
-            mma_commit(drain_bar);
-            drain_wait(drain_bar, 0);
-        }
         }
         __syncwarp();
     } else {
-        // ---------------- epilogue ----------------
-        const int quarter = warp & 3;  // TMEM lanes this warp may read
+        // ---------------- epilogue (both CTAs) ----------------
+        const int quarter = warp & 3;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < a.total_tiles; tile += gridDim.x) {
+        for (int tile = pair; tile < a.total_tiles; tile += npairs) {
             int g, mt, nt;
             tile_coords(a, tile, g, mt, nt);
-            // one lane waits; the warp follows its verdict so that the
-            // .sync.aligned TMEM loads below always run on a converged warp
             int ok = 1;
             if (lane == 0) ok = wait_bar(acc_full(acc), acc_phase, abort_flag, ERR_EPILOGUE) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            const int64_t row = a.m0 + mt * BM + quarter * 32 + lane;
-            const int64_t col = a.n0 + nt * BN;
+            const int64_t row = a.m0 + (int64_t)mt * BM2 + cta * 128 + quarter * 32 + lane;
+            const int64_t col = a.n0 + (int64_t)nt * BN;
             const bool row_ok = row < a.m_end;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
             for (int c = 0; c < BN / 32; ++c) {
@@ -388,8 +443,6 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
                 tmem_ld_wait();
                 const int64_t c0 = col + 32 * c;
                 if (!row_ok || c0 >= a.n_end) continue;
-                // 16-byte pieces; a piece is stored only if it lies inside the window
-                // (window edges are multiples of 8 columns)
                 if (a.epi == EPI_GELU_BF16) {
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out[g]) + row * a.ldo + c0);
 #pragma unroll
@@ -400,7 +453,7 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
                         v.y = pack_bf16(gelu(__uint_as_float(r[8 * q + 2])), gelu(__uint_as_float(r[8 * q + 3])));
                         v.z = pack_bf16(gelu(__uint_as_float(r[8 * q + 4])), gelu(__uint_as_float(r[8 * q + 5])));
                         v.w = pack_bf16(gelu(__uint_as_float(r[8 * q + 6])), gelu(__uint_as_float(r[8 * q + 7])));
-                        dst[q] = v;
+                        __stcs(dst + q, v);
                     }
                 } else {
                     float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out[g]) + row * a.ldo + c0);
@@ -414,7 +467,7 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty(acc));
+            if (lane == 0) mbar_arrive_cluster(map_to_rank(acc_empty(acc), 0));
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -423,8 +476,10 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // no CTA leaves while its peer may still signal or read it
     tc_fence_after();
-    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
 }
 
 // ---- host side --------------------------------------------------------------------
@@ -459,31 +514,38 @@ int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int bo
     return RTP_OK;
 }
 
-int sm_count_now()
-{
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
-}
-
 int launch_gemm(GemmArgs& args, cudaStream_t stream)
 {
     static bool configured[64] = {};
+    static int max_clusters[64] = {};
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tp_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(RTP_ECUDA, "tp_mlp: no CUDA device");
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM2_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (!configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(tp_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM2_BYTES);
         if (e != cudaSuccess) return fail(RTP_ECUDA, "tp_mlp: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        cfg.gridDim = dim3(2 * 64);
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, tp_gemm_kernel, &cfg);
+        if (e != cudaSuccess || n <= 0) return fail(RTP_ECUDA, "tp_mlp: cudaOccupancyMaxActiveClusters: %s", cudaGetErrorString(e));
+        max_clusters[dev] = n;
         configured[dev] = true;
     }
-    const int sms = sm_count_now();
-    if (sms <= 0) return fail(RTP_ECUDA, "tp_mlp: no CUDA device");
     args.total_tiles = (args.fused ? 1 : args.groups) * args.m_tiles * args.n_tiles;
-    const int grid = args.total_tiles < sms ? args.total_tiles : sms;
-    if (grid <= 0) return RTP_OK;
-    tp_gemm_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(args);
-    cudaError_t e = cudaGetLastError();
+    const int clusters = args.total_tiles < max_clusters[dev] ? args.total_tiles : max_clusters[dev];
+    if (clusters <= 0) return RTP_OK;
+    cfg.gridDim = dim3(2 * clusters);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, tp_gemm_kernel, args);
     if (e != cudaSuccess) return fail(RTP_ECUDA, "tp_mlp: GEMM launch failed: %s", cudaGetErrorString(e));
     return RTP_OK;
 }
@@ -562,10 +624,10 @@ int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
     std::memset(&g2, 0, sizeof g2);
     int st;
     for (int i = 0; i < P; ++i) {
-        if ((st = make_map(&g1.ta[i], X, M, K, BM))) return st;
+        if ((st = make_map(&g1.ta[i], X, M, K, 128))) return st;
         if ((st = make_map(&g1.tb[i], A_shards[i], K, Fp, BK))) return st;
         g1.out[i] = Y[i];
-        if ((st = make_map(&g2.ta[i], Y[i], M, Fp, BM))) return st;
+        if ((st = make_map(&g2.ta[i], Y[i], M, Fp, 128))) return st;
         if ((st = make_map(&g2.tb[i], B_shards[i], Fp, N, BK))) return st;
         g2.out[i] = mode == 0 ? partials[i] : (void*)Z;
     }
@@ -573,7 +635,8 @@ int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
     g1.groups = P;
     g1.fused = 0;
     g1.epi = EPI_GELU_BF16;
-    g1.m_tiles = (int)((Mc + BM - 1) / BM);
+    const int bm = BM2;
+    g1.m_tiles = (int)((Mc + bm - 1) / bm);
     g1.n_tiles = (int)((Fp + BN - 1) / BN);
     g1.kb_per_group = (int)((K + BK - 1) / BK);
     g1.n0 = 0;
@@ -582,7 +645,7 @@ int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
     g2.groups = P;
     g2.fused = mode == 1;
     g2.epi = EPI_F32;
-    g2.m_tiles = (int)((Mc + BM - 1) / BM);
+    g2.m_tiles = (int)((Mc + bm - 1) / bm);
     g2.n_tiles = (int)((Nb + BN - 1) / BN);
     g2.kb_per_group = (int)((Fp + BK - 1) / BK);
 
@@ -621,7 +684,12 @@ int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
                     return fail(RTP_ECUDA, "tp_mlp: event ordering failed");
                 rs = s1;
             }
-            if ((st = launch_tasks(RTP_F32, tasks, (const void* const*)partials, zdst, rs, nullptr))) return st;
+            // Beside the next chunk's GEMM (one CTA per SM), the reduction runs one
+            // block per SM so that both fit on every SM at once; the last window's
+            // reduction has nothing to overlap and takes the whole GPU.
+            const bool last = c == chunks - 1 && b == col_blocks - 1;
+            const int bps = two_streams && !last ? kOverlapBlocksPerSm : 4;
+            if ((st = launch_tasks(RTP_F32, tasks, (const void* const*)partials, zdst, rs, nullptr, bps))) return st;
         }
     }
     if (mode == 0 && two_streams) {
