@@ -187,6 +187,8 @@ def run_ours(args, rank, world, local_rank):
     # ---- sweep inputs: pieces resident in HBM ----
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     sweep = []  # (label, dtype_code, src pieces, src, dst pieces, dst, bytes, launches)
+    shards = []  # (label, full tensor, spec, pieces, bytes, launches): shard() of the sweep's S/B sources
+    whole = rtp.spec_nd_sbp((1,), ("B",))
     for dtype, code in ((torch.float32, rtp.F32), (torch.bfloat16, rtp.BF16)):
         T = randn(SWEEP_SHAPE, dtype)
         partials = [randn(SWEEP_SHAPE, dtype) for _ in range(8)]
@@ -196,9 +198,11 @@ def run_ours(args, rank, world, local_rank):
                 outs = [torch.empty(rtp.shard_shape(SWEEP_SHAPE, dst, r), dtype=dtype, device=dev)
                         for r in range(dst.num_ranks)]
                 rd, wr, nt, nl = rtp.reshard_cost(code, SWEEP_SHAPE, src, dst)
-                sweep.append(("%s %s %s" % (str(dtype).split(".")[-1], mesh_name, name), code, ins, src, outs, dst,
-                              rd + wr, nl))
-        del T
+                label = "%s %s %s" % (str(dtype).split(".")[-1], mesh_name, name)
+                sweep.append((label, code, ins, src, outs, dst, rd + wr, nl))
+                if not partial:
+                    srd, swr, _, snl = rtp.reshard_cost(code, SWEEP_SHAPE, whole, src)
+                    shards.append((label, T, src, ins, srd + swr, snl))
     torch.cuda.synchronize()
 
     # ---- MLP inputs ----
@@ -235,10 +239,20 @@ def run_ours(args, rank, world, local_rank):
 
     ops = [(label, (lambda c=c, i=i, s=s, o=o, d=d: rtp.reshard(i, SWEEP_SHAPE, s, d, out=o)), nbytes, nl)
            for (label, c, i, s, o, d, nbytes, nl) in sweep]
-    launches_per_step = sum(x[3] for x in ops) + 2 + 6 + 3 + 1  # mlp 2, domino 2x3, serial 3, reduce 1
+    shard_ops = [(label, (lambda T=T, sp=sp, o=o: rtp.shard(T, sp, out=o)), nbytes, nl)
+                 for (label, T, sp, o, nbytes, nl) in shards]
+    launches_per_step = (sum(x[3] for x in ops) + sum(x[3] for x in shard_ops) +
+                         2 + 6 + 3 + 1)  # mlp 2, domino 2x3, serial 3, reduce 1
     E = lambda: torch.cuda.Event(enable_timing=True)
 
     def step(record):
+        for label, fn, nbytes, nl in shard_ops:
+            flush.zero_()
+            e0, e1 = E(), E()
+            e0.record()
+            fn()
+            e1.record()
+            record.append(("shard", label, e0, e1, nbytes))
         for label, fn, nbytes, nl in ops:
             flush.zero_()
             e0, e1 = E(), E()
@@ -293,6 +307,29 @@ def run_ours(args, rank, world, local_rank):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
 
+    def gbs_of(kind, pred=lambda label: True):
+        ms = sum(v[0] for (k, l), v in per.items() if k == kind and pred(l))
+        by = sum(v[2] * v[1] for (k, l), v in per.items() if k == kind and pred(l))
+        return by / (ms * 1e-3) / 1e9 if ms > 0 else None
+
+    red_bytes = 8 * DOMINO["M"] * DOMINO["N"] * 4 + DOMINO["M"] * DOMINO["N"] * 4
+    host = host_inference_timings(rtp)
+    rows = {
+        "a1_shard": {"gbs": round(gbs_of("shard"), 1), "frac_hbm": round(gbs_of("shard") / hbm_peak, 4),
+                     "calls_per_step": len(shard_ops)},
+        "a2_reshard_S_B": {"gbs": round(gbs_of("reshard", lambda l: "P8" not in l), 1),
+                           "frac_hbm": round(gbs_of("reshard", lambda l: "P8" not in l) / hbm_peak, 4)},
+        "a3_reshard_P": {"gbs": round(gbs_of("reshard", lambda l: "P8" in l), 1),
+                         "frac_hbm": round(gbs_of("reshard", lambda l: "P8" in l) / hbm_peak, 4)},
+        "a4_infer_spmd": {"us_per_call": host["infer_spmd_us"], "where": "host"},
+        "a4p_reshape_rule": {"us_per_call": host["infer_reshape_us"], "where": "host"},
+        "a5_a6_a7_tp_mlp_fused": {"tflops": None, "frac_bf16": None},
+        "a7_reduce_separate": {"ms": round(red_ms, 4), "gbs": round(red_bytes / (red_ms * 1e-3) / 1e9, 1),
+                               "frac_hbm": round(red_bytes / (red_ms * 1e-3) / 1e9 / hbm_peak, 4),
+                               "shape": "8 float32 partials [4096,8192] -> Z"},
+        "a6_a7_separate_schedule": {"ms": round(ser_ms, 4), "tflops": round(DOMINO_FLOPS / (ser_ms * 1e-3) / 1e12, 1)},
+        "a8_domino": {"ms": round(dom_ms, 4), "hiding": round((ser_ms - dom_ms) / red_ms, 3) if red_ms > 0 else None},
+    }
     reshard_ms = max_over_ranks(reshard_ms)
     mlp_ms = max_over_ranks(mlp_ms)
     wall_ms = max_over_ranks(wall_ms)
@@ -300,6 +337,7 @@ def run_ours(args, rank, world, local_rank):
     tflops = MLP_FLOPS * args.steps * world / (mlp_ms * 1e-3) / 1e12
     per_launch_gbs = reshard_bytes / (reshard_ms * 1e-3) / 1e9
 
+    rows["a5_a6_a7_tp_mlp_fused"] = {"tflops": round(tflops / world, 1), "frac_bf16": round(tflops / world / bf16_peak, 4)}
     result = {
         "metric": METRIC,
         "value": round(gbs, 1),
@@ -330,6 +368,7 @@ def run_ours(args, rank, world, local_rank):
                    "ms_reduce_alone": round(red_ms, 4),
                    "hiding": round((ser_ms - dom_ms) / red_ms, 3) if red_ms > 0 else None,
                    "tflops_overlap": round(DOMINO_FLOPS / (dom_ms * 1e-3) / 1e12, 1)},
+        "rows": rows,
         "per_transition_gbs": {label: round(v[2] * v[1] / (v[0] * 1e-3) / 1e9, 1)
                                for (k, label), v in per.items() if k == "reshard"},
         "gpu_launches": launches_per_step * args.steps,
@@ -338,12 +377,26 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and not args.no_e2e:
         result["e2e"] = e2e_sweep(rtp, torch, dev, sweep)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(max_seconds=args.cpu_seconds)
+        result["cpu_baseline"] = cpu_baseline(max_seconds=args.cpu_seconds, with_mlp=True)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def host_inference_timings(rtp, reps: int = 2000):
+    """Host-side inference: the Paddle matmul example (mk,kn->mn on a 2D mesh)
+    and the reshape [2,3,4096] -> [6,4096]; microseconds per call."""
+    t = time.perf_counter()
+    for _ in range(reps):
+        rtp.infer_spmd("mk,kn->mn", [[0, -1], [-1, 1]], 2)
+    a = (time.perf_counter() - t) / reps * 1e6
+    t = time.perf_counter()
+    for _ in range(reps):
+        rtp.infer_reshape([2, 3, 4096], [0, -1, -1], [6, 4096], [2])
+    b = (time.perf_counter() - t) / reps * 1e6
+    return {"infer_spmd_us": round(a, 2), "infer_reshape_us": round(b, 2)}
 
 
 MLP_FLOPS = 2 * MLP["M"] * MLP["K"] * MLP["F"] + 2 * MLP["M"] * MLP["F"] * MLP["N"]
@@ -384,7 +437,7 @@ def e2e_sweep(rtp, torch, dev, sweep):
 CPU_SAMPLE_SHAPE = (8, 64, 4096)
 
 
-def cpu_baseline(max_seconds: float = 20.0, steps: int = 1):
+def cpu_baseline(max_seconds: float = 20.0, steps: int = 1, with_mlp: bool = False):
     """The oracle (single-threaded C++) on a bounded sample of the sweep: the
     twelve float32 transitions on a [8,64,4096] slice of the activation
     tensor (same meshes and specs), GB/s of algorithmic bytes."""
@@ -413,9 +466,36 @@ def cpu_baseline(max_seconds: float = 20.0, steps: int = 1):
             done += 1
             if time.perf_counter() - t_start > max_seconds:
                 break
-    return {"value": round(total_bytes / total_s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "%d float32 reshard calls of the sweep on a [8,64,4096] slice (meshes 1x8 and 2x4)" % done,
-            "seconds": round(total_s, 2), "host_cores": os.cpu_count()}
+    out = {"value": round(total_bytes / total_s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": "%d float32 reshard calls of the sweep on a [8,64,4096] slice (meshes 1x8 and 2x4)" % done,
+           "seconds": round(total_s, 2), "host_cores": os.cpu_count()}
+    if with_mlp:
+        out["tp_mlp"] = cpu_mlp_baseline()
+    return out
+
+
+def cpu_mlp_baseline(rows: int = 2):
+    """The oracle's TP-MLP (float64) on `rows` rows of the 8192x4096x16384x4096
+    configuration, all columns; TFLOP/s of the sample (its full-size time is
+    the sample time x 8192 / rows)."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    M, K, F, N, P = MLP["M"], MLP["K"], MLP["F"], MLP["N"], MLP["P"]
+    X = synth.normal(40, (rows, K), "bf16")
+    A = synth.normal(41, (K, F), "bf16", std=0.02)
+    B = synth.normal(42, (F, N), "bf16", std=0.02)
+    As = [np.ascontiguousarray(a) for a in np.split(A, P, axis=1)]
+    Bs = [np.ascontiguousarray(b) for b in np.split(B, P, axis=0)]
+    t = time.perf_counter()
+    oracle.tp_mlp(X, As, Bs)
+    dt = time.perf_counter() - t
+    flops = 2 * rows * K * F + 2 * rows * F * N
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": "%d rows of Z (all 4096 columns) of the 8192x4096x16384x4096 P=8 MLP" % rows,
+            "seconds": round(dt, 2), "full_size_seconds_extrapolated": round(dt * M / rows, 1)}
 
 
 def _distinct_reads(pieces, layout, oracle, shape):
