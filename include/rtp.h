@@ -60,8 +60,24 @@ typedef enum {
     RTP_ENOMEM = -6        /* host-side allocation failed */
 } rtp_status;
 
-/* Per-mesh-dim distribution (OneFlow SBP page: split, broadcast, partial). */
-typedef enum { RTP_SBP_SPLIT = 0, RTP_SBP_BROADCAST = 1, RTP_SBP_PARTIAL_SUM = 2 } rtp_sbp;
+/*
+ * Per-mesh-dim distribution (OneFlow SBP page: split, broadcast, partial; the
+ * page notes that besides sum, min and max also work as partial reductions).
+ * All partial mesh dims of one spec use the same reduction (else
+ * RTP_EUNSUPPORTED). When a logical tensor is sharded to a partial layout,
+ * the rank whose partial coordinates are all zero holds the tensor and the
+ * others hold the reduction's identity: 0 (sum), +inf (min), -inf (max).
+ * Min and max are exact, so their reshards are bit-exact; they follow IEEE
+ * minNum/maxNum (a NaN member is ignored unless all members are NaN) and may
+ * return either zero for min/max of +0 and -0.
+ */
+typedef enum {
+    RTP_SBP_SPLIT = 0,
+    RTP_SBP_BROADCAST = 1,
+    RTP_SBP_PARTIAL_SUM = 2,
+    RTP_SBP_PARTIAL_MIN = 3,
+    RTP_SBP_PARTIAL_MAX = 4
+} rtp_sbp;
 
 /* A CUDA stream (cudaStream_t) passed as an opaque pointer; NULL = default stream. */
 typedef void* rtp_stream;
@@ -188,6 +204,35 @@ int rtp_reshard_cost(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_
 int rtp_infer_spmd(const char* einsum, int n_in, const int32_t* const* in_dims_mappings, int mesh_ndim,
                    int32_t* out_dims_mapping, uint32_t* out_partial_mask, uint32_t* in_needs_reshard_mask,
                    int32_t* const* in_inferred);
+
+/*
+ * SBP-signature inference for an element-wise n-ary op (OneFlow page, the
+ * add_n walk-through: candidate set, filters, sort by OrderValue then
+ * CopyCost). Host only.
+ *   n_in inputs of one logical shape [ndim] with element size elem_bytes;
+ *   in_kinds / in_axes: [n_in * mesh_ndim], input j's ND-SBP (rtp_sbp kind
+ *   and split axis per mesh dim; mesh_ndim = 1 is the 1D case)
+ *   constraint_kinds / constraint_axes: [mesh_ndim] required ND-SBP of the
+ *   signature, or NULL for none
+ *   out_kinds / out_axes: [mesh_ndim] the chosen signature (every input and
+ *   the output take it); out_cost: its CopyCost; out_order: its OrderValue
+ * Candidates per mesh dim: split(i) for every axis i, partial-sum, broadcast
+ * (in that order); on an ND mesh, every combination (mesh dim 0 varies
+ * slowest). A candidate whose split axis is not an axis of the tensor is
+ * dropped, and so is one that differs from the constraint.
+ * OrderValue: -10 for every input already in the candidate's SBP (0 for all
+ * candidates when a constraint is given). CopyCost, summed over inputs: 0 if
+ * the input's SBP equals the candidate's; otherwise a huge number (1e30) if
+ * the input is partial-sum or broadcast on some mesh dim, else the input's
+ * bytes. The least (OrderValue, CopyCost) wins; ties keep candidate order.
+ * Reading: "partial_sum and broadcast cost a huge number" refers to the input's
+ * current SBP; the page's example (split + broadcast inputs infer broadcast)
+ * only holds under that reading.
+ */
+int rtp_infer_sbp_signature(int n_in, int ndim, const int64_t* shape, int elem_bytes, int mesh_ndim,
+                            const int32_t* in_kinds, const int32_t* in_axes, const int32_t* constraint_kinds,
+                            const int32_t* constraint_axes, int32_t* out_kinds, int32_t* out_axes, double* out_cost,
+                            int32_t* out_order);
 
 /*
  * Reshape rule (Paddle note, DimTrans: InputDim, Flatten, Split, Singleton).

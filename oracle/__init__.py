@@ -7,8 +7,8 @@ shares no code with the CUDA library; the only common dependency is the
 seeded input generator in ``synth``.
 
 Layouts are passed in the ND-SBP form: a mesh shape, a row-major list of
-device ids on the mesh, and per mesh dim one of ``("S", axis)``, ``"B"`` or
-``"P"``. ``layout_from_dims_mapping`` and ``layout_from_onnx`` turn the Paddle
+device ids on the mesh, and per mesh dim one of ``("S", axis)``, ``"B"``,
+``"P"`` (partial sum), ``"Pmin"`` or ``"Pmax"`` (partial min / max). ``layout_from_dims_mapping`` and ``layout_from_onnx`` turn the Paddle
 and ONNX descriptions into that form.
 
 Parity status: every function here is pinned by tests in
@@ -77,8 +77,8 @@ class Layout:
         for d, e in enumerate(self.entries):
             if e == "B":
                 L.kind[d], L.axis[d] = ord("B"), -1
-            elif e == "P":
-                L.kind[d], L.axis[d] = ord("P"), -1
+            elif e in ("P", "Pmin", "Pmax"):
+                L.kind[d], L.axis[d] = ord({"P": "P", "Pmin": "N", "Pmax": "X"}[e]), -1
             else:
                 L.kind[d], L.axis[d] = ord("S"), int(e[1])
         return L
@@ -89,7 +89,7 @@ class Layout:
         entries = []
         for d in range(L.mesh_ndim):
             k = chr(L.kind[d])
-            entries.append(("S", L.axis[d]) if k == "S" else k)
+            entries.append(("S", L.axis[d]) if k == "S" else {"N": "Pmin", "X": "Pmax"}.get(k, k))
         n = int(np.prod(mesh))
         return Layout(mesh, tuple(entries), tuple(L.devices[p] for p in range(n)))
 
@@ -123,6 +123,10 @@ def _load():
                                       P(i32p)]
     lib.oracle_reshape_spmd.argtypes = [ctypes.c_int, i64p, i32p, ctypes.c_int, i64p, ctypes.c_int, i64p, i32p,
                                         i32p, i32p, i32p, i32p, i32p, i32p]
+    i8p = P(ctypes.c_int8)
+    lib.oracle_infer_sbp_signature.argtypes = [ctypes.c_int, ctypes.c_int, i64p, ctypes.c_int, ctypes.c_int, i8p,
+                                               i32p, i8p, i32p, i8p, i32p, dblp, i32p, i32p]
+    lib.oracle_infer_sbp_signature.restype = ctypes.c_int
     lib.oracle_bf16_round.argtypes = [ctypes.c_double]
     lib.oracle_bf16_round.restype = ctypes.c_uint16
     lib.oracle_gelu.argtypes = [ctypes.c_double]
@@ -279,6 +283,47 @@ def reshape_spmd(in_shape, in_dims_mapping, out_shape, mesh):
                                     _i64(mesh), after, outm, k, f, c, p, n), "reshape_spmd")
     dts = [(DIMTRANS[k[o]], f[o], c[o], p[o], n[o]) for o in range(no)]
     return [after[i] for i in range(ni)], [outm[o] for o in range(no)], dts
+
+
+def _sbp_code(e):
+    if e in ("B", "P"):
+        return ord(e), -1
+    if e in ("Pmin", "Pmax"):
+        return ord("N" if e == "Pmin" else "X"), -1
+    return ord("S"), int(e[1])
+
+
+def infer_sbp_signature(shape, elem_bytes, inputs, constraint=None):
+    """inputs: per input, its ND-SBP as a list of entries ("S", axis) / "B" / "P"
+    (one per mesh dim). Returns (signature entries, CopyCost, OrderValue,
+    number of candidates kept)."""
+    n_in = len(inputs)
+    md = len(inputs[0])
+    kinds, axes = [], []
+    for sbp in inputs:
+        for e in sbp:
+            k, a = _sbp_code(e)
+            kinds.append(k)
+            axes.append(a)
+    I8 = ctypes.c_int8
+    ck = ca = None
+    if constraint is not None:
+        c = [_sbp_code(e) for e in constraint]
+        ck = (I8 * md)(*[k for k, _ in c])
+        ca = _i32([a for _, a in c])
+    ok_, oa = (I8 * md)(), _i32([0] * md)
+    cost, order, ncand = ctypes.c_double(), ctypes.c_int32(), ctypes.c_int32()
+    rc = _load().oracle_infer_sbp_signature(n_in, len(shape), _i64(shape), elem_bytes, md,
+                                            (I8 * len(kinds))(*kinds), _i32(axes), ck, ca, ok_, oa,
+                                            ctypes.byref(cost), ctypes.byref(order), ctypes.byref(ncand))
+    if rc == -2:
+        raise OracleError("no candidate satisfies the constraint")
+    _ok(rc, "infer_sbp_signature")
+    sig = []
+    for d in range(md):
+        k = chr(ok_[d])
+        sig.append(("S", oa[d]) if k == "S" else k)
+    return sig, cost.value, order.value, ncand.value
 
 
 # ---- scalars and the TP-MLP -----------------------------------------------------

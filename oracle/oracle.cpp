@@ -26,8 +26,10 @@
 // Readings where the pages are silent (each is listed in the design notes):
 //   * uneven extents: ceil-sized leading shards, applied level by level;
 //   * shard() of a partial layout: the device whose partial coordinates are
-//     all zero holds the tensor, the others hold zeros;
+//     all zero holds the tensor, the others hold the reduction's identity
+//     (0 for sum, +inf for min, -inf for max);
 //   * GELU is the exact erf form; Y is rounded to bf16 before the second GEMM.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -45,7 +47,9 @@ constexpr int kMaxDim = 8;
 extern "C" {
 
 // A layout in the ND-SBP form: a row-major mesh of device ids and one entry per
-// mesh dim: 'S' (split tensor axis `axis`), 'B' (broadcast) or 'P' (partial sum).
+// mesh dim: 'S' (split tensor axis `axis`), 'B' (broadcast), or a partial
+// reduction: 'P' (sum), 'N' (min) or 'X' (max). The OneFlow SBP page defines
+// partial by sum and notes that min and max work the same way.
 struct OracleLayout {
     int32_t mesh_ndim;
     int64_t mesh_shape[kMaxMesh];
@@ -105,10 +109,29 @@ void slice_of(const OracleLayout& L, int ndim, const int64_t* shape, const int64
     }
 }
 
+bool is_partial_kind(int8_t k) { return k == 'P' || k == 'N' || k == 'X'; }
+
+// The partial reduction of a layout ('P', 'N' or 'X'; 'P' when there is none).
+int8_t reduction_of(const OracleLayout& L)
+{
+    for (int d = 0; d < L.mesh_ndim; ++d)
+        if (is_partial_kind(L.kind[d])) return L.kind[d];
+    return 'P';
+}
+
+// What members of a partial group that do not hold the tensor contain: the
+// value that leaves the reduction unchanged.
+double identity_of(int8_t reduction)
+{
+    if (reduction == 'N') return INFINITY;
+    if (reduction == 'X') return -INFINITY;
+    return 0.0;
+}
+
 bool holds_partial_value(const OracleLayout& L, const int64_t* c)
 {
     for (int d = 0; d < L.mesh_ndim; ++d)
-        if (L.kind[d] == 'P' && c[d] != 0) return false;
+        if (is_partial_kind(L.kind[d]) && c[d] != 0) return false;
     return true;
 }
 
@@ -131,8 +154,10 @@ int check_layout(const OracleLayout& L, int ndim)
         seen[v] = 1;
     }
     for (int d = 0; d < L.mesh_ndim; ++d) {
-        if (L.kind[d] != 'S' && L.kind[d] != 'B' && L.kind[d] != 'P') return -1;
+        if (L.kind[d] != 'S' && L.kind[d] != 'B' && !is_partial_kind(L.kind[d])) return -1;
         if (L.kind[d] == 'S' && (L.axis[d] < 0 || L.axis[d] >= ndim)) return -1;
+        for (int e = 0; e < d; ++e)  // one reduction per layout
+            if (is_partial_kind(L.kind[d]) && is_partial_kind(L.kind[e]) && L.kind[d] != L.kind[e]) return -1;
     }
     return 0;
 }
@@ -235,7 +260,7 @@ int oracle_shard(int dtype, int ndim, const int64_t* shape, const void* full, co
         int64_t k = 0;
         do {
             for (int a = 0; a < ndim; ++a) g[a] = lo[a] + e[a];
-            double v = value ? load(dtype, full, linear(ndim, shape, g)) : 0.0;
+            double v = value ? load(dtype, full, linear(ndim, shape, g)) : identity_of(reduction_of(*L));
             store(dtype, out[dev], k++, v);
         } while (next_index(ndim, ext, e));
     }
@@ -244,14 +269,16 @@ int oracle_shard(int dtype, int ndim, const int64_t* shape, const void* full, co
 
 // The logical tensor (in double) described by per-device pieces `in` laid out
 // by L: pieces of B replicas other than coordinate 0 are skipped, partial
-// pieces are added.
+// pieces are combined by the layout's reduction (sum in double; min / max
+// with the IEEE minNum / maxNum of std::fmin / std::fmax).
 int oracle_gather(int dtype, int ndim, const int64_t* shape, const void* const* in, const OracleLayout* L,
                   double* logical)
 {
     if (check_layout(*L, ndim)) return -1;
     int64_t total = 1;
     for (int a = 0; a < ndim; ++a) total *= shape[a];
-    for (int64_t i = 0; i < total; ++i) logical[i] = 0.0;
+    const int8_t red = reduction_of(*L);
+    for (int64_t i = 0; i < total; ++i) logical[i] = identity_of(red);
     int64_t n = num_devices(*L);
     for (int dev = 0; dev < n; ++dev) {
         int64_t c[kMaxMesh], lo[kMaxDim], hi[kMaxDim], ext[kMaxDim], e[kMaxDim], g[kMaxDim];
@@ -268,7 +295,11 @@ int oracle_gather(int dtype, int ndim, const int64_t* shape, const void* const* 
         int64_t k = 0;
         do {
             for (int a = 0; a < ndim; ++a) g[a] = lo[a] + e[a];
-            logical[linear(ndim, shape, g)] += load(dtype, in[dev], k++);
+            double& acc = logical[linear(ndim, shape, g)];
+            const double v = load(dtype, in[dev], k++);
+            if (red == 'N') acc = std::fmin(acc, v);
+            else if (red == 'X') acc = std::fmax(acc, v);
+            else acc += v;
         } while (next_index(ndim, ext, e));
     }
     return 0;
@@ -301,7 +332,7 @@ int oracle_reshard(int dtype, int ndim, const int64_t* shape, const void* const*
         int64_t k = 0;
         do {
             for (int a = 0; a < ndim; ++a) g[a] = lo[a] + e[a];
-            store(dtype, dst[dev], k++, value ? logical[linear(ndim, shape, g)] : 0.0);
+            store(dtype, dst[dev], k++, value ? logical[linear(ndim, shape, g)] : identity_of(reduction_of(*Ld)));
         } while (next_index(ndim, ext, e));
     }
     return 0;
@@ -587,6 +618,89 @@ int oracle_reshape_spmd(int in_ndim, const int64_t* in_shape, const int32_t* in_
         if (same) out_dims_mapping[lo] = d;
         else in_dims_after[li] = -1;
     }
+    return 0;
+}
+
+// ---- SBP signature inference (OneFlow page, add_n walk-through) -------------
+
+// A signature: one (kind, axis) per mesh dim, shared by every input and the
+// output of an element-wise op. kind: 'S' split(axis), 'P' partial sum,
+// 'B' broadcast (inputs may also be 'N' / 'X', partial min / max).
+struct Sig {
+    std::vector<std::pair<char, int>> dims;
+    int order = 0;
+    double cost = 0;
+};
+
+// Step 1: candidates. For one mesh dim the op offers split(i) for every axis
+// i of the input shape, then partial sum; broadcast is added by default. On an
+// ND mesh every slot takes any 1D candidate: the direct product, built with
+// mesh dim 0 varying slowest.
+// Step 2: filters: a split axis must be an axis of the tensor; a required
+// signature (constraint), when given, must match.
+// Step 3: sort by OrderValue (-10 per input already in the candidate's SBP,
+// 0 for all when a constraint is given), then by CopyCost (per input: 0 if
+// equal; a huge number when the input is partial or broadcast; else its
+// bytes), keeping the candidate order among equals; the first one wins.
+int oracle_infer_sbp_signature(int n_in, int ndim, const int64_t* shape, int elem_bytes, int mesh_ndim,
+                               const int8_t* in_kinds, const int32_t* in_axes, const int8_t* constraint_kinds,
+                               const int32_t* constraint_axes, int8_t* out_kinds, int32_t* out_axes, double* out_cost,
+                               int32_t* out_order, int32_t* n_candidates)
+{
+    if (n_in < 1 || ndim < 1 || mesh_ndim < 1 || mesh_ndim > kMaxMesh) return -1;
+    std::vector<std::pair<char, int>> one;
+    for (int i = 0; i < ndim; ++i) one.push_back({'S', i});
+    one.push_back({'P', -1});
+    one.push_back({'B', -1});
+    std::vector<Sig> cands(1);
+    for (int d = 0; d < mesh_ndim; ++d) {
+        std::vector<Sig> next;
+        for (const Sig& c : cands)
+            for (const auto& e : one) {
+                Sig n = c;
+                n.dims.push_back(e);
+                next.push_back(n);
+            }
+        cands = next;
+    }
+    std::vector<Sig> kept;
+    for (const Sig& c : cands) {
+        bool ok = true;
+        for (int d = 0; d < mesh_ndim; ++d) {
+            if (c.dims[d].first == 'S' && c.dims[d].second >= ndim) ok = false;
+            if (constraint_kinds && (constraint_kinds[d] != c.dims[d].first ||
+                                     (c.dims[d].first == 'S' && constraint_axes[d] != c.dims[d].second)))
+                ok = false;
+        }
+        if (ok) kept.push_back(c);
+    }
+    if (n_candidates) *n_candidates = (int32_t)kept.size();
+    if (kept.empty()) return -2;
+    double bytes = elem_bytes;
+    for (int a = 0; a < ndim; ++a) bytes *= (double)shape[a];
+    for (Sig& c : kept) {
+        for (int j = 0; j < n_in; ++j) {
+            bool same = true, partial_or_broadcast = false;
+            for (int d = 0; d < mesh_ndim; ++d) {
+                char k = (char)in_kinds[j * mesh_ndim + d];
+                int ax = in_axes[j * mesh_ndim + d];
+                if (k != 'S') partial_or_broadcast = true;
+                if (k != c.dims[d].first || (k == 'S' && ax != c.dims[d].second)) same = false;
+            }
+            if (same && !constraint_kinds) c.order -= 10;
+            if (!same) c.cost += partial_or_broadcast ? 1e30 : bytes;
+        }
+    }
+    std::stable_sort(kept.begin(), kept.end(), [](const Sig& a, const Sig& b) {
+        if (a.order != b.order) return a.order < b.order;
+        return a.cost < b.cost;
+    });
+    for (int d = 0; d < mesh_ndim; ++d) {
+        out_kinds[d] = (int8_t)kept[0].dims[d].first;
+        out_axes[d] = kept[0].dims[d].second;
+    }
+    *out_cost = kept[0].cost;
+    *out_order = kept[0].order;
     return 0;
 }
 

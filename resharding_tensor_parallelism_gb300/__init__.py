@@ -23,7 +23,7 @@ MAX_NDIM = 8
 MAX_MESH_NDIM = 4
 MAX_RANKS = 64
 F32, BF16 = 0, 1
-SPLIT, BROADCAST, PARTIAL = 0, 1, 2
+SPLIT, BROADCAST, PARTIAL, PARTIAL_MIN, PARTIAL_MAX = 0, 1, 2, 3, 4
 STATUS = {0: "RTP_OK", -1: "RTP_EINVAL", -2: "RTP_ESHAPE", -3: "RTP_EUNSUPPORTED", -4: "RTP_ECONFLICT",
           -5: "RTP_ECUDA", -6: "RTP_ENOMEM"}
 
@@ -56,7 +56,8 @@ class Spec(ctypes.Structure):
         ents = []
         for d in range(self.mesh_ndim):
             k = self.sbp_kind[d]
-            ents.append(("S", self.sbp_axis[d]) if k == SPLIT else ("B" if k == BROADCAST else "P"))
+            ents.append(("S", self.sbp_axis[d]) if k == SPLIT else
+                        {BROADCAST: "B", PARTIAL: "P", PARTIAL_MIN: "Pmin", PARTIAL_MAX: "Pmax"}[k])
         mesh = tuple(self.mesh_shape[d] for d in range(self.mesh_ndim))
         return mesh, tuple(ents), tuple(self.rank_ids[p] for p in range(self.num_ranks))
 
@@ -91,6 +92,8 @@ def _load():
         "rtp_reshard_cost": [c_int, c_int, i64p, P(Spec), P(Spec), i64p, i64p, i32p, i32p],
         "rtp_infer_spmd": [ctypes.c_char_p, c_int, P(i32p), c_int, i32p, u32p, u32p, P(i32p)],
         "rtp_infer_reshape": [c_int, i64p, i32p, c_int, i64p, c_int, i64p, i32p, i32p],
+        "rtp_infer_sbp_signature": [c_int, c_int, i64p, c_int, c_int, i32p, i32p, i32p, i32p, i32p, i32p,
+                                    P(ctypes.c_double), i32p],
         "rtp_device_error": [vp, u32p],
         "rtp_tp_mlp_noalloc": [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vpp, vpp,
                                vp, vp],
@@ -143,7 +146,8 @@ Entry = Union[str, Tuple[str, int]]
 
 
 def spec_nd_sbp(mesh: Sequence[int], entries: Sequence[Entry], rank_ids: Sequence[int] = ()) -> Spec:
-    """ND-SBP form: one entry per mesh dim, ("S", axis), "B" or "P" (OneFlow page)."""
+    """ND-SBP form: one entry per mesh dim, ("S", axis), "B", "P" (partial sum),
+    "Pmin" or "Pmax" (partial min / max) (OneFlow page)."""
     s = Spec()
     s.mesh_ndim = len(mesh)
     n = 1
@@ -158,8 +162,8 @@ def spec_nd_sbp(mesh: Sequence[int], entries: Sequence[Entry], rank_ids: Sequenc
     for d, e in enumerate(entries):
         if e == "B":
             s.sbp_kind[d], s.sbp_axis[d] = BROADCAST, -1
-        elif e == "P":
-            s.sbp_kind[d], s.sbp_axis[d] = PARTIAL, -1
+        elif e in ("P", "Pmin", "Pmax"):
+            s.sbp_kind[d], s.sbp_axis[d] = {"P": PARTIAL, "Pmin": PARTIAL_MIN, "Pmax": PARTIAL_MAX}[e], -1
         else:
             s.sbp_kind[d], s.sbp_axis[d] = SPLIT, int(e[1])
     return s
@@ -305,6 +309,40 @@ def infer_reshape(in_shape, in_dims_mapping, out_shape, mesh):
     _check(_load().rtp_infer_reshape(ni, _i64(in_shape), _i32(in_dims_mapping), no, _i64(out_shape), len(mesh),
                                      _i64(mesh), after, outm))
     return [after[i] for i in range(ni)], [outm[o] for o in range(no)]
+
+
+def _sbp_entry(e):
+    if e == "B":
+        return BROADCAST, -1
+    if e in ("P", "Pmin", "Pmax"):
+        return {"P": PARTIAL, "Pmin": PARTIAL_MIN, "Pmax": PARTIAL_MAX}[e], -1
+    return SPLIT, int(e[1])
+
+
+def infer_sbp_signature(shape, elem_bytes, inputs, constraint=None):
+    """OneFlow-style SBP signature of an element-wise op. inputs: per input its
+    ND-SBP (entries ("S", axis) / "B" / "P" per mesh dim). Returns
+    (signature entries, CopyCost, OrderValue)."""
+    md = len(inputs[0])
+    kinds, axes = [], []
+    for sbp in inputs:
+        for e in sbp:
+            k, a = _sbp_entry(e)
+            kinds.append(k)
+            axes.append(a)
+    ck = ca = None
+    if constraint is not None:
+        c = [_sbp_entry(e) for e in constraint]
+        ck, ca = _i32([k for k, _ in c]), _i32([a for _, a in c])
+    okind, oaxis = _i32([0] * md), _i32([0] * md)
+    cost, order = ctypes.c_double(), ctypes.c_int32()
+    _check(_load().rtp_infer_sbp_signature(len(inputs), len(shape), _i64(shape), elem_bytes, md, _i32(kinds),
+                                           _i32(axes), ck, ca, okind, oaxis, ctypes.byref(cost), ctypes.byref(order)))
+    sig = []
+    for d in range(md):
+        k = okind[d]
+        sig.append(("S", oaxis[d]) if k == SPLIT else {BROADCAST: "B", PARTIAL: "P"}[k])
+    return sig, cost.value, order.value
 
 
 # ---- tensor-parallel MLP ------------------------------------------------------------

@@ -16,7 +16,10 @@
 //   * a task with several destinations (broadcast pieces) reads its source
 //     once and writes every destination from registers;
 //   * a task with several sources (partial sums) adds them in float32 in a
-//     fixed order (partial coordinates row-major) and rounds once.
+//     fixed order (partial coordinates row-major) and rounds once; partial
+//     min / max members combine with fminf / fmaxf (exact);
+//   * a task with no source fills its destinations with the identity of the
+//     destination's partial reduction (0, +inf or -inf).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -42,6 +45,9 @@ struct KTask {
     int32_t vec;          // bytes per vector access
     int32_t n_outer, n_src, n_dst, ptr0;
     int32_t ext[kMaxOuter];
+    int32_t op;           // RED_SUM / RED_MIN / RED_MAX: how several sources combine
+    uint32_t fill;        // with no source: the element pattern written (the op's identity),
+                          // repeated to 32 bits for 16-bit elements
     int32_t pad_;
     int64_t sstr[kMaxOuter], dstr[kMaxOuter];
 };
@@ -153,7 +159,7 @@ __device__ __forceinline__ void run_chunk(const KParams& p, const KTask& t, int 
         if (ns == 0) {
             Lanes<VB> z;
 #pragma unroll
-            for (int k = 0; k < VB / 2; ++k) z.h[k] = 0;
+            for (int k = 0; k < VB / 2; ++k) z.h[k] = (uint16_t)(t.fill >> (16 * (k & 1)));
             for (int j = 0; j < nd; ++j)
 #pragma unroll
                 for (int u = 0; u < U; ++u)
@@ -174,6 +180,7 @@ __device__ __forceinline__ void run_chunk(const KParams& p, const KTask& t, int 
             for (int u = 0; u < U; ++u)
 #pragma unroll
                 for (int e = 0; e < NE; ++e) acc[u][e] = 0.f;
+            const int op = t.op;
 #pragma unroll 4
             for (int j = 0; j < ns; ++j) {
                 Lanes<VB> in[U];
@@ -187,7 +194,10 @@ __device__ __forceinline__ void run_chunk(const KParams& p, const KTask& t, int 
                         float x;
                         if constexpr (ES == 4) x = __uint_as_float(in[u].w[e]);
                         else x = __uint_as_float((uint32_t)in[u].h[e] << 16);
-                        acc[u][e] = j == 0 ? x : acc[u][e] + x;
+                        if (j == 0) acc[u][e] = x;
+                        else if (op == RED_SUM) acc[u][e] = acc[u][e] + x;
+                        else if (op == RED_MIN) acc[u][e] = fminf(acc[u][e], x);
+                        else acc[u][e] = fmaxf(acc[u][e], x);
                     }
             }
             Lanes<VB> out[U];
@@ -282,6 +292,10 @@ int64_t fill_task(KTask& k, const PlanTask& t, int vec, int es)
     }
     k.n_src = (int32_t)t.src.size();
     k.n_dst = (int32_t)t.dst.size();
+    k.op = t.op;
+    // identity of the reduction: 0 (sum), +inf (min), -inf (max)
+    if (es == 4) k.fill = t.op == RED_MIN ? 0x7F800000u : t.op == RED_MAX ? 0xFF800000u : 0u;
+    else k.fill = t.op == RED_MIN ? 0x7F807F80u : t.op == RED_MAX ? 0xFF80FF80u : 0u;
     const int64_t row_bytes = t.cols * es;
     const int64_t epv = vec / es;
     if (row_bytes >= kChunkBytes) {

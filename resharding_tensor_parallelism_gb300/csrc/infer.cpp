@@ -10,6 +10,10 @@
 //
 // The reshape rule follows the same note's DimTrans table (InputDim, Flatten,
 // Split, Singleton).
+//
+// rtp_infer_sbp_signature follows the OneFlow page's walk-through of SBP
+// signature inference for add_n: candidate set (split on every axis, partial
+// sum, broadcast), filters, and the sort by OrderValue then CopyCost.
 #include <cstring>
 #include <string>
 
@@ -185,3 +189,89 @@ int rtp_infer_reshape(int in_ndim, const int64_t* in_shape, const int32_t* in_di
 }
 
 }  // extern "C"
+
+extern "C" int rtp_infer_sbp_signature(int n_in, int ndim, const int64_t* shape, int elem_bytes, int mesh_ndim,
+                                       const int32_t* in_kinds, const int32_t* in_axes, const int32_t* constraint_kinds,
+                                       const int32_t* constraint_axes, int32_t* out_kinds, int32_t* out_axes,
+                                       double* out_cost, int32_t* out_order)
+{
+    const char* fn = "rtp_infer_sbp_signature";
+    if (!shape || !in_kinds || !in_axes || !out_kinds || !out_axes) return fail(RTP_EINVAL, "%s: NULL argument", fn);
+    if (n_in < 1 || ndim < 1 || ndim > RTP_MAX_NDIM || elem_bytes < 1)
+        return fail(RTP_EINVAL, "%s: n_in %d, ndim %d, elem_bytes %d", fn, n_in, ndim, elem_bytes);
+    if (mesh_ndim < 1 || mesh_ndim > RTP_MAX_MESH_NDIM) return fail(RTP_EINVAL, "%s: mesh_ndim %d", fn, mesh_ndim);
+    if ((constraint_kinds == nullptr) != (constraint_axes == nullptr))
+        return fail(RTP_EINVAL, "%s: constraint kinds and axes go together", fn);
+    int64_t bytes = elem_bytes;
+    for (int a = 0; a < ndim; ++a) bytes *= shape[a];
+    // per input: kind/axis per mesh dim; "same" compares whole ND-SBPs
+    auto entry_ok = [&](int k, int ax) {
+        return k == RTP_SBP_BROADCAST || k == RTP_SBP_PARTIAL_SUM || k == RTP_SBP_PARTIAL_MIN ||
+               k == RTP_SBP_PARTIAL_MAX || (k == RTP_SBP_SPLIT && ax >= 0);
+    };
+    for (int j = 0; j < n_in; ++j)
+        for (int d = 0; d < mesh_ndim; ++d)
+            if (!entry_ok(in_kinds[j * mesh_ndim + d], in_axes[j * mesh_ndim + d]))
+                return fail(RTP_EINVAL, "%s: input %d mesh dim %d has a bad SBP", fn, j, d);
+    // 1D candidates: S(0..ndim-1), P, B
+    const int n1 = ndim + 2;
+    auto kind_of = [&](int c) { return c < ndim ? RTP_SBP_SPLIT : (c == ndim ? RTP_SBP_PARTIAL_SUM : RTP_SBP_BROADCAST); };
+    auto axis_of = [&](int c) { return c < ndim ? c : -1; };
+    int64_t total = 1;
+    for (int d = 0; d < mesh_ndim; ++d) total *= n1;
+    bool found = false;
+    int64_t best = -1;
+    int best_order = 0;
+    double best_cost = 0;
+    for (int64_t cand = 0; cand < total; ++cand) {
+        int ck[RTP_MAX_MESH_NDIM], ca[RTP_MAX_MESH_NDIM];
+        int64_t rem = cand;
+        for (int d = mesh_ndim - 1; d >= 0; --d) {
+            int c = (int)(rem % n1);
+            rem /= n1;
+            ck[d] = kind_of(c);
+            ca[d] = axis_of(c);
+        }
+        // filter: split axes must be axes of the tensor (always true for these
+        // candidates); and the constraint, when given
+        bool keep = true;
+        for (int d = 0; d < mesh_ndim && keep; ++d) {
+            if (ck[d] == RTP_SBP_SPLIT && ca[d] >= ndim) keep = false;
+            if (constraint_kinds && (constraint_kinds[d] != ck[d] || (ck[d] == RTP_SBP_SPLIT && constraint_axes[d] != ca[d])))
+                keep = false;
+        }
+        if (!keep) continue;
+        int order = 0;
+        double cost = 0;
+        for (int j = 0; j < n_in; ++j) {
+            bool same = true, pb = false;
+            for (int d = 0; d < mesh_ndim; ++d) {
+                const int k = in_kinds[j * mesh_ndim + d], ax = in_axes[j * mesh_ndim + d];
+                if (k != ck[d] || (k == RTP_SBP_SPLIT && ax != ca[d])) same = false;
+                if (k != RTP_SBP_SPLIT) pb = true;  // broadcast or partial
+            }
+            if (same) {
+                if (!constraint_kinds) order -= 10;
+                continue;
+            }
+            cost += pb ? 1e30 : (double)bytes;
+        }
+        if (!found || order < best_order || (order == best_order && cost < best_cost)) {
+            found = true;
+            best = cand;
+            best_order = order;
+            best_cost = cost;
+        }
+    }
+    if (!found) return fail(RTP_ECONFLICT, "%s: no candidate signature satisfies the constraint", fn);
+    int64_t rem = best;
+    for (int d = mesh_ndim - 1; d >= 0; --d) {
+        int c = (int)(rem % n1);
+        rem /= n1;
+        out_kinds[d] = kind_of(c);
+        out_axes[d] = axis_of(c);
+    }
+    if (out_cost) *out_cost = best_cost;
+    if (out_order) *out_order = best_order;
+    return RTP_OK;
+}

@@ -152,6 +152,7 @@ int plan_reshard(int ndim, const int64_t* shape, const rtp_spec& src, const rtp_
             if (st) return st;
             for (auto& m : g.members) t.src.push_back(Ref{m.second, so});
             for (int r : dg.ranks) t.dst.push_back(Ref{r, dof});
+            t.op = partial_reduction(src);
             tasks->push_back(std::move(t));
         }
     }
@@ -161,6 +162,7 @@ int plan_reshard(int ndim, const int64_t* shape, const rtp_spec& src, const rtp_
         int st = make_task(ndim, dg.box.lo, dg.box.hi, dg.box, dg.box, &t, &so, &dof);
         if (st) return st;
         for (int r : dg.ranks) t.dst.push_back(Ref{r, dof});
+        t.op = partial_reduction(dst);  // filled with the identity of the destination's reduction
         tasks->push_back(std::move(t));
     }
     return RTP_OK;

@@ -18,13 +18,17 @@ void clear_error();
 int64_t num_ranks(const rtp_spec& s);
 // RTP_OK or an error (message recorded) if the spec cannot describe a tensor of rank ndim.
 int check_spec(int ndim, const rtp_spec& s, const char* what);
+// Reduction of a spec's partial mesh dims: RED_SUM (also when there are none), RED_MIN, RED_MAX.
+enum { RED_SUM = 0, RED_MIN = 1, RED_MAX = 2 };
+int partial_reduction(const rtp_spec& s);
+bool is_partial(int sbp_kind);
 // Mesh coordinates of every rank: coords[r * RTP_MAX_MESH_NDIM + d].
 void rank_coords(const rtp_spec& s, int64_t* coords);
 
 struct Box {
     int64_t lo[RTP_MAX_NDIM];
     int64_t hi[RTP_MAX_NDIM];
-    bool holds_value;  // false: zero-filled member of a partial group
+    bool holds_value;  // false: member of a partial group that holds the reduction's identity
     bool b_rep;        // coordinate 0 on every broadcast mesh dim
     int64_t pidx;      // index of the partial coordinates (row-major), 0 if no P dim
 };
@@ -50,6 +54,7 @@ struct PlanTask {
     int64_t dstr[kMaxOuter] = {};
     std::vector<Ref> src;
     std::vector<Ref> dst;
+    int op = RED_SUM;  // how several sources combine; with no source, dst is filled with op's identity
 };
 // Plans moving a tensor laid out by `src` into the layout `dst`.
 int plan_reshard(int ndim, const int64_t* shape, const rtp_spec& src, const rtp_spec& dst,

@@ -58,12 +58,26 @@ int check_spec(int ndim, const rtp_spec& s, const char* what)
     }
     for (int d = 0; d < s.mesh_ndim; ++d) {
         int k = s.sbp_kind[d];
-        if (k != RTP_SBP_SPLIT && k != RTP_SBP_BROADCAST && k != RTP_SBP_PARTIAL_SUM)
+        if (k != RTP_SBP_SPLIT && k != RTP_SBP_BROADCAST && !is_partial(k))
             return fail(RTP_EINVAL, "%s: mesh dim %d has unknown sbp kind %d", what, d, k);
+        for (int e = 0; e < d; ++e)
+            if (is_partial(k) && is_partial(s.sbp_kind[e]) && s.sbp_kind[e] != k)
+                return fail(RTP_EUNSUPPORTED, "%s: mesh dims %d and %d are partial with different reductions", what, e, d);
         if (k == RTP_SBP_SPLIT && (s.sbp_axis[d] < 0 || s.sbp_axis[d] >= ndim))
             return fail(RTP_EINVAL, "%s: mesh dim %d splits axis %d of a rank-%d tensor", what, d, s.sbp_axis[d], ndim);
     }
     return RTP_OK;
+}
+
+bool is_partial(int k) { return k == RTP_SBP_PARTIAL_SUM || k == RTP_SBP_PARTIAL_MIN || k == RTP_SBP_PARTIAL_MAX; }
+
+int partial_reduction(const rtp_spec& s)
+{
+    for (int d = 0; d < s.mesh_ndim; ++d) {
+        if (s.sbp_kind[d] == RTP_SBP_PARTIAL_MIN) return RED_MIN;
+        if (s.sbp_kind[d] == RTP_SBP_PARTIAL_MAX) return RED_MAX;
+    }
+    return RED_SUM;
 }
 
 void rank_coords(const rtp_spec& s, int64_t* coords)
@@ -104,7 +118,7 @@ Box rank_box(int ndim, const int64_t* shape, const rtp_spec& s, const int64_t* c
         case RTP_SBP_BROADCAST:
             if (c[d] != 0) b.b_rep = false;
             break;
-        default:  // partial sum
+        default:  // partial (sum, min or max)
             if (c[d] != 0) b.holds_value = false;
             b.pidx = b.pidx * s.mesh_shape[d] + c[d];
             break;

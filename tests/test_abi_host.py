@@ -94,10 +94,15 @@ def test_front_ends_match_oracle():
 
 
 def test_nd_sbp_geometry_matches_oracle():
-    opts = lambda nd: [("S", a) for a in range(nd)] + ["B", "P"]
+    opts = lambda nd: [("S", a) for a in range(nd)] + ["B", "P", "Pmax"]
     for shape in [(7,), (5, 4), (3, 1, 9)]:
         for mesh in [(2,), (4,), (2, 2), (2, 3), (3, 2)]:
             for ents in itertools.product(opts(len(shape)), repeat=len(mesh)):
+                if "P" in ents and "Pmax" in ents:  # one reduction per layout
+                    with pytest.raises(rtp.RtpError) as e:
+                        rtp.spec_check(len(shape), rtp.spec_nd_sbp(mesh, ents))
+                    assert e.value.status == -3
+                    continue
                 _same_layout(rtp.spec_nd_sbp(mesh, ents), oracle.Layout(mesh, ents), shape)
 
 
@@ -181,3 +186,22 @@ def test_planned_traffic_matches_algorithmic_bytes():
     s01 = rtp.spec_nd_sbp((2, 2), (("S", 0), ("S", 1)))
     assert sum(rtp.reshard_cost(rtp.F32, shape, s01, rtp.spec_nd_sbp((2, 2), (("S", 1), ("S", 0))))[:2]) == 2 * N * 4
     assert sum(rtp.reshard_cost(rtp.F32, shape, s01, rtp.spec_nd_sbp((2, 2), ("B", ("S", 1))))[:2]) == 3 * N * 4
+
+
+def test_sbp_signature_matches_oracle():
+    rng = np.random.default_rng(9)
+    for ndim in (1, 2, 3):
+        opts = [("S", a) for a in range(ndim)] + ["P", "B", "Pmax"]
+        for md in (1, 2, 3):
+            for _ in range(40):
+                shape = tuple(int(x) for x in rng.integers(1, 7, size=ndim))
+                n_in = int(rng.integers(1, 4))
+                inputs = [[opts[i] for i in rng.integers(len(opts), size=md)] for _ in range(n_in)]
+                want = oracle.infer_sbp_signature(shape, 2, inputs)
+                got = rtp.infer_sbp_signature(shape, 2, inputs)
+                assert got == tuple(want[:3]), (shape, inputs)
+                cons = [opts[i] for i in rng.integers(len(opts) - 1, size=md)]
+                want = oracle.infer_sbp_signature(shape, 2, inputs, constraint=cons)
+                assert rtp.infer_sbp_signature(shape, 2, inputs, constraint=cons) == tuple(want[:3])
+    assert rtp.infer_sbp_signature((2, 4), 4, [[("S", 0)], [("S", 1)]])[0] == [("S", 0)]
+    assert rtp.infer_sbp_signature((2, 4), 4, [[("S", 0)], ["B"]])[0] == ["B"]

@@ -406,3 +406,83 @@ def test_tp_mlp_row_subset_matches_full():
     zs, ys = oracle.tp_mlp(X, _split_cols(A, P), _split_rows(B, P), rows=rows)
     np.testing.assert_array_equal(zs, zf[rows])
     np.testing.assert_array_equal(ys, yf[rows])
+
+
+# ---- partial min / max (OneFlow page: min and max also work as partial reductions) ----
+
+def test_partial_min_max_against_numpy():
+    parts = [synth.normal(300 + k, (5, 7), "f32") for k in range(4)]
+    stack = np.stack(parts)
+    for red, fn in (("Pmin", np.minimum.reduce), ("Pmax", np.maximum.reduce)):
+        L = Layout((4,), (red,))
+        np.testing.assert_array_equal(oracle.gather(parts, (5, 7), L), fn(stack).astype(np.float64))
+        for out in oracle.reshard(parts, (5, 7), L, Layout((4,), ("B",))):
+            np.testing.assert_array_equal(out, fn(stack))
+        outs = oracle.reshard(parts, (5, 7), L, Layout((4,), (("S", 1),)))
+        np.testing.assert_array_equal(np.concatenate(outs, axis=1), fn(stack))
+    # bf16 members: min / max are exact
+    pb = [synth.normal(400 + k, (3, 9), "bf16") for k in range(3)]
+    got = oracle.reshard(pb, (3, 9), Layout((3,), ("Pmax",)), Layout((3,), ("B",)))[0]
+    want_f = np.maximum.reduce([synth.bf16_bits_to_f32(p) for p in pb])
+    np.testing.assert_array_equal(synth.bf16_bits_to_f32(got), want_f)
+
+
+def test_shard_to_partial_min_max_holds_identity():
+    T = synth.normal(5, (4, 6), "f32")
+    for red, ident in (("Pmin", np.inf), ("Pmax", -np.inf), ("P", 0.0)):
+        L = Layout((2, 2), (red, ("S", 1)))
+        pieces = oracle.shard(T, L)
+        np.testing.assert_array_equal(pieces[0], T[:, :3])
+        np.testing.assert_array_equal(pieces[1], T[:, 3:])
+        assert np.all(pieces[2] == ident) and np.all(pieces[3] == ident)
+        np.testing.assert_array_equal(oracle.gather(pieces, T.shape, L), T.astype(np.float64))
+
+
+def test_mixed_partial_reductions_rejected():
+    with pytest.raises(oracle.OracleError):
+        oracle.shard(np.zeros((2, 2), np.float32), Layout((2, 2), ("P", "Pmax")))
+
+
+# ---- SBP signature inference (OneFlow add_n walk-through) ------------------------
+
+def _ent(e):
+    return e if isinstance(e, str) else (e[0], e[1])
+
+
+def test_sbp_signature_page_examples(golden_dir):
+    g = _golden(golden_dir, "oneflow_sbp_examples.json")["signature_inference"]
+    shape = tuple(g["shape"])
+    for case in g["cases"]:
+        inputs = [[_ent(e) for e in sbp] for sbp in case["inputs"]]
+        sig, cost, order, ncand = oracle.infer_sbp_signature(shape, g["elem_bytes"], inputs)
+        assert sig == [_ent(e) for e in case["expected"]]
+        assert ncand == len(g["candidates_1d_in_order"])
+    # the candidate order: with no input matching any candidate's SBP except
+    # through ties, the first candidate wins (two partial-min inputs: every
+    # candidate costs the same huge amount)
+    sig, cost, order, _ = oracle.infer_sbp_signature(shape, 4, [["Pmin"], ["Pmin"]])
+    assert sig == [_ent(g["candidates_1d_in_order"][0])] and order == 0
+
+
+def test_sbp_signature_invariants():
+    rng = np.random.default_rng(7)
+    for ndim in (1, 2, 3):
+        shape = tuple(int(x) for x in rng.integers(1, 5, size=ndim))
+        opts = [("S", a) for a in range(ndim)] + ["P", "B"]
+        for md in (1, 2):
+            for _ in range(20):
+                common = [opts[i] for i in rng.integers(len(opts), size=md)]
+                n_in = int(rng.integers(1, 4))
+                # all inputs already agree: that signature, order -10 n, no cost
+                sig, cost, order, ncand = oracle.infer_sbp_signature(shape, 2, [common] * n_in)
+                assert sig == common and cost == 0 and order == -10 * n_in
+                assert ncand == (ndim + 2) ** md
+                # a constraint is obeyed and disables the order value
+                other = [opts[i] for i in rng.integers(len(opts), size=md)]
+                sig, cost, order, ncand = oracle.infer_sbp_signature(shape, 2, [common] * n_in, constraint=other)
+                assert sig == other and order == 0 and ncand == 1
+    # a split input moved to another split costs its bytes; a broadcast one is "huge"
+    sig, cost, order, _ = oracle.infer_sbp_signature((4, 4), 4, [[("S", 0)], [("S", 1)], [("S", 1)]])
+    assert sig == [("S", 1)] and cost == 64 and order == -20
+    with pytest.raises(oracle.OracleError):
+        oracle.infer_sbp_signature((4,), 4, [[("S", 0)]], constraint=[("S", 3)])
