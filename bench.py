@@ -218,6 +218,10 @@ def run_ours(args, rank, world, local_rank):
 
     mlp = mlp_buffers(MLP, False)
     dom = mlp_buffers(DOMINO, True)
+    # sequence parallel: X split by rows over the ranks, Z scattered by rows
+    sp_rows = MLP["M"] // MLP["P"]
+    sp_x = [mlp["X"][r * sp_rows:(r + 1) * sp_rows].contiguous() for r in range(MLP["P"])]
+    sp_z = [torch.empty((sp_rows, MLP["N"]), dtype=torch.float32, device=dev) for _ in range(MLP["P"])]
     s1 = torch.cuda.Stream(device=dev)
     # the reduction alone: P-sum of the 8 float32 partials into one buffer
     dom_red_src = rtp.spec_nd_sbp((8,), ("P",))
@@ -226,6 +230,9 @@ def run_ours(args, rank, world, local_rank):
 
     def run_mlp():
         rtp.tp_mlp(mlp["X"], mlp["A"], mlp["B"], Y=mlp["Y"], Z=mlp["Z"], mode=1)
+
+    def run_sp():
+        rtp.tp_mlp_sp(sp_x, mlp["A"], mlp["B"], Y=mlp["Y"], Z_shards=sp_z)
 
     def run_domino():
         rtp.tp_mlp(dom["X"], dom["A"], dom["B"], Y=dom["Y"], partials=dom["parts"], Z=dom["Z"], mode=0, chunks=2,
@@ -242,7 +249,7 @@ def run_ours(args, rank, world, local_rank):
     shard_ops = [(label, (lambda T=T, sp=sp, o=o: rtp.shard(T, sp, out=o)), nbytes, nl)
                  for (label, T, sp, o, nbytes, nl) in shards]
     launches_per_step = (sum(x[3] for x in ops) + sum(x[3] for x in shard_ops) +
-                         2 + 6 + 3 + 1)  # mlp 2, domino 2x3, serial 3, reduce 1
+                         2 + 2 + 6 + 3 + 1)  # mlp 2, sequence parallel 2, domino 2x3, serial 3, reduce 1
     E = lambda: torch.cuda.Event(enable_timing=True)
 
     def step(record):
@@ -260,7 +267,8 @@ def run_ours(args, rank, world, local_rank):
             fn()
             e1.record()
             record.append(("reshard", label, e0, e1, nbytes))
-        for kind, fn in (("mlp", run_mlp), ("domino", run_domino), ("serial", run_serial), ("reduce", run_reduce)):
+        for kind, fn in (("mlp", run_mlp), ("sp", run_sp), ("domino", run_domino), ("serial", run_serial),
+                         ("reduce", run_reduce)):
             flush.zero_()
             e0, e1 = E(), E()
             e0.record()
@@ -299,6 +307,7 @@ def run_ours(args, rank, world, local_rank):
     dom_ms = per[("domino", "domino")][0] / args.steps
     ser_ms = per[("serial", "serial")][0] / args.steps
     red_ms = per[("reduce", "reduce")][0] / args.steps
+    sp_ms = per[("sp", "sp")][0] / args.steps
 
     def max_over_ranks(x):
         if dist is None:
@@ -329,6 +338,9 @@ def run_ours(args, rank, world, local_rank):
                                "shape": "8 float32 partials [4096,8192] -> Z"},
         "a6_a7_separate_schedule": {"ms": round(ser_ms, 4), "tflops": round(DOMINO_FLOPS / (ser_ms * 1e-3) / 1e12, 1)},
         "a8_domino": {"ms": round(dom_ms, 4), "hiding": round((ser_ms - dom_ms) / red_ms, 3) if red_ms > 0 else None},
+        "f2_tp_mlp_sequence_parallel": {"ms": round(sp_ms, 4), "tflops": round(MLP_FLOPS / (sp_ms * 1e-3) / 1e12, 1),
+                                        "frac_bf16": round(MLP_FLOPS / (sp_ms * 1e-3) / 1e12 / bf16_peak, 4)},
+        "f3_infer_sbp_signature": {"us_per_call": host["sbp_signature_us"], "where": "host"},
     }
     reshard_ms = max_over_ranks(reshard_ms)
     mlp_ms = max_over_ranks(mlp_ms)
@@ -396,7 +408,11 @@ def host_inference_timings(rtp, reps: int = 2000):
     for _ in range(reps):
         rtp.infer_reshape([2, 3, 4096], [0, -1, -1], [6, 4096], [2])
     b = (time.perf_counter() - t) / reps * 1e6
-    return {"infer_spmd_us": round(a, 2), "infer_reshape_us": round(b, 2)}
+    t = time.perf_counter()
+    for _ in range(reps):
+        rtp.infer_sbp_signature((2, 4), 4, [[("S", 0)], [("S", 1)]])
+    c = (time.perf_counter() - t) / reps * 1e6
+    return {"infer_spmd_us": round(a, 2), "infer_reshape_us": round(b, 2), "sbp_signature_us": round(c, 2)}
 
 
 MLP_FLOPS = 2 * MLP["M"] * MLP["K"] * MLP["F"] + 2 * MLP["M"] * MLP["F"] * MLP["N"]

@@ -280,6 +280,25 @@ int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
                int col_blocks, rtp_stream s0, rtp_stream s1);
 
 /*
+ * The tensor-parallel MLP with sequence parallelism (ColossalAI "1D tensor
+ * parallelism" page, section 5.3: with sequence parallelism the column-parallel
+ * layer all-gathers its input in the forward pass and the row-parallel layer
+ * reduce-scatters its output instead of all-reducing it).
+ *   X_shards  P bf16 [M/P, K]: rank r holds rows [r M/P, (r+1) M/P) of X
+ *   A_shards, B_shards, Y: as in rtp_tp_mlp (Y_i [M, F/P] covers all rows)
+ *   Z_shards  P float32 [M/P, N]: rank r receives rows [r M/P, (r+1) M/P) of
+ *             Z = sum_i GELU(X A_i) B_i
+ * Both collectives are fused into the GEMMs: the column-parallel GEMM reads X
+ * from the shards directly and the row-parallel GEMM sums the ranks in its
+ * accumulator and writes each row to its shard. Requires M % P == 0 and
+ * (M/P) % 128 == 0, K, F/P and N multiples of 8, P <= 8 (else RTP_ESHAPE /
+ * RTP_EUNSUPPORTED); pointers 16-byte aligned.
+ */
+int rtp_tp_mlp_sp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* const* X_shards,
+                  const void* const* A_shards, const void* const* B_shards, void* const* Y, float* const* Z_shards,
+                  rtp_stream stream);
+
+/*
  * tp_mlp for callers that cannot allocate device memory (code running inside
  * another runtime's memory pool, or a serving loop whose memory plan is fixed
  * at start-up). The pages have no counterpart to this call; it is a service

@@ -95,6 +95,8 @@ def _load():
         "rtp_infer_sbp_signature": [c_int, c_int, i64p, c_int, c_int, i32p, i32p, i32p, i32p, i32p, i32p,
                                     P(ctypes.c_double), i32p],
         "rtp_device_error": [vp, u32p],
+        "rtp_tp_mlp_sp": [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vpp, vpp, vpp, vpp,
+                          vpp, vp],
         "rtp_tp_mlp_noalloc": [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vpp, vpp,
                                vp, vp],
         "rtp_tp_mlp": [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vpp, vpp, vpp,
@@ -374,6 +376,28 @@ def tp_mlp(X, A_shards, B_shards, Y=None, partials=None, Z=None, mode: int = 1, 
                               _ptrs([b.data_ptr() for b in B_shards]), _ptrs([y.data_ptr() for y in Y]), pp,
                               Z.data_ptr(), mode, chunks, col_blocks, _stream_ptr(s0), _stream_ptr(s1)))
     return Z, Y
+
+
+def tp_mlp_sp(X_shards, A_shards, B_shards, Y=None, Z_shards=None, stream=None):
+    """Sequence-parallel TP-MLP: X_shards[r] holds rows r*M/P.. of X; returns
+    (Z_shards, Y) with Z_shards[r] the same rows of sum_i GELU(X A_i) B_i."""
+    torch = _torch()
+    P = len(A_shards)
+    Mr, K = X_shards[0].shape
+    M = Mr * P
+    Fp = A_shards[0].shape[1]
+    N = B_shards[0].shape[1]
+    dev = X_shards[0].device
+    if Y is None:
+        Y = [torch.empty((M, Fp), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    if Z_shards is None:
+        Z_shards = [torch.empty((Mr, N), dtype=torch.float32, device=dev) for _ in range(P)]
+    _check_cuda(list(X_shards) + list(A_shards) + list(B_shards) + list(Y) + list(Z_shards), "tp_mlp_sp")
+    _check(_load().rtp_tp_mlp_sp(P, M, K, Fp * P, N, _ptrs([x.data_ptr() for x in X_shards]),
+                                 _ptrs([a.data_ptr() for a in A_shards]), _ptrs([b.data_ptr() for b in B_shards]),
+                                 _ptrs([y.data_ptr() for y in Y]), _ptrs([z.data_ptr() for z in Z_shards]),
+                                 _stream_ptr(stream)))
+    return Z_shards, Y
 
 
 def tp_mlp_noalloc(X, A_shards, B_shards, Z=None, stream=None):

@@ -29,6 +29,12 @@
 // rank's K range in turn, so the sum of ranks happens in the TMEM accumulator
 // and no partial is ever written.
 //
+// Sequence parallelism (ColossalAI page, section 5.3: the column layer
+// all-gathers its sequence-split input, the row layer reduce-scatters its
+// output) is fused too: the column-parallel GEMM loads each 128-row block of X
+// from the rank that holds it, and the rank-summing row-parallel GEMM writes
+// each output row to the rank that owns it.
+//
 // The Domino schedule (Domino page, row split of X and column split of B)
 // cuts X into row chunks (and B_i into column blocks): the reduction of
 // chunk c runs on a second stream while the GEMMs of chunk c+1 run.
@@ -74,6 +80,13 @@ struct GemmArgs {
     int32_t m0, n0;              // window of the problem (Domino chunk / column block)
     int32_t m_end, n_end;        // exclusive bounds of the output window
     int32_t total_tiles;
+    // Sequence parallelism (rows sharded over the ranks): when > 0, the
+    // K-major operand of row r comes from map ta[r / a_rows_per_map] at row
+    // r % a_rows_per_map (an all-gather fused into the loads), and/or output
+    // row r goes to out[r / out_rows_per_ptr] at row r % out_rows_per_ptr (a
+    // reduce-scatter fused into the epilogue of the rank-summing GEMM).
+    int32_t a_rows_per_map, a_maps;
+    int32_t out_rows_per_ptr, out_ptrs;
 };
 
 __device__ unsigned int g_tp_error;
@@ -112,10 +125,9 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
-// Bounded wait. False: this wait gave up, or another role already did.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, uint32_t code)
+// Slow path of wait_bar, kept out of line.
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, uint32_t code)
 {
-    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -128,6 +140,13 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile ui
             }
         }
     }
+}
+
+// Bounded wait. False: this wait gave up, or another role already did.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, uint32_t code)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bar_slow(bar, parity, abort_flag, code);
 }
 
 // Bounded wait used only while tearing down after an abort: it ignores the
@@ -275,6 +294,10 @@ __device__ __forceinline__ void mma_commit_pair_local(uint32_t bar)
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// SP_A: the K-major operand's rows come from per-shard maps (sequence-parallel
+// all-gather); SP_OUT: output rows go to per-shard buffers (reduce-scatter).
+// Compile-time, so the common kernel carries no extra work in its loops.
+template <bool SP_A, bool SP_OUT>
 __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_constant__ GemmArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -332,26 +355,40 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
             uint32_t phase = 0;
             uint32_t issued = 0, issued_parity = 0;
             bool ok = true;
+            const uint32_t smem0 = smem_u32(smem);
+            const uint32_t leader_full0 = map_to_rank(full_bar(0), 0);  // barriers are 8 bytes apart
             for (int tile = pair; ok && tile < a.total_tiles; tile += npairs) {
                 int g, mt, nt;
                 tile_coords(a, tile, g, mt, nt);
                 const int row = a.m0 + mt * BM2 + (int)cta * 128, col = a.n0 + nt * BN + (int)cta * 128;
+                const CUtensorMap* amap_sp = nullptr;
+                int arow = row;
+                if constexpr (SP_A) {
+                    // the 128-row block lies in one shard (shards are multiples of 128
+                    // rows); rows past the last shard read as zeros
+                    const int sh = min(row / a.a_rows_per_map, a.a_maps - 1);
+                    amap_sp = &a.ta[sh];
+                    arow = row - sh * a.a_rows_per_map;
+                }
+                int gg = a.fused ? 0 : g, kk = 0;
                 for (int kb = 0; kb < kbs; ++kb) {
                     if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, ERR_PRODUCER)) {
                         ok = false;
                         break;
                     }
-                    const int gg = a.fused ? kb / a.kb_per_group : g;
-                    const int kk = a.fused ? kb - gg * a.kb_per_group : kb;
-                    const uint32_t sa = smem_u32(smem + stage * STAGE2_BYTES);
+                    const uint32_t sa = smem0 + (uint32_t)stage * STAGE2_BYTES;
                     const uint32_t sb = sa + A2_BYTES;
-                    const uint32_t fb = map_to_rank(full_bar(stage), 0);
+                    const uint32_t fb = leader_full0 + 8u * (uint32_t)stage;
                     if (cta == 0) mbar_expect_tx(full_bar(stage), 2 * STAGE2_BYTES);
-                    tma_load_2d_pair(sa, &a.ta[gg], fb, kk * BK, row);
+                    tma_load_2d_pair(sa, SP_A ? amap_sp : &a.ta[gg], fb, kk * BK, arow);
                     tma_load_2d_pair(sb, &a.tb[gg], fb, col, kk * BK);
                     tma_load_2d_pair(sb + B_SUB, &a.tb[gg], fb, col + 64, kk * BK);
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++kk == a.kb_per_group) {  // next rank's K range (fused reduction)
+                        kk = 0;
+                        ++gg;
+                    }
                     if (++stage == STAGES2) {
                         stage = 0;
                         phase ^= 1u;
@@ -378,6 +415,11 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
+            // K-major A: 32-byte steps inside the 128-byte swizzle row, 8-row groups
+            // 1024 bytes apart. N-major B: 16 K-rows = 2 groups of 8 rows of 128 bytes;
+            // the two 64-wide N boxes are B_SUB bytes apart.
+            const uint64_t desc_a0 = smem_desc(smem_u32(smem), 16u, 1024u);
+            const uint64_t desc_b0 = smem_desc(smem_u32(smem) + A2_BYTES, B_SUB, 1024u);
             uint32_t acc_phase = 0;
             bool ok = true;
             for (int tile = pair; ok && tile < a.total_tiles; tile += npairs) {
@@ -393,12 +435,12 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + stage * STAGE2_BYTES);
-                    const uint32_t sb = sa + A2_BYTES;
+                    // descriptors are affine in the start address (bits 0-13 hold addr >> 4)
+                    const uint64_t off = (uint64_t)((uint32_t)stage * STAGE2_BYTES >> 4);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        const uint64_t da = smem_desc(sa + 32u * k, 16u, 1024u);
-                        const uint64_t db = smem_desc(sb + 2048u * k, B_SUB, 1024u);
+                        const uint64_t da = desc_a0 + off + (uint64_t)(32u * k >> 4);
+                        const uint64_t db = desc_b0 + off + (uint64_t)(2048u * k >> 4);
                         mma_bf16_pair(d_tmem, da, db, (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit_pair(empty_bar(stage));
@@ -436,6 +478,13 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
             const int64_t row = a.m0 + (int64_t)mt * BM2 + cta * 128 + quarter * 32 + lane;
             const int64_t col = a.n0 + (int64_t)nt * BN;
             const bool row_ok = row < a.m_end;
+            void* out_base = a.out[g];
+            int64_t orow = row;
+            if (SP_OUT && row_ok) {
+                const int sh = min((int)(row / a.out_rows_per_ptr), a.out_ptrs - 1);
+                out_base = a.out[sh];
+                orow = row - (int64_t)sh * a.out_rows_per_ptr;
+            }
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
@@ -444,7 +493,7 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
                 const int64_t c0 = col + 32 * c;
                 if (!row_ok || c0 >= a.n_end) continue;
                 if (a.epi == EPI_GELU_BF16) {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out[g]) + row * a.ldo + c0);
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_base) + orow * a.ldo + c0);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         if (c0 + 8 * q >= a.n_end) break;
@@ -456,7 +505,7 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
                         __stcs(dst + q, v);
                     }
                 } else {
-                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out[g]) + row * a.ldo + c0);
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_base) + orow * a.ldo + c0);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         if (c0 + 4 * q >= a.n_end) break;
@@ -514,7 +563,8 @@ int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int bo
     return RTP_OK;
 }
 
-int launch_gemm(GemmArgs& args, cudaStream_t stream)
+template <bool SP_A, bool SP_OUT>
+int launch_gemm_t(GemmArgs& args, cudaStream_t stream)
 {
     static bool configured[64] = {};
     static int max_clusters[64] = {};
@@ -532,11 +582,11 @@ int launch_gemm(GemmArgs& args, cudaStream_t stream)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tp_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM2_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(tp_gemm_kernel<SP_A, SP_OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM2_BYTES);
         if (e != cudaSuccess) return fail(RTP_ECUDA, "tp_mlp: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         cfg.gridDim = dim3(2 * 64);
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, tp_gemm_kernel, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, tp_gemm_kernel<SP_A, SP_OUT>, &cfg);
         if (e != cudaSuccess || n <= 0) return fail(RTP_ECUDA, "tp_mlp: cudaOccupancyMaxActiveClusters: %s", cudaGetErrorString(e));
         max_clusters[dev] = n;
         configured[dev] = true;
@@ -545,9 +595,16 @@ int launch_gemm(GemmArgs& args, cudaStream_t stream)
     const int clusters = args.total_tiles < max_clusters[dev] ? args.total_tiles : max_clusters[dev];
     if (clusters <= 0) return RTP_OK;
     cfg.gridDim = dim3(2 * clusters);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, tp_gemm_kernel, args);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, tp_gemm_kernel<SP_A, SP_OUT>, args);
     if (e != cudaSuccess) return fail(RTP_ECUDA, "tp_mlp: GEMM launch failed: %s", cudaGetErrorString(e));
     return RTP_OK;
+}
+
+int launch_gemm(GemmArgs& args, cudaStream_t stream)
+{
+    if (args.a_rows_per_map > 0) return launch_gemm_t<true, false>(args, stream);
+    if (args.out_rows_per_ptr > 0) return launch_gemm_t<false, true>(args, stream);
+    return launch_gemm_t<false, false>(args, stream);
 }
 
 struct Events {
@@ -697,6 +754,68 @@ int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
             return fail(RTP_ECUDA, "tp_mlp: event ordering failed");
     }
     return RTP_OK;
+}
+
+int rtp_tp_mlp_sp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* const* X_shards,
+                  const void* const* A_shards, const void* const* B_shards, void* const* Y, float* const* Z_shards,
+                  rtp_stream stream_)
+{
+    const char* fn = "rtp_tp_mlp_sp";
+    if (P < 1 || P > MAX_GROUPS) return fail(RTP_EUNSUPPORTED, "%s: P = %d outside [1, %d]", fn, P, MAX_GROUPS);
+    if (!X_shards || !A_shards || !B_shards || !Y || !Z_shards) return fail(RTP_EINVAL, "%s: NULL argument", fn);
+    if (M < 0 || K < 1 || F < 1 || N < 1) return fail(RTP_ESHAPE, "%s: sizes M=%lld K=%lld F=%lld N=%lld", fn,
+                                                      (long long)M, (long long)K, (long long)F, (long long)N);
+    if (F % P || M % P) return fail(RTP_ESHAPE, "%s: F=%lld and M=%lld must be divisible by P=%d", fn, (long long)F, (long long)M, P);
+    const int64_t Fp = F / P, Mr = M / P;
+    if (Mr % 128) return fail(RTP_ESHAPE, "%s: M/P=%lld must be a multiple of 128 (one row block per shard)", fn, (long long)Mr);
+    if (K % 8 || Fp % 8 || N % 8) return fail(RTP_ESHAPE, "%s: K, F/P and N must be multiples of 8 (16-byte rows)", fn);
+    if (M >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 31) || Fp >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31))
+        return fail(RTP_ESHAPE, "%s: extents must stay below 2^31", fn);
+    for (int i = 0; i < P; ++i) {
+        if (!X_shards[i] || !A_shards[i] || !B_shards[i] || !Y[i] || !Z_shards[i]) return fail(RTP_EINVAL, "%s: NULL buffer for rank %d", fn, i);
+        if (!aligned16(X_shards[i]) || !aligned16(A_shards[i]) || !aligned16(B_shards[i]) || !aligned16(Y[i]) || !aligned16(Z_shards[i]))
+            return fail(RTP_EINVAL, "%s: buffers of rank %d must be 16-byte aligned", fn, i);
+    }
+    if (M == 0) return RTP_OK;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    static thread_local GemmArgs g1, g2;
+    std::memset(&g1, 0, sizeof g1);
+    std::memset(&g2, 0, sizeof g2);
+    int st;
+    for (int i = 0; i < P; ++i) {
+        if ((st = make_map(&g1.ta[i], X_shards[i], Mr, K, 128))) return st;  // X rows by shard
+        if ((st = make_map(&g1.tb[i], A_shards[i], K, Fp, BK))) return st;
+        g1.out[i] = Y[i];
+        if ((st = make_map(&g2.ta[i], Y[i], M, Fp, 128))) return st;
+        if ((st = make_map(&g2.tb[i], B_shards[i], Fp, N, BK))) return st;
+        g2.out[i] = Z_shards[i];  // Z rows by shard
+    }
+    // column-parallel GEMM with the all-gather of X fused into its loads
+    g1.ldo = Fp;
+    g1.groups = P;
+    g1.fused = 0;
+    g1.epi = EPI_GELU_BF16;
+    g1.m_tiles = (int)((M + BM2 - 1) / BM2);
+    g1.n_tiles = (int)((Fp + BN - 1) / BN);
+    g1.kb_per_group = (int)((K + BK - 1) / BK);
+    g1.m_end = (int)M;
+    g1.n_end = (int)Fp;
+    g1.a_rows_per_map = (int)Mr;
+    g1.a_maps = P;
+    if ((st = launch_gemm(g1, stream))) return st;
+    // row-parallel GEMM: ranks summed in TMEM, rows scattered to their shard
+    g2.ldo = N;
+    g2.groups = P;
+    g2.fused = 1;
+    g2.epi = EPI_F32;
+    g2.m_tiles = (int)((M + BM2 - 1) / BM2);
+    g2.n_tiles = (int)((N + BN - 1) / BN);
+    g2.kb_per_group = (int)((Fp + BK - 1) / BK);
+    g2.m_end = (int)M;
+    g2.n_end = (int)N;
+    g2.out_rows_per_ptr = (int)Mr;
+    g2.out_ptrs = P;
+    return launch_gemm(g2, stream);
 }
 
 int rtp_device_error(rtp_stream stream, uint32_t* code)

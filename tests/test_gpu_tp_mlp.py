@@ -159,3 +159,43 @@ def test_argument_errors():
     Z, _ = rtp.tp_mlp(X, As, Bs)
     torch.cuda.synchronize()
     assert float(Z.abs().max()) == 0.0
+
+
+# ---- sequence parallelism (ColossalAI page, section 5.3) --------------------------
+
+@pytest.mark.parametrize("M,K,F,N,P", [(256, 64, 512, 256, 2), (512, 200, 1056, 264, 4), (1024, 512, 2048, 512, 8),
+                                       (128, 96, 264, 136, 1)])
+def test_sequence_parallel_matches_oracle_and_fused(M, K, F, N, P):
+    """X split by rows over the ranks in, Z split by rows over the ranks out;
+    the all-gather and reduce-scatter are fused into the GEMMs."""
+    X, As, Bs = _inputs(M, K, F, N, P, seed=M + 3 * K)
+    Mr = M // P
+    Xs = [np.ascontiguousarray(X[r * Mr:(r + 1) * Mr]) for r in range(P)]
+    Zs, Ys = rtp.tp_mlp_sp([to_dev(x) for x in Xs], [to_dev(a) for a in As], [to_dev(b) for b in Bs])
+    torch.cuda.synchronize()
+    Z = np.concatenate([to_host(z) for z in Zs], axis=0)
+    _check(X, As, Bs, Z, [to_host(y) for y in Ys], np.arange(M), "sequence parallel")
+    # the same accumulation as the fused MLP on the gathered X: identical bits
+    Zf, Yf = _gpu(X, As, Bs, 1)
+    np.testing.assert_array_equal(Z, Zf)
+    for a, b in zip(Ys, Yf):
+        np.testing.assert_array_equal(to_host(a), b)
+
+
+def test_sequence_parallel_full_size(cfg4):
+    X, As, Bs = cfg4
+    P, M = 8, 8192
+    Mr = M // P
+    Zs, Ys = rtp.tp_mlp_sp([to_dev(np.ascontiguousarray(X[r * Mr:(r + 1) * Mr])) for r in range(P)],
+                           [to_dev(a) for a in As], [to_dev(b) for b in Bs])
+    torch.cuda.synchronize()
+    Z = np.concatenate([to_host(z) for z in Zs], axis=0)
+    rows = _sample_rows(M, 12)
+    _check(X, As, Bs, Z, [to_host(y) for y in Ys], rows, "sequence parallel full size")
+
+
+def test_sequence_parallel_errors():
+    dev = lambda *s: torch.zeros(s, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(rtp.RtpError) as e:  # M/P = 100 rows is not a multiple of 128
+        rtp.tp_mlp_sp([dev(100, 64)] * 2, [dev(64, 256)] * 2, [dev(256, 64)] * 2)
+    assert e.value.status == -2
