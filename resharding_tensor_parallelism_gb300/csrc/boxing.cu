@@ -127,98 +127,161 @@ __device__ __forceinline__ void divmod(int jj, int nv, float inv, int& q, int& r
     }
 }
 
-// One chunk: nr rows (element offsets of each row's first element in s_off /
-// d_off, relative to the task's buffers) of nv vectors each. Items (row,
-// vector) are spread over the block, U per thread per pass. ES: element size.
-template <int VB, int ES, bool SUM>
-__device__ __forceinline__ void run_chunk(const KParams& p, const KTask& t, int nr, int nv, const int64_t* s_off,
-                                          const int64_t* d_off)
-{
+// Items (row, vector) of one chunk are spread over the block, U per thread per
+// pass: item j is vector j % nv of row j / nv; s_off / d_off hold each row's
+// first element offset (relative to the task's buffers).
+template <int VB, int ES, int U>
+struct Items {
     using V = typename Raw<VB>::T;
-    constexpr int U = SUM ? 2 : 4;
-    const int total = nr * nv;
-    const float inv = 1.0f / (float)nv;
-    const int ns = t.n_src, nd = t.n_dst;
-    const void* const* sp = p.ptrs + t.ptr0;
-    const void* const* dp = sp + ns;
-    for (int j0 = threadIdx.x; j0 < total; j0 += kBlock * U) {
-        int q[U], r[U];
+    int q[U], r[U];  // row and vector of each item; r < 0 marks a dead item
+    const int64_t* s_off;
+    const int64_t* d_off;
+    __device__ __forceinline__ void at(int j0, int total, int nv, float inv)
+    {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int jj = j0 + u * kBlock;
             q[u] = 0;
-            r[u] = -1;  // r < 0 marks a dead item
+            r[u] = -1;
             if (jj < total) divmod(jj, nv, inv, q[u], r[u]);
         }
-        auto saddr = [&](const void* base, int u) {
-            return reinterpret_cast<const V*>(static_cast<const char*>(base) + s_off[q[u]] * ES) + r[u];
-        };
-        auto daddr = [&](const void* base, int u) {
-            return reinterpret_cast<V*>(static_cast<char*>(const_cast<void*>(base)) + d_off[q[u]] * ES) + r[u];
-        };
-        if (ns == 0) {
-            Lanes<VB> z;
+    }
+    __device__ __forceinline__ const V* src(const void* base, int u) const
+    {
+        return reinterpret_cast<const V*>(static_cast<const char*>(base) + s_off[q[u]] * ES) + r[u];
+    }
+    __device__ __forceinline__ V* dst(const void* base, int u) const
+    {
+        return reinterpret_cast<V*>(static_cast<char*>(const_cast<void*>(base)) + d_off[q[u]] * ES) + r[u];
+    }
+};
+
+// No source: every destination gets the fill pattern (the identity of the
+// destination's partial reduction).
+template <int VB, int ES>
+__device__ __forceinline__ void fill_chunk(const KParams& p, const KTask& t, int total, int nv, const int64_t* s_off,
+                                           const int64_t* d_off)
+{
+    constexpr int U = 4;
+    Items<VB, ES, U> it{{}, {}, s_off, d_off};
+    Lanes<VB> z;
 #pragma unroll
-            for (int k = 0; k < VB / 2; ++k) z.h[k] = (uint16_t)(t.fill >> (16 * (k & 1)));
-            for (int j = 0; j < nd; ++j)
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-                    if (r[u] >= 0) __stcs(daddr(dp[j], u), z.v);
-        } else if (!SUM || ns == 1) {
-            V x[U];
+    for (int k = 0; k < VB / 2; ++k) z.h[k] = (uint16_t)(t.fill >> (16 * (k & 1)));
+    const float inv = 1.0f / (float)nv;
+    const void* const* dp = p.ptrs + t.ptr0;
+    for (int j0 = threadIdx.x; j0 < total; j0 += kBlock * U) {
+        it.at(j0, total, nv, inv);
+        for (int j = 0; j < t.n_dst; ++j)
 #pragma unroll
             for (int u = 0; u < U; ++u)
-                if (r[u] >= 0) x[u] = __ldcs(saddr(sp[0], u));
-            for (int j = 0; j < nd; ++j)
+                if (it.r[u] >= 0) __stcs(it.dst(dp[j], u), z.v);
+    }
+}
+
+// One source: its bits go to every destination (read once).
+template <int VB, int ES>
+__device__ __forceinline__ void copy_chunk(const KParams& p, const KTask& t, int total, int nv, const int64_t* s_off,
+                                           const int64_t* d_off)
+{
+    constexpr int U = 4;
+    using V = typename Raw<VB>::T;
+    Items<VB, ES, U> it{{}, {}, s_off, d_off};
+    const float inv = 1.0f / (float)nv;
+    const void* const* sp = p.ptrs + t.ptr0;
+    const void* const* dp = sp + 1;
+    for (int j0 = threadIdx.x; j0 < total; j0 += kBlock * U) {
+        it.at(j0, total, nv, inv);
+        V x[U];
 #pragma unroll
-                for (int u = 0; u < U; ++u)
-                    if (r[u] >= 0) __stcs(daddr(dp[j], u), x[u]);
-        } else if constexpr (SUM) {
-            constexpr int NE = VB / ES;  // elements per vector
-            float acc[U][NE];
+        for (int u = 0; u < U; ++u)
+            if (it.r[u] >= 0) x[u] = __ldcs(it.src(sp[0], u));
+        for (int j = 0; j < t.n_dst; ++j)
 #pragma unroll
             for (int u = 0; u < U; ++u)
+                if (it.r[u] >= 0) __stcs(it.dst(dp[j], u), x[u]);
+    }
+}
+
+template <int OP>
+__device__ __forceinline__ float combine(float acc, float x)
+{
+    if constexpr (OP == RED_SUM) return acc + x;
+    else if constexpr (OP == RED_MIN) return fminf(acc, x);
+    else return fmaxf(acc, x);
+}
+
+// Several sources combined element-wise in float32 in source order (partial
+// coordinates row-major), starting from the reduction's identity, rounded once
+// to the element type.
+template <int VB, int ES, int OP>
+__device__ __forceinline__ void reduce_chunk(const KParams& p, const KTask& t, int total, int nv, const int64_t* s_off,
+                                             const int64_t* d_off)
+{
+    constexpr int U = 2;
+    constexpr int NE = VB / ES;  // elements per vector
+    using V = typename Raw<VB>::T;
+    Items<VB, ES, U> it{{}, {}, s_off, d_off};
+    const float inv = 1.0f / (float)nv;
+    const int ns = t.n_src;
+    const void* const* sp = p.ptrs + t.ptr0;
+    const void* const* dp = sp + ns;
+    const float ident = OP == RED_SUM ? 0.0f : (OP == RED_MIN ? __int_as_float(0x7F800000) : __int_as_float(0xFF800000));
+    for (int j0 = threadIdx.x; j0 < total; j0 += kBlock * U) {
+        it.at(j0, total, nv, inv);
+        float acc[U][NE];
 #pragma unroll
-                for (int e = 0; e < NE; ++e) acc[u][e] = 0.f;
-            const int op = t.op;
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int e = 0; e < NE; ++e) acc[u][e] = ident;
 #pragma unroll 4
-            for (int j = 0; j < ns; ++j) {
-                Lanes<VB> in[U];
+        for (int j = 0; j < ns; ++j) {
+            Lanes<VB> in[U];
 #pragma unroll
-                for (int u = 0; u < U; ++u)
-                    if (r[u] >= 0) in[u].v = __ldcs(saddr(sp[j], u));
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-#pragma unroll
-                    for (int e = 0; e < NE; ++e) {
-                        float x;
-                        if constexpr (ES == 4) x = __uint_as_float(in[u].w[e]);
-                        else x = __uint_as_float((uint32_t)in[u].h[e] << 16);
-                        if (j == 0) acc[u][e] = x;
-                        else if (op == RED_SUM) acc[u][e] = acc[u][e] + x;
-                        else if (op == RED_MIN) acc[u][e] = fminf(acc[u][e], x);
-                        else acc[u][e] = fmaxf(acc[u][e], x);
-                    }
-            }
-            Lanes<VB> out[U];
+            for (int u = 0; u < U; ++u)
+                if (it.r[u] >= 0) in[u].v = __ldcs(it.src(sp[j], u));
 #pragma unroll
             for (int u = 0; u < U; ++u)
 #pragma unroll
                 for (int e = 0; e < NE; ++e) {
-                    if constexpr (ES == 4) out[u].w[e] = __float_as_uint(acc[u][e]);
-                    else out[u].h[e] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[u][e]));
+                    float x;
+                    if constexpr (ES == 4) x = __uint_as_float(in[u].w[e]);
+                    else x = __uint_as_float((uint32_t)in[u].h[e] << 16);
+                    acc[u][e] = combine<OP>(acc[u][e], x);
                 }
-            for (int j = 0; j < nd; ++j)
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-                    if (r[u] >= 0) __stcs(daddr(dp[j], u), out[u].v);
         }
+        Lanes<VB> out[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int e = 0; e < NE; ++e) {
+                if constexpr (ES == 4) out[u].w[e] = __float_as_uint(acc[u][e]);
+                else out[u].h[e] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[u][e]));
+            }
+        for (int j = 0; j < t.n_dst; ++j)
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (it.r[u] >= 0) __stcs(it.dst(dp[j], u), out[u].v);
     }
 }
 
-// SUM = false: copies and zero fills only; SUM = true: also multi-source
-// sums. ES: element size in bytes.
-template <bool SUM, int ES>
+template <int VB, int ES, bool SUM, int OP>
+__device__ __forceinline__ void run_chunk(const KParams& p, const KTask& t, int nr, int nv, const int64_t* s_off,
+                                          const int64_t* d_off)
+{
+    const int total = nr * nv;
+    if (t.n_src == 0) {
+        fill_chunk<VB, ES>(p, t, total, nv, s_off, d_off);
+    } else if (!SUM || t.n_src == 1) {
+        copy_chunk<VB, ES>(p, t, total, nv, s_off, d_off);
+    } else if constexpr (SUM) {
+        reduce_chunk<VB, ES, OP>(p, t, total, nv, s_off, d_off);
+    }
+}
+
+// SUM = false: copies and fills only; SUM = true: also multi-source
+// reductions with OP (every reduction of one launch has the same op, that of
+// the source spec). ES: element size in bytes.
+template <bool SUM, int ES, int OP>
 __global__ void __launch_bounds__(kBlock, 4) boxing_kernel(const __grid_constant__ KParams p)
 {
     __shared__ int64_t s_off[kBlock], d_off[kBlock];
@@ -239,11 +302,11 @@ __global__ void __launch_bounds__(kBlock, 4) boxing_kernel(const __grid_constant
         __syncthreads();
         const int nv = (int)(len * ES / t.vec);
         switch (t.vec) {
-        case 16: run_chunk<16, ES, SUM>(p, t, nr, nv, s_off, d_off); break;
-        case 8: run_chunk<8, ES, SUM>(p, t, nr, nv, s_off, d_off); break;
-        case 4: run_chunk<4, ES, SUM>(p, t, nr, nv, s_off, d_off); break;
+        case 16: run_chunk<16, ES, SUM, OP>(p, t, nr, nv, s_off, d_off); break;
+        case 8: run_chunk<8, ES, SUM, OP>(p, t, nr, nv, s_off, d_off); break;
+        case 4: run_chunk<4, ES, SUM, OP>(p, t, nr, nv, s_off, d_off); break;
         default:
-            if constexpr (ES == 2) run_chunk<2, ES, SUM>(p, t, nr, nv, s_off, d_off);
+            if constexpr (ES == 2) run_chunk<2, ES, SUM, OP>(p, t, nr, nv, s_off, d_off);
             break;
         }
         __syncthreads();
@@ -366,16 +429,28 @@ int launch_tasks(int dtype, const std::vector<PlanTask>& tasks, const void* cons
         prm.n_tasks = nt;
         prm.total_chunks = chunks;
         bool any_sum = false;
-        for (int k = 0; k < nt; ++k) any_sum = any_sum || prm.tasks[k].n_src > 1;
+        int sum_op = RED_SUM;
+        for (int k = 0; k < nt; ++k)
+            if (prm.tasks[k].n_src > 1) {
+                if (any_sum && prm.tasks[k].op != sum_op)
+                    return fail(RTP_EUNSUPPORTED, "reshard: reductions of different kinds in one launch");
+                any_sum = true;
+                sum_op = prm.tasks[k].op;
+            }
         if (chunks == 0) continue;
         const int grid = (int)std::min<int64_t>(chunks, max_grid);
         cudaStream_t st = static_cast<cudaStream_t>(stream);
-        if (es == 4) {
-            if (any_sum) boxing_kernel<true, 4><<<grid, kBlock, 0, st>>>(prm);
-            else boxing_kernel<false, 4><<<grid, kBlock, 0, st>>>(prm);
+        if (!any_sum) {
+            if (es == 4) boxing_kernel<false, 4, RED_SUM><<<grid, kBlock, 0, st>>>(prm);
+            else boxing_kernel<false, 2, RED_SUM><<<grid, kBlock, 0, st>>>(prm);
+        } else if (es == 4) {
+            if (sum_op == RED_MIN) boxing_kernel<true, 4, RED_MIN><<<grid, kBlock, 0, st>>>(prm);
+            else if (sum_op == RED_MAX) boxing_kernel<true, 4, RED_MAX><<<grid, kBlock, 0, st>>>(prm);
+            else boxing_kernel<true, 4, RED_SUM><<<grid, kBlock, 0, st>>>(prm);
         } else {
-            if (any_sum) boxing_kernel<true, 2><<<grid, kBlock, 0, st>>>(prm);
-            else boxing_kernel<false, 2><<<grid, kBlock, 0, st>>>(prm);
+            if (sum_op == RED_MIN) boxing_kernel<true, 2, RED_MIN><<<grid, kBlock, 0, st>>>(prm);
+            else if (sum_op == RED_MAX) boxing_kernel<true, 2, RED_MAX><<<grid, kBlock, 0, st>>>(prm);
+            else boxing_kernel<true, 2, RED_SUM><<<grid, kBlock, 0, st>>>(prm);
         }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return fail(RTP_ECUDA, "boxing kernel launch failed: %s", cudaGetErrorString(e));
