@@ -218,6 +218,15 @@ def run_ours(args, rank, world, local_rank):
 
     mlp = mlp_buffers(MLP, False)
     dom = mlp_buffers(DOMINO, True)
+    # training: the forward that keeps H, and the backward from a bf16 dZ
+    M_, K_, F_, N_, P_ = MLP["M"], MLP["K"], MLP["F"], MLP["N"], MLP["P"]
+    trn = dict(H=[torch.empty((M_, F_ // P_), dtype=torch.bfloat16, device=dev) for _ in range(P_)],
+               dZ=randn((M_, N_), torch.bfloat16),
+               dH=[torch.empty((M_, F_ // P_), dtype=torch.bfloat16, device=dev) for _ in range(P_)],
+               dX=torch.empty((M_, K_), dtype=torch.float32, device=dev),
+               dA=[torch.empty((K_, F_ // P_), dtype=torch.float32, device=dev) for _ in range(P_)],
+               dB=[torch.empty((F_ // P_, N_), dtype=torch.float32, device=dev) for _ in range(P_)],
+               parts=[torch.empty((M_, K_), dtype=torch.float32, device=dev) for _ in range(P_)])
     # sequence parallel: X split by rows over the ranks, Z scattered by rows
     sp_rows = MLP["M"] // MLP["P"]
     sp_x = [mlp["X"][r * sp_rows:(r + 1) * sp_rows].contiguous() for r in range(MLP["P"])]
@@ -244,12 +253,25 @@ def run_ours(args, rank, world, local_rank):
     def run_reduce():
         rtp.reshard(dom["parts"], dom_shape, dom_red_src, dom_red_dst, out=[dom["Z"]])
 
+    def run_train_fwd():
+        rtp.tp_mlp_train_forward(mlp["X"], mlp["A"], mlp["B"], Y=mlp["Y"], H=trn["H"], Z=mlp["Z"])
+
+    def run_bwd():
+        rtp.tp_mlp_backward(mlp["X"], mlp["A"], mlp["B"], trn["H"], mlp["Y"], trn["dZ"], dH=trn["dH"], dX=trn["dX"],
+                            dA=trn["dA"], dB=trn["dB"], mode=1)
+
+    def run_bwd_overlap():
+        rtp.tp_mlp_backward(mlp["X"], mlp["A"], mlp["B"], trn["H"], mlp["Y"], trn["dZ"], dH=trn["dH"], dX=trn["dX"],
+                            dA=trn["dA"], dB=trn["dB"], dX_partials=trn["parts"], mode=0, s1=s1)
+
     ops = [(label, (lambda c=c, i=i, s=s, o=o, d=d: rtp.reshard(i, SWEEP_SHAPE, s, d, out=o)), nbytes, nl)
            for (label, c, i, s, o, d, nbytes, nl) in sweep]
     shard_ops = [(label, (lambda T=T, sp=sp, o=o: rtp.shard(T, sp, out=o)), nbytes, nl)
                  for (label, T, sp, o, nbytes, nl) in shards]
     launches_per_step = (sum(x[3] for x in ops) + sum(x[3] for x in shard_ops) +
-                         2 + 2 + 6 + 3 + 1)  # mlp 2, sequence parallel 2, domino 2x3, serial 3, reduce 1
+                         2 + 2 + 6 + 3 + 1 + 2 + 4 + 5)
+    # mlp 2, sequence parallel 2, domino 2x3, serial 3, reduce 1, training forward 2, backward 4, backward with
+    # the separate, overlapped dX sum 5
     E = lambda: torch.cuda.Event(enable_timing=True)
 
     def step(record):
@@ -268,7 +290,8 @@ def run_ours(args, rank, world, local_rank):
             e1.record()
             record.append(("reshard", label, e0, e1, nbytes))
         for kind, fn in (("mlp", run_mlp), ("sp", run_sp), ("domino", run_domino), ("serial", run_serial),
-                         ("reduce", run_reduce)):
+                         ("reduce", run_reduce), ("train_fwd", run_train_fwd), ("bwd", run_bwd),
+                         ("bwd_overlap", run_bwd_overlap)):
             flush.zero_()
             e0, e1 = E(), E()
             e0.record()
@@ -308,6 +331,9 @@ def run_ours(args, rank, world, local_rank):
     ser_ms = per[("serial", "serial")][0] / args.steps
     red_ms = per[("reduce", "reduce")][0] / args.steps
     sp_ms = per[("sp", "sp")][0] / args.steps
+    tf_ms = per[("train_fwd", "train_fwd")][0] / args.steps
+    bwd_ms = per[("bwd", "bwd")][0] / args.steps
+    bwo_ms = per[("bwd_overlap", "bwd_overlap")][0] / args.steps
 
     def max_over_ranks(x):
         if dist is None:
@@ -341,6 +367,12 @@ def run_ours(args, rank, world, local_rank):
         "f2_tp_mlp_sequence_parallel": {"ms": round(sp_ms, 4), "tflops": round(MLP_FLOPS / (sp_ms * 1e-3) / 1e12, 1),
                                         "frac_bf16": round(MLP_FLOPS / (sp_ms * 1e-3) / 1e12 / bf16_peak, 4)},
         "f3_infer_sbp_signature": {"us_per_call": host["sbp_signature_us"], "where": "host"},
+        "f1_tp_mlp_backward": {"ms": round(bwd_ms, 4), "tflops": round(2 * MLP_FLOPS / (bwd_ms * 1e-3) / 1e12, 1),
+                               "frac_bf16": round(2 * MLP_FLOPS / (bwd_ms * 1e-3) / 1e12 / bf16_peak, 4),
+                               "dX_sum": "fused in the GEMM",
+                               "ms_separate_dX_sum_overlapped": round(bwo_ms, 4),
+                               "train_forward_ms": round(tf_ms, 4),
+                               "train_forward_tflops": round(MLP_FLOPS / (tf_ms * 1e-3) / 1e12, 1)},
     }
     reshard_ms = max_over_ranks(reshard_ms)
     mlp_ms = max_over_ranks(mlp_ms)

@@ -280,6 +280,49 @@ int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
                int col_blocks, rtp_stream s0, rtp_stream s1);
 
 /*
+ * The fused forward of rtp_tp_mlp (mode 1, one chunk) that also keeps what the
+ * backward pass needs: H_i = X A_i, the pre-activation, rounded to bf16.
+ *   H         P bf16 [M, F/P] device pointers (caller-owned, 16-byte aligned)
+ *   the rest  as in rtp_tp_mlp; Y_i = GELU of the float32 accumulator (not of
+ *             the rounded H_i), so Y and Z are bit-identical to rtp_tp_mlp's
+ * Same requirements and errors as rtp_tp_mlp; H NULL is RTP_EINVAL.
+ */
+int rtp_tp_mlp_train_forward(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
+                             const void* const* A_shards, const void* const* B_shards, void* const* Y, void* const* H,
+                             float* Z, rtp_stream stream);
+
+/*
+ * Backward pass of the tensor-parallel MLP (ColossalAI "1D tensor
+ * parallelism" page, section 2.2: each rank's column-parallel layer yields a
+ * partial input gradient dY_i A_i^T and the full one is their all-reduced sum;
+ * the row-parallel layer's input Y_i is already split the way its gradient is
+ * needed, so dZ reaches every rank unchanged). Per rank i:
+ *   dH_i = bf16( (dZ B_i^T) * GELU'(H_i) )     GELU'(h) = Phi(h) + h phi(h)
+ *   dA_i = X^T dH_i         dB_i = Y_i^T dZ    dX = sum_i dH_i A_i^T
+ *   X, A_shards, B_shards  as in rtp_tp_mlp (bf16 [M,K], [K,F/P], [F/P,N])
+ *   H, Y      P bf16 [M, F/P]: what rtp_tp_mlp_train_forward kept
+ *   dZ        bf16 [M, N]: gradient of the loss with respect to Z
+ *   dH        P bf16 [M, F/P] device scratch (receives dH_i)
+ *   dX_partials P float32 [M, K] device scratch for mode 0; may be NULL in mode 1
+ *   dX        float32 [M, K]; dA: P float32 [K, F/P]; dB: P float32 [F/P, N]
+ *   mode      1: the input-gradient GEMM walks all ranks' F/P ranges in one
+ *             accumulator (the all-reduce fused); 0: it writes per-rank
+ *             partials and a separate kernel sums them; with s1 != s0 that sum
+ *             runs on s1 beside the weight-gradient GEMMs on s0 (the DeepSpeed
+ *             Domino page, backward: the all-reduce of the input gradient
+ *             overlaps the same micro-batch's weight-gradient GEMMs)
+ *   s0, s1    streams; the call's completion is ordered on s0
+ * float32 accumulation of bf16 products throughout; GELU' is evaluated in
+ * float32 on the bf16 H_i. Requirements: F % P == 0, K, F/P, N multiples of 8,
+ * P <= 8, pointers 16-byte aligned (RTP_ESHAPE / RTP_EUNSUPPORTED /
+ * RTP_EINVAL). M == 0 zeroes dA and dB. Errors leave nothing launched.
+ */
+int rtp_tp_mlp_backward(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X, const void* const* A_shards,
+                        const void* const* B_shards, const void* const* H, const void* const* Y, const void* dZ,
+                        void* const* dH, void* const* dX_partials, float* dX, float* const* dA, float* const* dB,
+                        int mode, rtp_stream s0, rtp_stream s1);
+
+/*
  * The tensor-parallel MLP with sequence parallelism (ColossalAI "1D tensor
  * parallelism" page, section 5.3: with sequence parallelism the column-parallel
  * layer all-gathers its input in the forward pass and the row-parallel layer

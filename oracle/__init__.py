@@ -133,9 +133,14 @@ def _load():
     lib.oracle_gelu.restype = ctypes.c_double
     lib.oracle_tp_mlp.argtypes = [ctypes.c_int64] * 5 + [P(ctypes.c_uint16), vpp, vpp, ctypes.c_int, ctypes.c_int,
                                                          ctypes.c_int64, i64p, dblp, dblp]
+    lib.oracle_gelu_grad.argtypes = [ctypes.c_double]
+    lib.oracle_gelu_grad.restype = ctypes.c_double
+    lib.oracle_tp_mlp_backward.argtypes = ([ctypes.c_int64] * 5 + [P(ctypes.c_uint16), vpp, vpp, P(ctypes.c_uint16),
+                                           ctypes.c_int, ctypes.c_int64, i64p, dblp, dblp, dblp, dblp,
+                                           ctypes.c_int64, i64p, dblp, dblp])
     for f in ("oracle_shard_box", "oracle_shard", "oracle_gather", "oracle_reshard",
               "oracle_layout_from_dims_mapping", "oracle_layout_from_onnx", "oracle_infer_spmd",
-              "oracle_reshape_spmd", "oracle_tp_mlp"):
+              "oracle_reshape_spmd", "oracle_tp_mlp", "oracle_tp_mlp_backward"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -334,6 +339,42 @@ def bf16_round(x: float) -> int:
 
 def gelu(x: float) -> float:
     return float(_load().oracle_gelu(float(x)))
+
+
+def gelu_grad(x: float) -> float:
+    return float(_load().oracle_gelu_grad(float(x)))
+
+
+def tp_mlp_backward(X, A_shards, B_shards, dZ, rows=(), cols=(), flags: int = 7):
+    """Gradients of sum(dZ * Z) for Z = sum_i GELU(X A_i) B_i (all bf16 bit
+    patterns), in float64. flags: 1 round H, 2 round Y, 4 round dH to bf16
+    (7 = what a bf16 pipeline stores; 0 = the exact gradient).
+    Returns a dict with, for the listed rows m: dX [r, K], dH (before its own
+    rounding), dY and H [r, F]; for the listed hidden columns f in [0, F):
+    dA [c, K] = dA_{f // (F/P)}[:, f % (F/P)] and dB [c, N] = the matching row of dB."""
+    X = np.ascontiguousarray(X, dtype=np.uint16)
+    dZ = np.ascontiguousarray(dZ, dtype=np.uint16)
+    A_shards = [np.ascontiguousarray(a, dtype=np.uint16) for a in A_shards]
+    B_shards = [np.ascontiguousarray(b, dtype=np.uint16) for b in B_shards]
+    P = len(A_shards)
+    M, K = X.shape
+    Fp = A_shards[0].shape[1]
+    N = B_shards[0].shape[1]
+    F = Fp * P
+    rows = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1)
+    cols = np.ascontiguousarray(cols, dtype=np.int64).reshape(-1)
+    out = {"dX": np.zeros((len(rows), K)), "dH": np.zeros((len(rows), F)), "dY": np.zeros((len(rows), F)),
+           "H": np.zeros((len(rows), F)), "dA": np.zeros((len(cols), K)), "dB": np.zeros((len(cols), N))}
+    ap = (ctypes.c_void_p * P)(*[a.ctypes.data for a in A_shards])
+    bp = (ctypes.c_void_p * P)(*[b.ctypes.data for b in B_shards])
+    dbl = ctypes.POINTER(ctypes.c_double)
+    u16 = ctypes.POINTER(ctypes.c_uint16)
+    i64 = ctypes.POINTER(ctypes.c_int64)
+    d = {k: v.ctypes.data_as(dbl) for k, v in out.items()}
+    _ok(_load().oracle_tp_mlp_backward(P, M, K, F, N, X.ctypes.data_as(u16), ap, bp, dZ.ctypes.data_as(u16), flags,
+                                       len(rows), rows.ctypes.data_as(i64), d["dX"], d["dH"], d["dY"], d["H"],
+                                       len(cols), cols.ctypes.data_as(i64), d["dA"], d["dB"]), "tp_mlp_backward")
+    return out
 
 
 def tp_mlp(X: np.ndarray, A_shards: Sequence[np.ndarray], B_shards: Sequence[np.ndarray], rows=None,

@@ -22,6 +22,10 @@
 //   * TP-MLP: ColossalAI 1D tensor parallelism page (mhpq.cn) section 2 and
 //     2.1: Y_i = X A_i, Z = sum_i Y_i B_i; GELU between the GEMMs from the
 //     Domino page (mzlw.cn), forward section ("GeMM GeLU GeMM").
+//   * TP-MLP backward: ColossalAI page section 2.2: each rank's input
+//     gradient is dY_i A_i^T and the full one is their sum; the weight
+//     gradients are the usual products of the layer input and the output
+//     gradient, on each rank's own shard.
 //
 // Readings where the pages are silent (each is listed in the design notes):
 //   * uneven extents: ceil-sized leading shards, applied level by level;
@@ -29,6 +33,8 @@
 //     all zero holds the tensor, the others hold the reduction's identity
 //     (0 for sum, +inf for min, -inf for max);
 //   * GELU is the exact erf form; Y is rounded to bf16 before the second GEMM.
+//   * backward: the saved pre-activation H and the gradient dH are bf16
+//     tensors (the compute type), so they may be rounded (flags below).
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -710,6 +716,13 @@ uint16_t oracle_bf16_round(double x) { return double_to_bf16_bits(x); }
 
 double oracle_gelu(double x) { return 0.5 * x * (1.0 + std::erf(x / std::sqrt(2.0))); }
 
+// Derivative of the exact GELU x Phi(x): Phi(x) + x phi(x).
+double oracle_gelu_grad(double x)
+{
+    const double pi = 3.14159265358979323846;
+    return 0.5 * (1.0 + std::erf(x / std::sqrt(2.0))) + x * std::exp(-0.5 * x * x) / std::sqrt(2.0 * pi);
+}
+
 // ---- TP-MLP -------------------------------------------------------------------
 
 // Megatron 1D tensor-parallel MLP on P virtual devices, for the listed rows of X:
@@ -749,6 +762,79 @@ int oracle_tp_mlp(int64_t P, int64_t M, int64_t K, int64_t F, int64_t N, const u
                 const uint16_t* brow = B[i] + f * N;
                 for (int64_t n = 0; n < N; ++n) z[n] += y[f] * bf16_bits_to_double(brow[n]);
             }
+        }
+    }
+    return 0;
+}
+
+// Backward of the TP-MLP above (act = GELU) for the loss L = sum(dZ * Z),
+// i.e. dZ is the gradient arriving at Z. With H_i = X A_i, Y_i = GELU(H_i):
+//   dY_i = dZ B_i^T,  dH_i = dY_i * GELU'(H_i),
+//   dX   = sum_i dH_i A_i^T,  dA_i = X^T dH_i,  dB_i = Y_i^T dZ.
+// All products are summed in double. flags select the bf16 roundings of the
+// stored tensors: 1 = H rounded before GELU', 2 = Y rounded (as the forward
+// stores it), 4 = dH rounded before the products that read it. flags = 0 gives
+// the exact gradient.
+// Rows (of X, dX): for each listed row m
+//   dx_out [n_rows, K] = row m of dX; dh_out / dy_out / h_out (optional,
+//   [n_rows, F], shard i in columns [i F/P, (i+1) F/P)) = row m of dH (before
+//   rounding), dY and H (after rounding if flag 1).
+// Columns (of the hidden dimension): for each listed f in [0, F) (rank
+//   i = f / (F/P), local column f - i F/P)
+//   da_out [n_cols, K] = column f of A's gradient (dA_i[:, local f]),
+//   db_out [n_cols, N] = row f of B's gradient (dB_i[local f, :]).
+int oracle_tp_mlp_backward(int64_t P, int64_t M, int64_t K, int64_t F, int64_t N, const uint16_t* X,
+                           const uint16_t* const* A, const uint16_t* const* B, const uint16_t* dZ, int flags,
+                           int64_t n_rows, const int64_t* rows, double* dx_out, double* dh_out, double* dy_out,
+                           double* h_out, int64_t n_cols, const int64_t* cols, double* da_out, double* db_out)
+{
+    if (P < 1 || F % P != 0 || M < 0 || K < 1 || N < 1 || n_rows < 0 || n_cols < 0) return -1;
+    const int64_t Fp = F / P;
+    const bool round_h = flags & 1, round_y = flags & 2, round_dh = flags & 4;
+    auto rnd = [](double v) { return bf16_bits_to_double(double_to_bf16_bits(v)); };
+    auto a_at = [&](int64_t k, int64_t f) { return bf16_bits_to_double(A[f / Fp][k * Fp + f % Fp]); };
+    auto b_at = [&](int64_t f, int64_t n) { return bf16_bits_to_double(B[f / Fp][(f % Fp) * N + n]); };
+    std::vector<double> x((size_t)K), dz((size_t)N), dh((size_t)F);
+    for (int64_t r = 0; r < n_rows; ++r) {
+        const int64_t m = rows[r];
+        if (m < 0 || m >= M) return -1;
+        for (int64_t k = 0; k < K; ++k) x[k] = bf16_bits_to_double(X[m * K + k]);
+        for (int64_t n = 0; n < N; ++n) dz[n] = bf16_bits_to_double(dZ[m * N + n]);
+        for (int64_t f = 0; f < F; ++f) {
+            double h = 0.0, dy = 0.0;
+            for (int64_t k = 0; k < K; ++k) h += x[k] * a_at(k, f);
+            for (int64_t n = 0; n < N; ++n) dy += dz[n] * b_at(f, n);
+            if (round_h) h = rnd(h);
+            const double g = dy * oracle_gelu_grad(h);
+            if (dh_out) dh_out[r * F + f] = g;
+            if (dy_out) dy_out[r * F + f] = dy;
+            if (h_out) h_out[r * F + f] = h;
+            dh[f] = round_dh ? rnd(g) : g;
+        }
+        for (int64_t k = 0; k < K; ++k) {
+            double acc = 0.0;
+            for (int64_t f = 0; f < F; ++f) acc += dh[f] * a_at(k, f);
+            dx_out[r * K + k] = acc;
+        }
+    }
+    for (int64_t c = 0; c < n_cols; ++c) {
+        const int64_t f = cols[c];
+        if (f < 0 || f >= F) return -1;
+        double* da = da_out + c * K;
+        double* db = db_out + c * N;
+        for (int64_t k = 0; k < K; ++k) da[k] = 0.0;
+        for (int64_t n = 0; n < N; ++n) db[n] = 0.0;
+        for (int64_t m = 0; m < M; ++m) {
+            double h = 0.0, dy = 0.0;
+            for (int64_t k = 0; k < K; ++k) h += bf16_bits_to_double(X[m * K + k]) * a_at(k, f);
+            for (int64_t n = 0; n < N; ++n) dy += bf16_bits_to_double(dZ[m * N + n]) * b_at(f, n);
+            double y = oracle_gelu(h);
+            if (round_y) y = rnd(y);
+            if (round_h) h = rnd(h);
+            double g = dy * oracle_gelu_grad(h);
+            if (round_dh) g = rnd(g);
+            for (int64_t k = 0; k < K; ++k) da[k] += bf16_bits_to_double(X[m * K + k]) * g;
+            for (int64_t n = 0; n < N; ++n) db[n] += y * bf16_bits_to_double(dZ[m * N + n]);
         }
     }
     return 0;

@@ -101,6 +101,10 @@ def _load():
                                vp, vp],
         "rtp_tp_mlp": [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vpp, vpp, vpp,
                        vpp, vp, c_int, c_int, c_int, vp, vp],
+        "rtp_tp_mlp_train_forward": [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vpp,
+                                     vpp, vpp, vpp, vp, vp],
+        "rtp_tp_mlp_backward": [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vpp, vpp,
+                                vpp, vpp, vp, vpp, vpp, vp, vpp, vpp, c_int, vp, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -376,6 +380,64 @@ def tp_mlp(X, A_shards, B_shards, Y=None, partials=None, Z=None, mode: int = 1, 
                               _ptrs([b.data_ptr() for b in B_shards]), _ptrs([y.data_ptr() for y in Y]), pp,
                               Z.data_ptr(), mode, chunks, col_blocks, _stream_ptr(s0), _stream_ptr(s1)))
     return Z, Y
+
+
+def tp_mlp_train_forward(X, A_shards, B_shards, Y=None, H=None, Z=None, stream=None):
+    """The fused forward that also keeps the bf16 pre-activations H_i = X A_i
+    for the backward pass. Returns (Z, Y, H)."""
+    torch = _torch()
+    P = len(A_shards)
+    M, K = X.shape
+    Fp = A_shards[0].shape[1]
+    N = B_shards[0].shape[1]
+    dev = X.device
+    if Y is None:
+        Y = [torch.empty((M, Fp), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    if H is None:
+        H = [torch.empty((M, Fp), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    if Z is None:
+        Z = torch.empty((M, N), dtype=torch.float32, device=dev)
+    _check_cuda([X, Z] + list(A_shards) + list(B_shards) + list(Y) + list(H), "tp_mlp_train_forward")
+    _check(_load().rtp_tp_mlp_train_forward(P, M, K, Fp * P, N, X.data_ptr(), _ptrs([a.data_ptr() for a in A_shards]),
+                                            _ptrs([b.data_ptr() for b in B_shards]), _ptrs([y.data_ptr() for y in Y]),
+                                            _ptrs([h.data_ptr() for h in H]), Z.data_ptr(), _stream_ptr(stream)))
+    return Z, Y, H
+
+
+def tp_mlp_backward(X, A_shards, B_shards, H, Y, dZ, dH=None, dX_partials=None, dX=None, dA=None, dB=None,
+                    mode: int = 1, s0=None, s1=None):
+    """Gradients of Z = sum_i GELU(X A_i) B_i given dZ (bf16 [M, N]):
+    returns (dX, dA, dB, dH) with dX float32 [M, K], dA[i] float32 [K, F/P],
+    dB[i] float32 [F/P, N] and dH[i] = bf16(dZ B_i^T * GELU'(H_i))."""
+    torch = _torch()
+    P = len(A_shards)
+    M, K = X.shape
+    Fp = A_shards[0].shape[1]
+    N = B_shards[0].shape[1]
+    dev = X.device
+    f32, bf16 = torch.float32, torch.bfloat16
+    if dH is None:
+        dH = [torch.empty((M, Fp), dtype=bf16, device=dev) for _ in range(P)]
+    if dX is None:
+        dX = torch.empty((M, K), dtype=f32, device=dev)
+    if dA is None:
+        dA = [torch.empty((K, Fp), dtype=f32, device=dev) for _ in range(P)]
+    if dB is None:
+        dB = [torch.empty((Fp, N), dtype=f32, device=dev) for _ in range(P)]
+    if mode == 0 and dX_partials is None:
+        dX_partials = [torch.empty((M, K), dtype=f32, device=dev) for _ in range(P)]
+    _check_cuda([X, dZ, dX] + list(A_shards) + list(B_shards) + list(H) + list(Y) + list(dH) + list(dA) + list(dB)
+                + list(dX_partials or []), "tp_mlp_backward")
+    if s0 is None:
+        s0 = torch.cuda.current_stream()
+    if s1 is None:
+        s1 = s0
+    ptrs = lambda ts: _ptrs([t.data_ptr() for t in ts])
+    pp = ptrs(dX_partials) if dX_partials is not None else None
+    _check(_load().rtp_tp_mlp_backward(P, M, K, Fp * P, N, X.data_ptr(), ptrs(A_shards), ptrs(B_shards), ptrs(H),
+                                       ptrs(Y), dZ.data_ptr(), ptrs(dH), pp, dX.data_ptr(), ptrs(dA), ptrs(dB), mode,
+                                       _stream_ptr(s0), _stream_ptr(s1)))
+    return dX, dA, dB, dH
 
 
 def tp_mlp_sp(X_shards, A_shards, B_shards, Y=None, Z_shards=None, stream=None):

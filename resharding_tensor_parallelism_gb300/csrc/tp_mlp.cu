@@ -67,13 +67,21 @@ constexpr int MAX_GROUPS = 8;
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;
 
 enum : uint32_t { ERR_PRODUCER = 1, ERR_MMA_STAGE = 2, ERR_MMA_ACC = 3, ERR_EPILOGUE = 4 };
-enum { EPI_GELU_BF16 = 0, EPI_F32 = 1 };
+enum { EPI_GELU_BF16 = 0, EPI_F32 = 1, EPI_DGELU_BF16 = 2 };
+// Kernel configuration (a compile-time template parameter):
+//   CFG_SP_A    rows of the A operand come from per-shard maps (sequence parallel)
+//   CFG_SP_OUT  output rows go to per-shard buffers (sequence parallel)
+//   CFG_A_MN    A is M-major in memory (a transposed operand: X^T, Y^T)
+//   CFG_B_K     B is K-major in memory (a transposed operand: A_i^T, B_i^T)
+enum : int { CFG_SP_A = 1, CFG_SP_OUT = 2, CFG_A_MN = 4, CFG_B_K = 8 };
 
 
 struct GemmArgs {
-    CUtensorMap ta[MAX_GROUPS];  // K-major operand of each group: rows x K
-    CUtensorMap tb[MAX_GROUPS];  // N-major operand of each group: K x N
+    CUtensorMap ta[MAX_GROUPS];  // A operand of each group ([M rows, K] K-major, or [K rows, M] M-major)
+    CUtensorMap tb[MAX_GROUPS];  // B operand of each group ([K rows, N] N-major, or [N rows, K] K-major)
     void* out[MAX_GROUPS];       // output of each group (out[0] when fused)
+    void* out2[MAX_GROUPS];      // GELU epilogue: also store the pre-activation here (if not NULL)
+    const void* aux[MAX_GROUPS]; // GELU-gradient epilogue: the pre-activation H read at each output
     int64_t ldo;                 // output row stride, elements
     int32_t groups, fused, epi;
     int32_t m_tiles, n_tiles, kb_per_group;
@@ -87,6 +95,7 @@ struct GemmArgs {
     // reduce-scatter fused into the epilogue of the rank-summing GEMM).
     int32_t a_rows_per_map, a_maps;
     int32_t out_rows_per_ptr, out_ptrs;
+    int32_t cfg;                 // kernel configuration (CFG_* bits), chosen by the host
 };
 
 __device__ unsigned int g_tp_error;
@@ -205,6 +214,17 @@ __device__ __forceinline__ void tile_coords(const GemmArgs& a, int tile, int& g,
 
 __device__ __forceinline__ float gelu(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752440f)); }
 
+// d GELU(h) / dh = Phi(h) + h phi(h) for the exact erf form.
+__device__ __forceinline__ float gelu_grad(float h)
+{
+    const float cdf = 0.5f * (1.0f + erff(h * 0.70710678118654752440f));
+    const float pdf = 0.39894228040143267794f * expf(-0.5f * h * h);
+    return cdf + h * pdf;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
 {
     return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
@@ -228,10 +248,13 @@ constexpr uint32_t B2_BYTES = 128 * BK * 2;           // 16 KB: 2 boxes of 64(N)
 constexpr uint32_t STAGE2_BYTES = A2_BYTES + B2_BYTES;  // 32 KB
 constexpr size_t SMEM2_BYTES = STAGES2 * STAGE2_BYTES + 1024 + 1024;
 // Instruction descriptor of tcgen05.mma kind::f16: D float32 (bits 4-5 = 1),
-// A and B bf16 (bits 7-9 = 1, 10-12 = 1), A K-major (bit 15 = 0), B N-major
-// (bit 16 = 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28 (M = 256 for the pair).
-constexpr uint32_t IDESC2 = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) | ((uint32_t)(256 >> 3) << 17) |
-                            ((uint32_t)(BM2 >> 4) << 24);
+// A and B bf16 (bits 7-9 = 1, 10-12 = 1), bit 15 = A M-major, bit 16 = B
+// N-major, N >> 3 in bits 17-22, M >> 4 in bits 24-28 (M = 256 for the pair).
+__host__ __device__ constexpr uint32_t idesc2(bool a_mn, bool b_k)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_k ? 0u : 1u) << 16) |
+           ((uint32_t)(256 >> 3) << 17) | ((uint32_t)(BM2 >> 4) << 24);
+}
 
 __device__ __forceinline__ uint32_t cluster_rank()
 {
@@ -273,13 +296,14 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
         : "memory");
 }
-__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate)
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(IDESC2), "r"(accumulate)
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar)
@@ -294,12 +318,13 @@ __device__ __forceinline__ void mma_commit_pair_local(uint32_t bar)
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// SP_A: the K-major operand's rows come from per-shard maps (sequence-parallel
-// all-gather); SP_OUT: output rows go to per-shard buffers (reduce-scatter).
-// Compile-time, so the common kernel carries no extra work in its loops.
-template <bool SP_A, bool SP_OUT>
+// CFG (CFG_* bits) is compile-time, so each configuration's loops carry no
+// work for the others.
+template <int CFG>
 __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_constant__ GemmArgs a)
 {
+    constexpr bool SP_A = (CFG & CFG_SP_A) != 0, SP_OUT = (CFG & CFG_SP_OUT) != 0;
+    constexpr bool A_MN = (CFG & CFG_A_MN) != 0, B_K = (CFG & CFG_B_K) != 0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES2 * STAGE2_BYTES);
@@ -380,9 +405,19 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
                     const uint32_t sb = sa + A2_BYTES;
                     const uint32_t fb = leader_full0 + 8u * (uint32_t)stage;
                     if (cta == 0) mbar_expect_tx(full_bar(stage), 2 * STAGE2_BYTES);
-                    tma_load_2d_pair(sa, SP_A ? amap_sp : &a.ta[gg], fb, kk * BK, arow);
-                    tma_load_2d_pair(sb, &a.tb[gg], fb, col, kk * BK);
-                    tma_load_2d_pair(sb + B_SUB, &a.tb[gg], fb, col + 64, kk * BK);
+                    const CUtensorMap* am = SP_A ? amap_sp : &a.ta[gg];
+                    if constexpr (A_MN) {  // two 64(M) x 64(K) boxes
+                        tma_load_2d_pair(sa, am, fb, arow, kk * BK);
+                        tma_load_2d_pair(sa + B_SUB, am, fb, arow + 64, kk * BK);
+                    } else {  // one 128(M) x 64(K) box
+                        tma_load_2d_pair(sa, am, fb, kk * BK, arow);
+                    }
+                    if constexpr (B_K) {  // one 128(N) x 64(K) box
+                        tma_load_2d_pair(sb, &a.tb[gg], fb, kk * BK, col);
+                    } else {  // two 64(N) x 64(K) boxes
+                        tma_load_2d_pair(sb, &a.tb[gg], fb, col, kk * BK);
+                        tma_load_2d_pair(sb + B_SUB, &a.tb[gg], fb, col + 64, kk * BK);
+                    }
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++kk == a.kb_per_group) {  // next rank's K range (fused reduction)
@@ -415,11 +450,14 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
-            // K-major A: 32-byte steps inside the 128-byte swizzle row, 8-row groups
-            // 1024 bytes apart. N-major B: 16 K-rows = 2 groups of 8 rows of 128 bytes;
-            // the two 64-wide N boxes are B_SUB bytes apart.
-            const uint64_t desc_a0 = smem_desc(smem_u32(smem), 16u, 1024u);
-            const uint64_t desc_b0 = smem_desc(smem_u32(smem) + A2_BYTES, B_SUB, 1024u);
+            // K-major operand: 32-byte steps (16 bf16) inside the 128-byte swizzle
+            // row, 8-row groups 1024 bytes apart. M/N-major operand: 16 K-rows = 2
+            // groups of 8 rows of 128 bytes (2048-byte steps); its two 64-wide boxes
+            // are B_SUB bytes apart.
+            constexpr uint32_t a_step = A_MN ? 2048u : 32u, b_step = B_K ? 32u : 2048u;
+            constexpr uint32_t idesc = idesc2(A_MN, B_K);
+            const uint64_t desc_a0 = smem_desc(smem_u32(smem), A_MN ? B_SUB : 16u, 1024u);
+            const uint64_t desc_b0 = smem_desc(smem_u32(smem) + A2_BYTES, B_K ? 16u : B_SUB, 1024u);
             uint32_t acc_phase = 0;
             bool ok = true;
             for (int tile = pair; ok && tile < a.total_tiles; tile += npairs) {
@@ -439,9 +477,9 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
                     const uint64_t off = (uint64_t)((uint32_t)stage * STAGE2_BYTES >> 4);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        const uint64_t da = desc_a0 + off + (uint64_t)(32u * k >> 4);
-                        const uint64_t db = desc_b0 + off + (uint64_t)(2048u * k >> 4);
-                        mma_bf16_pair(d_tmem, da, db, (kb > 0 || k > 0) ? 1u : 0u);
+                        const uint64_t da = desc_a0 + off + (uint64_t)(a_step * k >> 4);
+                        const uint64_t db = desc_b0 + off + (uint64_t)(b_step * k >> 4);
+                        mma_bf16_pair(d_tmem, da, db, idesc, (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit_pair(empty_bar(stage));
                     if (++stage == STAGES2) {
@@ -494,6 +532,8 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
                 if (!row_ok || c0 >= a.n_end) continue;
                 if (a.epi == EPI_GELU_BF16) {
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_base) + orow * a.ldo + c0);
+                    uint4* hdst = a.out2[g] ? reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out2[g]) + orow * a.ldo + c0)
+                                            : nullptr;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         if (c0 + 8 * q >= a.n_end) break;
@@ -502,6 +542,33 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
                         v.y = pack_bf16(gelu(__uint_as_float(r[8 * q + 2])), gelu(__uint_as_float(r[8 * q + 3])));
                         v.z = pack_bf16(gelu(__uint_as_float(r[8 * q + 4])), gelu(__uint_as_float(r[8 * q + 5])));
                         v.w = pack_bf16(gelu(__uint_as_float(r[8 * q + 6])), gelu(__uint_as_float(r[8 * q + 7])));
+                        __stcs(dst + q, v);
+                        if (hdst) {  // the pre-activation, for the backward pass
+                            uint4 h;
+                            h.x = pack_bf16(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]));
+                            h.y = pack_bf16(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]));
+                            h.z = pack_bf16(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]));
+                            h.w = pack_bf16(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]));
+                            __stcs(hdst + q, h);
+                        }
+                    }
+                } else if (a.epi == EPI_DGELU_BF16) {
+                    // dH = dY * GELU'(H): the accumulator is dY, H is read at the same place
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_base) + orow * a.ldo + c0);
+                    const uint4* hsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.aux[g]) + orow * a.ldo + c0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (c0 + 8 * q >= a.n_end) break;
+                        const uint4 h = __ldcs(hsrc + q);
+                        uint4 v;
+                        v.x = pack_bf16(__uint_as_float(r[8 * q + 0]) * gelu_grad(bf16_lo(h.x)),
+                                        __uint_as_float(r[8 * q + 1]) * gelu_grad(bf16_hi(h.x)));
+                        v.y = pack_bf16(__uint_as_float(r[8 * q + 2]) * gelu_grad(bf16_lo(h.y)),
+                                        __uint_as_float(r[8 * q + 3]) * gelu_grad(bf16_hi(h.y)));
+                        v.z = pack_bf16(__uint_as_float(r[8 * q + 4]) * gelu_grad(bf16_lo(h.z)),
+                                        __uint_as_float(r[8 * q + 5]) * gelu_grad(bf16_hi(h.z)));
+                        v.w = pack_bf16(__uint_as_float(r[8 * q + 6]) * gelu_grad(bf16_lo(h.w)),
+                                        __uint_as_float(r[8 * q + 7]) * gelu_grad(bf16_hi(h.w)));
                         __stcs(dst + q, v);
                     }
                 } else {
@@ -563,7 +630,7 @@ int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int bo
     return RTP_OK;
 }
 
-template <bool SP_A, bool SP_OUT>
+template <int CFG>
 int launch_gemm_t(GemmArgs& args, cudaStream_t stream)
 {
     static bool configured[64] = {};
@@ -582,11 +649,11 @@ int launch_gemm_t(GemmArgs& args, cudaStream_t stream)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tp_gemm_kernel<SP_A, SP_OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM2_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(tp_gemm_kernel<CFG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM2_BYTES);
         if (e != cudaSuccess) return fail(RTP_ECUDA, "tp_mlp: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         cfg.gridDim = dim3(2 * 64);
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, tp_gemm_kernel<SP_A, SP_OUT>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, tp_gemm_kernel<CFG>, &cfg);
         if (e != cudaSuccess || n <= 0) return fail(RTP_ECUDA, "tp_mlp: cudaOccupancyMaxActiveClusters: %s", cudaGetErrorString(e));
         max_clusters[dev] = n;
         configured[dev] = true;
@@ -595,16 +662,21 @@ int launch_gemm_t(GemmArgs& args, cudaStream_t stream)
     const int clusters = args.total_tiles < max_clusters[dev] ? args.total_tiles : max_clusters[dev];
     if (clusters <= 0) return RTP_OK;
     cfg.gridDim = dim3(2 * clusters);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, tp_gemm_kernel<SP_A, SP_OUT>, args);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, tp_gemm_kernel<CFG>, args);
     if (e != cudaSuccess) return fail(RTP_ECUDA, "tp_mlp: GEMM launch failed: %s", cudaGetErrorString(e));
     return RTP_OK;
 }
 
 int launch_gemm(GemmArgs& args, cudaStream_t stream)
 {
-    if (args.a_rows_per_map > 0) return launch_gemm_t<true, false>(args, stream);
-    if (args.out_rows_per_ptr > 0) return launch_gemm_t<false, true>(args, stream);
-    return launch_gemm_t<false, false>(args, stream);
+    switch (args.cfg) {
+    case 0: return launch_gemm_t<0>(args, stream);
+    case CFG_SP_A: return launch_gemm_t<CFG_SP_A>(args, stream);
+    case CFG_SP_OUT: return launch_gemm_t<CFG_SP_OUT>(args, stream);
+    case CFG_A_MN: return launch_gemm_t<CFG_A_MN>(args, stream);
+    case CFG_B_K: return launch_gemm_t<CFG_B_K>(args, stream);
+    default: return fail(RTP_EUNSUPPORTED, "tp_mlp: no GEMM kernel for configuration %d", args.cfg);
+    }
 }
 
 struct Events {
@@ -634,13 +706,13 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 using namespace rtp;
 
-extern "C" {
+namespace {
 
-int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X, const void* const* A_shards,
-               const void* const* B_shards, void* const* Y, void* const* partials, float* Z, int mode, int chunks,
-               int col_blocks, rtp_stream s0_, rtp_stream s1_)
+// Forward MLP; H (may be NULL) receives the bf16 pre-activations X A_i.
+int tp_mlp_impl(const char* fn, int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
+                const void* const* A_shards, const void* const* B_shards, void* const* Y, void* const* H,
+                void* const* partials, float* Z, int mode, int chunks, int col_blocks, rtp_stream s0_, rtp_stream s1_)
 {
-    const char* fn = "rtp_tp_mlp";
     if (P < 1 || P > MAX_GROUPS) return fail(RTP_EUNSUPPORTED, "%s: P = %d outside [1, %d]", fn, P, MAX_GROUPS);
     if (!X || !A_shards || !B_shards || !Y || !Z) return fail(RTP_EINVAL, "%s: NULL argument", fn);
     if (mode != 0 && mode != 1) return fail(RTP_EINVAL, "%s: mode %d", fn, mode);
@@ -659,9 +731,10 @@ int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
         return fail(RTP_ESHAPE, "%s: extents must stay below 2^31", fn);
     if (!aligned16(X) || !aligned16(Z)) return fail(RTP_EINVAL, "%s: X and Z must be 16-byte aligned", fn);
     for (int i = 0; i < P; ++i) {
-        if (!A_shards[i] || !B_shards[i] || !Y[i] || (mode == 0 && !partials[i]))
+        if (!A_shards[i] || !B_shards[i] || !Y[i] || (mode == 0 && !partials[i]) || (H && !H[i]))
             return fail(RTP_EINVAL, "%s: NULL buffer for rank %d", fn, i);
-        if (!aligned16(A_shards[i]) || !aligned16(B_shards[i]) || !aligned16(Y[i]) || (mode == 0 && !aligned16(partials[i])))
+        if (!aligned16(A_shards[i]) || !aligned16(B_shards[i]) || !aligned16(Y[i]) ||
+            (mode == 0 && !aligned16(partials[i])) || (H && !aligned16(H[i])))
             return fail(RTP_EINVAL, "%s: buffers of rank %d must be 16-byte aligned", fn, i);
     }
     if (M == 0) return RTP_OK;
@@ -684,6 +757,7 @@ int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
         if ((st = make_map(&g1.ta[i], X, M, K, 128))) return st;
         if ((st = make_map(&g1.tb[i], A_shards[i], K, Fp, BK))) return st;
         g1.out[i] = Y[i];
+        g1.out2[i] = H ? H[i] : nullptr;
         if ((st = make_map(&g2.ta[i], Y[i], M, Fp, 128))) return st;
         if ((st = make_map(&g2.tb[i], B_shards[i], Fp, N, BK))) return st;
         g2.out[i] = mode == 0 ? partials[i] : (void*)Z;
@@ -756,6 +830,146 @@ int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
     return RTP_OK;
 }
 
+// Sum over the ranks of a float32 [M, cols] buffer: dst = sum_i parts[i], as
+// one task of the boxing kernel on `stream`.
+int reduce_partials(int P, int64_t M, int64_t cols, void* const* parts, float* dst, cudaStream_t stream, int blocks_per_sm)
+{
+    PlanTask t;
+    t.cols = M * cols;
+    t.rows = 1;
+    t.n_outer = 0;
+    for (int i = 0; i < P; ++i) t.src.push_back(Ref{i, 0});
+    t.dst.push_back(Ref{0, 0});
+    std::vector<PlanTask> tasks{t};
+    void* d[1] = {dst};
+    return launch_tasks(RTP_F32, tasks, (const void* const*)parts, d, stream, nullptr, blocks_per_sm);
+}
+
+}  // namespace
+
+extern "C" {
+
+int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X, const void* const* A_shards,
+               const void* const* B_shards, void* const* Y, void* const* partials, float* Z, int mode, int chunks,
+               int col_blocks, rtp_stream s0, rtp_stream s1)
+{
+    return tp_mlp_impl("rtp_tp_mlp", P, M, K, F, N, X, A_shards, B_shards, Y, nullptr, partials, Z, mode, chunks,
+                       col_blocks, s0, s1);
+}
+
+int rtp_tp_mlp_train_forward(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
+                             const void* const* A_shards, const void* const* B_shards, void* const* Y, void* const* H,
+                             float* Z, rtp_stream stream)
+{
+    if (!H) return fail(RTP_EINVAL, "rtp_tp_mlp_train_forward: NULL H");
+    return tp_mlp_impl("rtp_tp_mlp_train_forward", P, M, K, F, N, X, A_shards, B_shards, Y, H, nullptr, Z, 1, 1, 1,
+                       stream, stream);
+}
+
+int rtp_tp_mlp_backward(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X, const void* const* A_shards,
+                        const void* const* B_shards, const void* const* H, const void* const* Y, const void* dZ,
+                        void* const* dH, void* const* dX_partials, float* dX, float* const* dA, float* const* dB,
+                        int mode, rtp_stream s0_, rtp_stream s1_)
+{
+    const char* fn = "rtp_tp_mlp_backward";
+    if (P < 1 || P > MAX_GROUPS) return fail(RTP_EUNSUPPORTED, "%s: P = %d outside [1, %d]", fn, P, MAX_GROUPS);
+    if (!A_shards || !B_shards || !H || !Y || !dH || !dA || !dB) return fail(RTP_EINVAL, "%s: NULL argument", fn);
+    if (M > 0 && (!X || !dZ || !dX)) return fail(RTP_EINVAL, "%s: NULL argument", fn);
+    if (mode != 0 && mode != 1) return fail(RTP_EINVAL, "%s: mode %d", fn, mode);
+    if (mode == 0 && !dX_partials) return fail(RTP_EINVAL, "%s: mode 0 needs partial buffers", fn);
+    if (M < 0 || K < 1 || F < 1 || N < 1) return fail(RTP_ESHAPE, "%s: sizes M=%lld K=%lld F=%lld N=%lld", fn, (long long)M,
+                                                      (long long)K, (long long)F, (long long)N);
+    if (F % P) return fail(RTP_ESHAPE, "%s: F=%lld is not divisible by P=%d", fn, (long long)F, P);
+    const int64_t Fp = F / P;
+    if (K % 8 || Fp % 8 || N % 8) return fail(RTP_ESHAPE, "%s: K, F/P and N must be multiples of 8 (16-byte rows)", fn);
+    if (M >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 31) || Fp >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31))
+        return fail(RTP_ESHAPE, "%s: extents must stay below 2^31", fn);
+    if (!aligned16(X) || !aligned16(dZ) || !aligned16(dX))
+        return fail(RTP_EINVAL, "%s: X, dZ and dX must be 16-byte aligned", fn);
+    for (int i = 0; i < P; ++i) {
+        // buffers with M rows are empty (and may be NULL) when M == 0
+        const void* bufs[8] = {A_shards[i], B_shards[i], dA[i], dB[i], H[i], Y[i], dH[i],
+                               mode == 0 ? dX_partials[i] : (const void*)dX};
+        for (int b = 0; b < (M > 0 ? 8 : 4); ++b) {
+            if (!bufs[b]) return fail(RTP_EINVAL, "%s: NULL buffer for rank %d", fn, i);
+            if (!aligned16(bufs[b])) return fail(RTP_EINVAL, "%s: buffers of rank %d must be 16-byte aligned", fn, i);
+        }
+    }
+    cudaStream_t s0 = static_cast<cudaStream_t>(s0_), s1 = static_cast<cudaStream_t>(s1_);
+    if (M == 0) {  // no tokens: the weight gradients are zero, dX is empty
+        for (int i = 0; i < P; ++i) {
+            if (cudaMemsetAsync(dA[i], 0, (size_t)(K * Fp * 4), s0) != cudaSuccess ||
+                cudaMemsetAsync(dB[i], 0, (size_t)(Fp * N * 4), s0) != cudaSuccess)
+                return fail(RTP_ECUDA, "%s: cudaMemsetAsync failed", fn);
+        }
+        return RTP_OK;
+    }
+    const bool two_streams = mode == 0 && s1 != s0;
+    Events* ev = nullptr;
+    if (two_streams) {
+        int st = events(&ev);
+        if (st) return st;
+    }
+    static thread_local GemmArgs gh, gx, ga, gb;
+    std::memset(&gh, 0, sizeof gh);
+    std::memset(&gx, 0, sizeof gx);
+    std::memset(&ga, 0, sizeof ga);
+    std::memset(&gb, 0, sizeof gb);
+    int st;
+    for (int i = 0; i < P; ++i) {
+        // dH_i = (dZ B_i^T) * GELU'(H_i): dZ K-major [M, N], B_i^T read K-major from B_i [F/P, N]
+        if ((st = make_map(&gh.ta[i], dZ, M, N, 128))) return st;
+        if ((st = make_map(&gh.tb[i], B_shards[i], Fp, N, 128))) return st;
+        gh.out[i] = dH[i];
+        gh.aux[i] = H[i];
+        // dX (+)= dH_i A_i^T: dH_i K-major [M, F/P], A_i^T read K-major from A_i [K, F/P]
+        if ((st = make_map(&gx.ta[i], dH[i], M, Fp, 128))) return st;
+        if ((st = make_map(&gx.tb[i], A_shards[i], K, Fp, 128))) return st;
+        gx.out[i] = mode == 0 ? dX_partials[i] : (void*)dX;
+        // dA_i = X^T dH_i: X^T read M-major from X [M, K], dH_i N-major
+        if ((st = make_map(&ga.ta[i], X, M, K, 64))) return st;
+        if ((st = make_map(&ga.tb[i], dH[i], M, Fp, BK))) return st;
+        ga.out[i] = dA[i];
+        // dB_i = Y_i^T dZ: Y_i^T read M-major from Y_i [M, F/P], dZ N-major
+        if ((st = make_map(&gb.ta[i], Y[i], M, Fp, 64))) return st;
+        if ((st = make_map(&gb.tb[i], dZ, M, N, BK))) return st;
+        gb.out[i] = dB[i];
+    }
+    auto shape = [&](GemmArgs& g, int64_t rows, int64_t cols, int64_t kdim, int epi, int cfg, int fused) {
+        g.groups = P;
+        g.fused = fused;
+        g.epi = epi;
+        g.cfg = cfg;
+        g.ldo = cols;
+        g.m_tiles = (int)((rows + BM2 - 1) / BM2);
+        g.n_tiles = (int)((cols + BN - 1) / BN);
+        g.kb_per_group = (int)((kdim + BK - 1) / BK);
+        g.m_end = (int)rows;
+        g.n_end = (int)cols;
+    };
+    shape(gh, M, Fp, N, EPI_DGELU_BF16, CFG_B_K, 0);
+    shape(gx, M, K, Fp, EPI_F32, CFG_B_K, mode == 1);
+    shape(ga, K, Fp, M, EPI_F32, CFG_A_MN, 0);
+    shape(gb, Fp, N, M, EPI_F32, CFG_A_MN, 0);
+    if ((st = launch_gemm(gh, s0)) || (st = launch_gemm(gx, s0))) return st;
+    if (mode == 0) {
+        // The rank sum of dX, beside the weight-gradient GEMMs when a second stream is given.
+        cudaStream_t rs = s0;
+        if (two_streams) {
+            if (cudaEventRecord(ev->fwd, s0) != cudaSuccess || cudaStreamWaitEvent(s1, ev->fwd, 0) != cudaSuccess)
+                return fail(RTP_ECUDA, "%s: event ordering failed", fn);
+            rs = s1;
+        }
+        if ((st = reduce_partials(P, M, K, dX_partials, dX, rs, two_streams ? kOverlapBlocksPerSm : 4))) return st;
+    }
+    if ((st = launch_gemm(ga, s0)) || (st = launch_gemm(gb, s0))) return st;
+    if (two_streams) {
+        if (cudaEventRecord(ev->back, s1) != cudaSuccess || cudaStreamWaitEvent(s0, ev->back, 0) != cudaSuccess)
+            return fail(RTP_ECUDA, "%s: event ordering failed", fn);
+    }
+    return RTP_OK;
+}
+
 int rtp_tp_mlp_sp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* const* X_shards,
                   const void* const* A_shards, const void* const* B_shards, void* const* Y, float* const* Z_shards,
                   rtp_stream stream_)
@@ -802,6 +1016,7 @@ int rtp_tp_mlp_sp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void*
     g1.n_end = (int)Fp;
     g1.a_rows_per_map = (int)Mr;
     g1.a_maps = P;
+    g1.cfg = CFG_SP_A;
     if ((st = launch_gemm(g1, stream))) return st;
     // row-parallel GEMM: ranks summed in TMEM, rows scattered to their shard
     g2.ldo = N;
@@ -815,6 +1030,7 @@ int rtp_tp_mlp_sp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void*
     g2.n_end = (int)N;
     g2.out_rows_per_ptr = (int)Mr;
     g2.out_ptrs = P;
+    g2.cfg = CFG_SP_OUT;
     return launch_gemm(g2, stream);
 }
 

@@ -408,6 +408,99 @@ def test_tp_mlp_row_subset_matches_full():
     np.testing.assert_array_equal(ys, yf[rows])
 
 
+# ---- TP-MLP backward (ColossalAI page, section 2.2) ---------------------------------
+
+def test_gelu_grad_is_the_derivative_of_gelu():
+    """GELU'(0) = 1/2, the limits 0 and 1, the minimum at -sqrt(2) (where
+    GELU'' = phi(x) (2 - x^2) vanishes), and central differences of GELU."""
+    from scipy.special import ndtr
+    assert oracle.gelu_grad(0.0) == 0.5
+    assert abs(oracle.gelu_grad(9.0) - 1.0) < 1e-15 and abs(oracle.gelu_grad(-9.0)) < 1e-15
+    xm = -np.sqrt(2.0)
+    gm = oracle.gelu_grad(xm)
+    assert gm < oracle.gelu_grad(xm - 1e-3) and gm < oracle.gelu_grad(xm + 1e-3)
+    for x in (-3.1, -0.7, 0.25, 1.0, 2.5):
+        h = 1e-5
+        fd = ((x + h) * ndtr(x + h) - (x - h) * ndtr(x - h)) / (2 * h)
+        assert abs(oracle.gelu_grad(x) - fd) < 1e-9
+        fo = (oracle.gelu(x + h) - oracle.gelu(x - h)) / (2 * h)
+        assert abs(oracle.gelu_grad(x) - fo) < 1e-9
+
+
+def test_tp_mlp_backward_matches_finite_differences():
+    """flags = 0: dX, dA_i, dB_i are the gradient of L = sum(dZ * Z) with
+    Z = GELU(X A) B; checked by central differences of a float64 numpy
+    forward on every input element."""
+    from scipy.special import ndtr
+    M, K, F, N, P = 5, 6, 8, 7, 2
+    X = synth.normal(11, (M, K), "bf16")
+    A = synth.normal(12, (K, F), "bf16", std=0.5)
+    B = synth.normal(13, (F, N), "bf16", std=0.5)
+    dZ = synth.normal(14, (M, N), "bf16")
+    x, a, b, dz = _bf16(X), _bf16(A), _bf16(B), _bf16(dZ)
+
+    def loss(x, a, b):
+        h = x @ a
+        return float(np.sum(dz * ((h * ndtr(h)) @ b)))
+
+    g = oracle.tp_mlp_backward(X, _split_cols(A, P), _split_rows(B, P), dZ, rows=np.arange(M), cols=np.arange(F),
+                               flags=0)
+    eps = 1e-6
+    for name, base, got in (("X", x, g["dX"]), ("A", a, g["dA"].T), ("B", b, g["dB"])):
+        fd = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            args = {"X": x, "A": a, "B": b}
+            up, dn = base.copy(), base.copy()
+            up[idx] += eps
+            dn[idx] -= eps
+            args[name] = up
+            lu = loss(args["X"], args["A"], args["B"])
+            args[name] = dn
+            ld = loss(args["X"], args["A"], args["B"])
+            fd[idx] = (lu - ld) / (2 * eps)
+        np.testing.assert_allclose(got, fd, rtol=1e-6, atol=1e-7, err_msg="d" + name)
+
+
+def test_tp_mlp_backward_independent_of_rank_count():
+    """The gradients of the full A and B do not depend on how many ranks hold
+    their shards, with or without the bf16 roundings (each is elementwise)."""
+    M, K, F, N = 6, 16, 32, 8
+    X = synth.normal(21, (M, K), "bf16")
+    A = synth.normal(22, (K, F), "bf16", std=0.1)
+    B = synth.normal(23, (F, N), "bf16", std=0.1)
+    dZ = synth.normal(24, (M, N), "bf16")
+    for flags in (0, 7):
+        g1 = oracle.tp_mlp_backward(X, [A], [B], dZ, rows=np.arange(M), cols=np.arange(F), flags=flags)
+        g4 = oracle.tp_mlp_backward(X, _split_cols(A, 4), _split_rows(B, 4), dZ, rows=np.arange(M),
+                                    cols=np.arange(F), flags=flags)
+        for k in ("dX", "dH", "dA", "dB"):
+            np.testing.assert_array_equal(g1[k], g4[k], err_msg="%s flags %d" % (k, flags))
+
+
+def test_tp_mlp_backward_row_and_column_paths_agree():
+    """dA and dB come from a per-column pass over all rows; with every rounding
+    on they equal X^T round(dH) and round(GELU(X A))^T dZ formed from the
+    per-row pass (dH, H) and the forward oracle (Y)."""
+    M, K, F, N, P = 7, 8, 16, 8, 2
+    X = synth.normal(31, (M, K), "bf16")
+    A = synth.normal(32, (K, F), "bf16", std=0.3)
+    B = synth.normal(33, (F, N), "bf16", std=0.3)
+    dZ = synth.normal(34, (M, N), "bf16")
+    As, Bs = _split_cols(A, P), _split_rows(B, P)
+    g = oracle.tp_mlp_backward(X, As, Bs, dZ, rows=np.arange(M), cols=np.arange(F), flags=7)
+    dh = torch.from_numpy(g["dH"]).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_allclose(g["dA"], (_bf16(X).T @ dh).T, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(g["dX"], dh @ _bf16(A).T, rtol=1e-12, atol=1e-12)
+    _, y = oracle.tp_mlp(X, As, Bs)
+    np.testing.assert_allclose(g["dB"], y.T @ _bf16(dZ), rtol=1e-12, atol=1e-12)
+    # H is rounded to bf16 with flag 1, and dH = dY * GELU'(H)
+    hb = torch.from_numpy(_bf16(X) @ _bf16(A)).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(g["H"], hb)
+    np.testing.assert_allclose(g["dY"], _bf16(dZ) @ _bf16(B).T, rtol=1e-12, atol=1e-12)
+    gg = np.vectorize(oracle.gelu_grad)(hb)
+    np.testing.assert_allclose(g["dH"], g["dY"] * gg, rtol=1e-12, atol=1e-15)
+
+
 # ---- partial min / max (OneFlow page: min and max also work as partial reductions) ----
 
 def test_partial_min_max_against_numpy():
