@@ -372,7 +372,8 @@ def run_ours(args, rank, world, local_rank):
                                "dX_sum": "fused in the GEMM",
                                "ms_separate_dX_sum_overlapped": round(bwo_ms, 4),
                                "train_forward_ms": round(tf_ms, 4),
-                               "train_forward_tflops": round(MLP_FLOPS / (tf_ms * 1e-3) / 1e12, 1)},
+                               "train_forward_tflops": round(MLP_FLOPS / (tf_ms * 1e-3) / 1e12, 1),
+                               "traffic": _traffic("tp_gemm_kernel", "mlp_backward")},
     }
     reshard_ms = max_over_ranks(reshard_ms)
     mlp_ms = max_over_ranks(mlp_ms)
@@ -611,6 +612,7 @@ PROFILE_CASES = {
     "sweep": ("sweep", None),
     "mlp_fused": ("mlp", MLP),
     "domino_fused": ("mlp", DOMINO),
+    "mlp_backward": ("mlp_backward", MLP),
 }
 
 
@@ -666,10 +668,20 @@ def run_profile_case(name: str, repeats: int = 2):
         Y = [torch.empty((M, F // P), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
         Z = torch.empty((M, N), dtype=torch.float32, device="cuda")
         torch.cuda.synchronize()
-        for _ in range(repeats):
-            rtp.tp_mlp(X, A, B, Y=Y, Z=Z, mode=1)
-        torch.cuda.synchronize()
-        print(json.dumps({"case": name, "flops_gemm1": 2 * M * K * F, "flops_gemm2": 2 * M * F * N}))
+        if kind == "mlp_backward":
+            # training forward (2 launches) then backward (4 launches: dH, dX, dA, dB) per repeat
+            dZ = torch.randn((M, N), generator=gen, device="cuda").bfloat16()
+            for _ in range(repeats):
+                _, Yt, H = rtp.tp_mlp_train_forward(X, A, B, Y=Y, Z=Z)
+                rtp.tp_mlp_backward(X, A, B, H, Yt, dZ, mode=1)
+            torch.cuda.synchronize()
+            print(json.dumps({"case": name, "flops_per_gemm": [2 * M * K * F, 2 * M * F * N, 2 * M * N * F,
+                                                               2 * M * F * K, 2 * K * M * F, 2 * F * M * N]}))
+        else:
+            for _ in range(repeats):
+                rtp.tp_mlp(X, A, B, Y=Y, Z=Z, mode=1)
+            torch.cuda.synchronize()
+            print(json.dumps({"case": name, "flops_gemm1": 2 * M * K * F, "flops_gemm2": 2 * M * F * N}))
     assert rtp.device_error() == 0
 
 
