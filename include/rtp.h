@@ -369,9 +369,24 @@ int rtp_tp_mlp_noalloc(int P, int64_t M, int64_t K, int64_t F, int64_t N, const 
  * Synchronises `stream`. *code == 0: no such event since the last check;
  * otherwise the results of the launches since then are invalid
  * (1 producer, 2 MMA waiting for operands, 3 MMA waiting for an accumulator,
- * 4 epilogue).
+ * 4 epilogue, 5 rtp_wait_selftest).
  */
 int rtp_device_error(rtp_stream stream, uint32_t* code);
+
+/*
+ * Self-test of the bounded waits that rtp_tp_mlp's kernels use (no page
+ * counterpart: it checks this library's failure detection without a fault).
+ * One block, two waiting threads, one mbarrier that nothing completes: the
+ * first waiter gives up after limit_ns of %globaltimer, records code 5 in the
+ * device word that rtp_device_error reads and raises the block's abort flag;
+ * the second waiter (own limit 4 x limit_ns) leaves on that flag. The kernel
+ * then returns normally and the context stays usable.
+ *   limit_ns  in [1e6, 1e9] (1 ms to 1 s), else RTP_EINVAL
+ *   out       device pointer to 2 uint32 (16-byte aligned, caller-owned):
+ *             out[w] = 1 when waiter w gave up (both, when the test works)
+ * Asynchronous on `stream`.
+ */
+int rtp_wait_selftest(unsigned long long limit_ns, uint32_t* out, rtp_stream stream);
 
 /* Text of the last error on the calling thread ("" if none). */
 const char* rtp_last_error(void);

@@ -59,21 +59,27 @@ namespace {
 
 constexpr int BN = 256, BK = 64;
 constexpr uint32_t B_SUB = 64 * BK * 2;  // one 64(N) x 64(K) box, 8 KB
-constexpr int THREADS = 192;
+// Warps: 0 TMA producer, 1 MMA issuer, then EPI_WARPS epilogue warps. An
+// epilogue warp reaches the TMEM lane quarter (warp % 4); with 8 of them, two
+// warps share each quarter and take half of the tile's columns each.
+constexpr int EPI_WARPS = 4;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int EPI_CHUNKS = BN / 32 / (EPI_WARPS / 4);  // 32-column chunks per epilogue warp
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int GROUP_M = 16;
 constexpr int kOverlapBlocksPerSm = 1;  // reduction blocks per SM while a GEMM runs beside it
 constexpr int MAX_GROUPS = 8;
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;
 
-enum : uint32_t { ERR_PRODUCER = 1, ERR_MMA_STAGE = 2, ERR_MMA_ACC = 3, ERR_EPILOGUE = 4 };
+enum : uint32_t { ERR_PRODUCER = 1, ERR_MMA_STAGE = 2, ERR_MMA_ACC = 3, ERR_EPILOGUE = 4, ERR_SELFTEST = 5 };
 enum { EPI_GELU_BF16 = 0, EPI_F32 = 1, EPI_DGELU_BF16 = 2 };
 // Kernel configuration (a compile-time template parameter):
 //   CFG_SP_A    rows of the A operand come from per-shard maps (sequence parallel)
 //   CFG_SP_OUT  output rows go to per-shard buffers (sequence parallel)
 //   CFG_A_MN    A is M-major in memory (a transposed operand: X^T, Y^T)
 //   CFG_B_K     B is K-major in memory (a transposed operand: A_i^T, B_i^T)
-enum : int { CFG_SP_A = 1, CFG_SP_OUT = 2, CFG_A_MN = 4, CFG_B_K = 8 };
+//   bits 4-5    the epilogue (EPI_*)
+enum : int { CFG_SP_A = 1, CFG_SP_OUT = 2, CFG_A_MN = 4, CFG_B_K = 8, CFG_EPI_SHIFT = 4 };
 
 
 struct GemmArgs {
@@ -95,7 +101,7 @@ struct GemmArgs {
     // reduce-scatter fused into the epilogue of the rank-summing GEMM).
     int32_t a_rows_per_map, a_maps;
     int32_t out_rows_per_ptr, out_ptrs;
-    int32_t cfg;                 // kernel configuration (CFG_* bits), chosen by the host
+    int32_t cfg;                 // kernel configuration (CFG_* operand bits), chosen by the host
 };
 
 __device__ unsigned int g_tp_error;
@@ -135,14 +141,15 @@ __device__ __forceinline__ uint64_t global_ns()
 }
 
 // Slow path of wait_bar, kept out of line.
-__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, uint32_t code)
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, uint32_t code,
+                                           unsigned long long limit_ns)
 {
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (*abort_flag) return false;
-            if (global_ns() - t0 > WAIT_LIMIT_NS) {
+            if (global_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicCAS(&g_tp_error, 0u, code);
                 return false;
@@ -152,10 +159,35 @@ __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volati
 }
 
 // Bounded wait. False: this wait gave up, or another role already did.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, uint32_t code)
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, uint32_t code,
+                                         unsigned long long limit_ns = WAIT_LIMIT_NS)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    return wait_bar_slow(bar, parity, abort_flag, code);
+    return wait_bar_slow(bar, parity, abort_flag, code, limit_ns);
+}
+
+// Self-test of the bounded wait: two threads wait on an mbarrier that nothing
+// completes. The first gives up after limit_ns, records ERR_SELFTEST and raises
+// the abort flag; the second leaves on the flag. out[w] = 1 if waiter w gave up.
+// The mbarrier is never armed or awaited again, so nothing is left in flight.
+__global__ void wait_selftest_kernel(unsigned long long limit_ns, uint32_t* out)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t abort_word;
+    volatile uint32_t* abort_flag = &abort_word;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        // waiter 1's own limit is 4x longer: it should leave on waiter 0's abort
+        // flag, so the kernel lasts about limit_ns (4 limit_ns at most)
+        const bool ok = wait_bar(smem_u32(&bar), 0, abort_flag, ERR_SELFTEST, w == 0 ? limit_ns : 4 * limit_ns);
+        out[w] = ok ? 0u : 1u;
+    }
 }
 
 // Bounded wait used only while tearing down after an abort: it ignores the
@@ -325,6 +357,7 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
 {
     constexpr bool SP_A = (CFG & CFG_SP_A) != 0, SP_OUT = (CFG & CFG_SP_OUT) != 0;
     constexpr bool A_MN = (CFG & CFG_A_MN) != 0, B_K = (CFG & CFG_B_K) != 0;
+    constexpr int EPI = (CFG >> CFG_EPI_SHIFT) & 3;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES2 * STAGE2_BYTES);
@@ -347,7 +380,7 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(acc_full(x), 1);
-            mbar_init(acc_empty(x), 8);  // 4 epilogue warps in each CTA of the pair
+            mbar_init(acc_empty(x), 2 * EPI_WARPS);  // every epilogue warp of both CTAs
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -503,6 +536,7 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
     } else {
         // ---------------- epilogue (both CTAs) ----------------
         const int quarter = warp & 3;
+        const int c_begin = ((warp - 2) >> 2) * EPI_CHUNKS;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = pair; tile < a.total_tiles; tile += npairs) {
@@ -524,60 +558,84 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
                 orow = row - (int64_t)sh * a.out_rows_per_ptr;
             }
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32cols(taddr + 32u * c, r);
-                tmem_ld_wait();
-                const int64_t c0 = col + 32 * c;
-                if (!row_ok || c0 >= a.n_end) continue;
-                if (a.epi == EPI_GELU_BF16) {
+            if constexpr (EPI == EPI_DGELU_BF16) {
+                // dH = dY * GELU'(H): the accumulator is dY, H is read at the same
+                // place; the next chunk's H is loaded while this chunk is computed
+                const __nv_bfloat16* hrow = static_cast<const __nv_bfloat16*>(a.aux[g]) + orow * a.ldo;
+                auto load_h = [&](int c, uint4 (&h)[4]) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int64_t cq = col + 32 * c + 8 * q;
+                        h[q] = (row_ok && cq < a.n_end) ? __ldg(reinterpret_cast<const uint4*>(hrow + cq))
+                                                         : make_uint4(0u, 0u, 0u, 0u);
+                    }
+                };
+                uint4 hn[4];
+                load_h(c_begin, hn);
+                for (int c = c_begin; c < c_begin + EPI_CHUNKS; ++c) {
+                    uint4 h[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) h[q] = hn[q];
+                    if (c + 1 < c_begin + EPI_CHUNKS) load_h(c + 1, hn);
+                    uint32_t r[32];
+                    tmem_ld_32cols(taddr + 32u * c, r);
+                    tmem_ld_wait();
+                    const int64_t c0 = col + 32 * c;
+                    if (!row_ok || c0 >= a.n_end) continue;
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_base) + orow * a.ldo + c0);
-                    uint4* hdst = a.out2[g] ? reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out2[g]) + orow * a.ldo + c0)
-                                            : nullptr;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         if (c0 + 8 * q >= a.n_end) break;
                         uint4 v;
-                        v.x = pack_bf16(gelu(__uint_as_float(r[8 * q + 0])), gelu(__uint_as_float(r[8 * q + 1])));
-                        v.y = pack_bf16(gelu(__uint_as_float(r[8 * q + 2])), gelu(__uint_as_float(r[8 * q + 3])));
-                        v.z = pack_bf16(gelu(__uint_as_float(r[8 * q + 4])), gelu(__uint_as_float(r[8 * q + 5])));
-                        v.w = pack_bf16(gelu(__uint_as_float(r[8 * q + 6])), gelu(__uint_as_float(r[8 * q + 7])));
+                        v.x = pack_bf16(__uint_as_float(r[8 * q + 0]) * gelu_grad(bf16_lo(h[q].x)),
+                                        __uint_as_float(r[8 * q + 1]) * gelu_grad(bf16_hi(h[q].x)));
+                        v.y = pack_bf16(__uint_as_float(r[8 * q + 2]) * gelu_grad(bf16_lo(h[q].y)),
+                                        __uint_as_float(r[8 * q + 3]) * gelu_grad(bf16_hi(h[q].y)));
+                        v.z = pack_bf16(__uint_as_float(r[8 * q + 4]) * gelu_grad(bf16_lo(h[q].z)),
+                                        __uint_as_float(r[8 * q + 5]) * gelu_grad(bf16_hi(h[q].z)));
+                        v.w = pack_bf16(__uint_as_float(r[8 * q + 6]) * gelu_grad(bf16_lo(h[q].w)),
+                                        __uint_as_float(r[8 * q + 7]) * gelu_grad(bf16_hi(h[q].w)));
                         __stcs(dst + q, v);
-                        if (hdst) {  // the pre-activation, for the backward pass
-                            uint4 h;
-                            h.x = pack_bf16(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]));
-                            h.y = pack_bf16(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]));
-                            h.z = pack_bf16(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]));
-                            h.w = pack_bf16(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]));
-                            __stcs(hdst + q, h);
+                    }
+                }
+            } else {
+                for (int c = c_begin; c < c_begin + EPI_CHUNKS; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32cols(taddr + 32u * c, r);
+                    tmem_ld_wait();
+                    const int64_t c0 = col + 32 * c;
+                    if (!row_ok || c0 >= a.n_end) continue;
+                    if constexpr (EPI == EPI_GELU_BF16) {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_base) + orow * a.ldo + c0);
+                        uint4* hdst = a.out2[g] ? reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out2[g]) +
+                                                                           orow * a.ldo + c0)
+                                                : nullptr;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            if (c0 + 8 * q >= a.n_end) break;
+                            uint4 v;
+                            v.x = pack_bf16(gelu(__uint_as_float(r[8 * q + 0])), gelu(__uint_as_float(r[8 * q + 1])));
+                            v.y = pack_bf16(gelu(__uint_as_float(r[8 * q + 2])), gelu(__uint_as_float(r[8 * q + 3])));
+                            v.z = pack_bf16(gelu(__uint_as_float(r[8 * q + 4])), gelu(__uint_as_float(r[8 * q + 5])));
+                            v.w = pack_bf16(gelu(__uint_as_float(r[8 * q + 6])), gelu(__uint_as_float(r[8 * q + 7])));
+                            __stcs(dst + q, v);
+                            if (hdst) {  // the pre-activation, for the backward pass
+                                uint4 h;
+                                h.x = pack_bf16(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]));
+                                h.y = pack_bf16(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]));
+                                h.z = pack_bf16(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]));
+                                h.w = pack_bf16(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]));
+                                __stcs(hdst + q, h);
+                            }
                         }
-                    }
-                } else if (a.epi == EPI_DGELU_BF16) {
-                    // dH = dY * GELU'(H): the accumulator is dY, H is read at the same place
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_base) + orow * a.ldo + c0);
-                    const uint4* hsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.aux[g]) + orow * a.ldo + c0);
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_base) + orow * a.ldo + c0);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (c0 + 8 * q >= a.n_end) break;
-                        const uint4 h = __ldcs(hsrc + q);
-                        uint4 v;
-                        v.x = pack_bf16(__uint_as_float(r[8 * q + 0]) * gelu_grad(bf16_lo(h.x)),
-                                        __uint_as_float(r[8 * q + 1]) * gelu_grad(bf16_hi(h.x)));
-                        v.y = pack_bf16(__uint_as_float(r[8 * q + 2]) * gelu_grad(bf16_lo(h.y)),
-                                        __uint_as_float(r[8 * q + 3]) * gelu_grad(bf16_hi(h.y)));
-                        v.z = pack_bf16(__uint_as_float(r[8 * q + 4]) * gelu_grad(bf16_lo(h.z)),
-                                        __uint_as_float(r[8 * q + 5]) * gelu_grad(bf16_hi(h.z)));
-                        v.w = pack_bf16(__uint_as_float(r[8 * q + 6]) * gelu_grad(bf16_lo(h.w)),
-                                        __uint_as_float(r[8 * q + 7]) * gelu_grad(bf16_hi(h.w)));
-                        __stcs(dst + q, v);
-                    }
-                } else {
-                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_base) + orow * a.ldo + c0);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        if (c0 + 4 * q >= a.n_end) break;
-                        __stcs(dst + q, make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
-                                                    __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
+                        for (int q = 0; q < 8; ++q) {
+                            if (c0 + 4 * q >= a.n_end) break;
+                            __stcs(dst + q, make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
+                                                        __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
+                        }
                     }
                 }
             }
@@ -669,13 +727,18 @@ int launch_gemm_t(GemmArgs& args, cudaStream_t stream)
 
 int launch_gemm(GemmArgs& args, cudaStream_t stream)
 {
-    switch (args.cfg) {
-    case 0: return launch_gemm_t<0>(args, stream);
-    case CFG_SP_A: return launch_gemm_t<CFG_SP_A>(args, stream);
-    case CFG_SP_OUT: return launch_gemm_t<CFG_SP_OUT>(args, stream);
-    case CFG_A_MN: return launch_gemm_t<CFG_A_MN>(args, stream);
-    case CFG_B_K: return launch_gemm_t<CFG_B_K>(args, stream);
-    default: return fail(RTP_EUNSUPPORTED, "tp_mlp: no GEMM kernel for configuration %d", args.cfg);
+    constexpr int GELU = EPI_GELU_BF16 << CFG_EPI_SHIFT, F32 = EPI_F32 << CFG_EPI_SHIFT,
+                  DGELU = EPI_DGELU_BF16 << CFG_EPI_SHIFT;
+    switch (args.cfg | (args.epi << CFG_EPI_SHIFT)) {
+    case GELU: return launch_gemm_t<GELU>(args, stream);
+    case F32: return launch_gemm_t<F32>(args, stream);
+    case CFG_SP_A | GELU: return launch_gemm_t<CFG_SP_A | GELU>(args, stream);
+    case CFG_SP_OUT | F32: return launch_gemm_t<CFG_SP_OUT | F32>(args, stream);
+    case CFG_A_MN | F32: return launch_gemm_t<CFG_A_MN | F32>(args, stream);
+    case CFG_B_K | DGELU: return launch_gemm_t<CFG_B_K | DGELU>(args, stream);
+    case CFG_B_K | F32: return launch_gemm_t<CFG_B_K | F32>(args, stream);
+    default:
+        return fail(RTP_EUNSUPPORTED, "tp_mlp: no GEMM kernel for configuration %d, epilogue %d", args.cfg, args.epi);
     }
 }
 
@@ -1032,6 +1095,18 @@ int rtp_tp_mlp_sp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void*
     g2.out_ptrs = P;
     g2.cfg = CFG_SP_OUT;
     return launch_gemm(g2, stream);
+}
+
+int rtp_wait_selftest(unsigned long long limit_ns, uint32_t* out, rtp_stream stream)
+{
+    if (!out) return fail(RTP_EINVAL, "rtp_wait_selftest: NULL out");
+    if (limit_ns < 1000000ull || limit_ns > 1000000000ull)
+        return fail(RTP_EINVAL, "rtp_wait_selftest: limit %llu ns outside [1 ms, 1 s]", limit_ns);
+    if (!aligned16(out)) return fail(RTP_EINVAL, "rtp_wait_selftest: out must be 16-byte aligned");
+    wait_selftest_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns, out);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(RTP_ECUDA, "rtp_wait_selftest: launch failed: %s", cudaGetErrorString(e));
+    return RTP_OK;
 }
 
 int rtp_device_error(rtp_stream stream, uint32_t* code)

@@ -56,6 +56,11 @@ def test_version_and_errors():
         rtp.infer_spmd("mk,kn->mz", [[0, -1], [-1, -1]], 1)
     with pytest.raises(rtp.RtpError):
         rtp.infer_reshape([2, 3], [0, -1], [7], [2])
+    # the wait self-test checks its limit on the host, before any launch
+    lib = rtp.lib()
+    for bad in (0, 999_999, 1_000_000_001):
+        assert lib.rtp_wait_selftest(bad, 16, None) == -1
+    assert lib.rtp_wait_selftest(5_000_000, None, None) == -1
 
 
 def _same_layout(spec, lay, shape):
