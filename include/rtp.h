@@ -246,6 +246,36 @@ int rtp_infer_reshape(int in_ndim, const int64_t* in_shape, const int32_t* in_di
                       int32_t* out_dims_mapping);
 
 /*
+ * Sharding checker and output inference for broadcast n-ary element-wise
+ * operators (Add, Mul, Sub, Where, ...): "ONNX multi-device proposal", sections
+ * on the validity check and on operator groups. A device computes the output
+ * elements whose inputs it holds; with broadcast axes a shard's devices are the
+ * intersection of the devices of the input shards it reads (the page's
+ * Add([M,1],[1,N]) example: output shard [i,j] lives where input-1 shard i and
+ * input-2 shard j both are). Host only.
+ *   in_ndims[k], in_shapes[k]  input k's rank and shape (extents >= 1); shapes
+ *                              broadcast with trailing dims aligned (else
+ *                              RTP_ESHAPE)
+ *   in_specs[k]                input k's layout; all on the same number of
+ *                              ranks, no partial mesh dims (RTP_EUNSUPPORTED:
+ *                              the ONNX rules have no partial layouts)
+ *   out_ndim, out_shape        the broadcast output shape (out_shape holds
+ *                              RTP_MAX_NDIM entries)
+ *   out_spec                   the output layout: an input's own spec when its
+ *                              pieces are exactly the computable boxes, else
+ *                              split mesh dims for the cut output axes (in axis
+ *                              order, outer first) and one broadcast mesh dim for
+ *                              replicas, ranks in ascending order within a piece
+ * RTP_ECONFLICT: some output element has no rank holding all of its inputs
+ * (e.g. one input split on axis 0 and the other on axis 1). RTP_EUNSUPPORTED:
+ * the computable pieces are not a layout (overlapping, not a grid, held by
+ * unequal numbers of ranks, a rank with nothing, or cuts other than the even
+ * split).
+ */
+int rtp_infer_broadcast(int n_in, const int32_t* in_ndims, const int64_t* const* in_shapes, const rtp_spec* in_specs,
+                        int* out_ndim, int64_t* out_shape, rtp_spec* out_spec);
+
+/*
  * tp_mlp(X, A_shards, B_shards): the Megatron 1D tensor-parallel MLP on P
  * virtual ranks (ColossalAI "1D tensor parallelism" page, sections 2 and 2.1:
  * column-parallel Y_i = X A_i, row-parallel Z = sum_i Y_i B_i; GELU between

@@ -138,7 +138,9 @@ def _load():
     lib.oracle_tp_mlp_backward.argtypes = ([ctypes.c_int64] * 5 + [P(ctypes.c_uint16), vpp, vpp, P(ctypes.c_uint16),
                                            ctypes.c_int, ctypes.c_int64, i64p, dblp, dblp, dblp, dblp,
                                            ctypes.c_int64, i64p, dblp, dblp])
-    for f in ("oracle_shard_box", "oracle_shard", "oracle_gather", "oracle_reshard",
+    lib.oracle_infer_broadcast.argtypes = [ctypes.c_int, i32p, P(i64p), P(_Layout), P(ctypes.c_int), i64p, i64p, i64p,
+                                           P(_Layout), P(ctypes.c_int)]
+    for f in ("oracle_infer_broadcast", "oracle_shard_box", "oracle_shard", "oracle_gather", "oracle_reshard",
               "oracle_layout_from_dims_mapping", "oracle_layout_from_onnx", "oracle_infer_spmd",
               "oracle_reshape_spmd", "oracle_tp_mlp", "oracle_tp_mlp_backward"):
         getattr(lib, f).restype = ctypes.c_int
@@ -209,6 +211,31 @@ def shard_box(shape: Sequence[int], layout: Layout, device: int):
     L = layout._c()
     _ok(_load().oracle_shard_box(nd, _i64(shape), ctypes.byref(L), device, lo, hi, ctypes.byref(hv)), "shard_box")
     return tuple(lo[a] for a in range(nd)), tuple(hi[a] for a in range(nd)), bool(hv.value)
+
+
+def infer_broadcast(shapes: Sequence[Sequence[int]], layouts: Sequence[Layout]):
+    """ONNX broadcast n-ary element-wise rule, per element. Returns
+    (status, out_shape, boxes, layout): status 0 = a layout (boxes[dev] =
+    (lo, hi) of the output each device computes), 1 = some output element has
+    no device, 2 = the pieces are not a layout."""
+    n = len(shapes)
+    nds = (ctypes.c_int32 * n)(*[len(sh) for sh in shapes])
+    arrs = [_i64(sh) for sh in shapes]
+    shp = (ctypes.POINTER(ctypes.c_int64) * n)(*[ctypes.cast(a, ctypes.POINTER(ctypes.c_int64)) for a in arrs])
+    Ls = (_Layout * n)(*[L._c() for L in layouts])
+    ndev = layouts[0].num_devices
+    out_nd, st = ctypes.c_int(), ctypes.c_int()
+    oshape = _i64([0] * 8)
+    lo, hi = _i64([0] * (8 * ndev)), _i64([0] * (8 * ndev))
+    outL = _Layout()
+    _ok(_load().oracle_infer_broadcast(n, nds, shp, Ls, ctypes.byref(out_nd), oshape, lo, hi, ctypes.byref(outL),
+                                       ctypes.byref(st)), "infer_broadcast")
+    nd = out_nd.value
+    shape = tuple(oshape[d] for d in range(nd))
+    if st.value != 0:
+        return st.value, shape, None, None
+    boxes = [(tuple(lo[v * 8 + d] for d in range(nd)), tuple(hi[v * 8 + d] for d in range(nd))) for v in range(ndev)]
+    return 0, shape, boxes, Layout._from_c(outL)
 
 
 def shard_shape(shape: Sequence[int], layout: Layout, device: int) -> Tuple[int, ...]:

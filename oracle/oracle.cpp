@@ -710,6 +710,225 @@ int oracle_infer_sbp_signature(int n_in, int ndim, const int64_t* shape, int ele
     return 0;
 }
 
+// ---- ONNX broadcast n-ary element-wise rule -----------------------------------
+
+// "ONNX multi-device proposal", operator groups: for a broadcast n-ary
+// element-wise operator a device computes the output elements whose inputs it
+// all holds; a shard's devices are the intersection of the devices of the input
+// shards it reads (the Add([M,1],[1,N]) example). Done per element here.
+// Inputs: n_in tensors (shapes right-aligned for broadcasting) on the same
+// n_dev devices. Result: *status = 0 and, per device, the box [lo, hi) of the
+// output it computes (out_lo/out_hi[dev * kMaxDim + axis]; empty = lo == hi on
+// some axis), plus a layout that yields those boxes; *status = 1 when some
+// output element has no device; *status = 2 when the boxes are not a layout
+// (two devices' boxes overlap without being equal, they do not form a grid,
+// the grid cells have unequal numbers of devices, or the cuts are not the even
+// split). An input whose own layout already gives exactly the boxes is
+// returned as the layout.
+int oracle_infer_broadcast(int n_in, const int32_t* in_ndims, const int64_t* const* in_shapes,
+                           const OracleLayout* in_layouts, int* out_ndim, int64_t* out_shape, int64_t* out_lo,
+                           int64_t* out_hi, OracleLayout* out_layout, int* status)
+{
+    if (n_in < 1) return -1;
+    int nd = 0;
+    for (int k = 0; k < n_in; ++k) {
+        if (in_ndims[k] < 1 || in_ndims[k] > kMaxDim) return -1;
+        if (check_layout(in_layouts[k], in_ndims[k])) return -1;
+        for (int d = 0; d < in_layouts[k].mesh_ndim; ++d)
+            if (is_partial_kind(in_layouts[k].kind[d])) return -1;
+        nd = std::max(nd, (int)in_ndims[k]);
+    }
+    const int64_t n_dev = num_devices(in_layouts[0]);
+    for (int k = 1; k < n_in; ++k)
+        if (num_devices(in_layouts[k]) != n_dev) return -1;
+    int64_t shape[kMaxDim];
+    for (int d = 0; d < nd; ++d) {
+        int64_t e = 1;
+        for (int k = 0; k < n_in; ++k) {
+            int dk = d - (nd - in_ndims[k]);
+            if (dk < 0) continue;
+            int64_t x = in_shapes[k][dk];
+            if (x < 1) return -1;  // empty tensors are not handled by this rule
+            if (x == 1) continue;
+            if (e != 1 && e != x) return -1;
+            e = x;
+        }
+        shape[d] = e;
+    }
+    int64_t total = 1;
+    for (int d = 0; d < nd; ++d) total *= shape[d];
+    // input pieces of every device
+    std::vector<int64_t> plo((size_t)n_in * n_dev * kMaxDim), phi((size_t)n_in * n_dev * kMaxDim);
+    for (int k = 0; k < n_in; ++k)
+        for (int64_t dev = 0; dev < n_dev; ++dev) {
+            int64_t c[kMaxMesh];
+            if (!coords_of(in_layouts[k], (int)dev, c)) return -1;
+            slice_of(in_layouts[k], in_ndims[k], in_shapes[k], c, &plo[(k * n_dev + dev) * kMaxDim],
+                     &phi[(k * n_dev + dev) * kMaxDim]);
+        }
+    // per device: which output elements it can compute (bounding box + count)
+    std::vector<int64_t> lo((size_t)n_dev * kMaxDim), hi((size_t)n_dev * kMaxDim), count((size_t)n_dev, 0);
+    std::vector<int> covered((size_t)total, 0);
+    for (int64_t dev = 0; dev < n_dev; ++dev) {
+        for (int d = 0; d < nd; ++d) {
+            lo[dev * kMaxDim + d] = shape[d];
+            hi[dev * kMaxDim + d] = 0;
+        }
+        int64_t e[kMaxDim];
+        for (int64_t flat = 0; flat < total; ++flat) {
+            int64_t rem = flat;
+            for (int d = nd - 1; d >= 0; --d) {
+                e[d] = rem % shape[d];
+                rem /= shape[d];
+            }
+            bool ok = true;
+            for (int k = 0; k < n_in && ok; ++k)
+                for (int dk = 0; dk < in_ndims[k] && ok; ++dk) {
+                    int d = dk + (nd - in_ndims[k]);
+                    int64_t i = in_shapes[k][dk] == 1 ? 0 : e[d];  // a broadcast axis reads element 0
+                    const int64_t* L = &plo[(k * n_dev + dev) * kMaxDim];
+                    const int64_t* H = &phi[(k * n_dev + dev) * kMaxDim];
+                    if (i < L[dk] || i >= H[dk]) ok = false;
+                }
+            if (!ok) continue;
+            ++count[dev];
+            ++covered[flat];
+            for (int d = 0; d < nd; ++d) {
+                lo[dev * kMaxDim + d] = std::min(lo[dev * kMaxDim + d], e[d]);
+                hi[dev * kMaxDim + d] = std::max(hi[dev * kMaxDim + d], e[d] + 1);
+            }
+        }
+        if (count[dev] == 0)
+            for (int d = 0; d < nd; ++d) lo[dev * kMaxDim + d] = hi[dev * kMaxDim + d] = 0;
+        int64_t vol = 1;
+        for (int d = 0; d < nd; ++d) vol *= hi[dev * kMaxDim + d] - lo[dev * kMaxDim + d];
+        if (count[dev] > 0 && vol != count[dev]) return -1;  // cannot happen: intersections of boxes are boxes
+    }
+    *out_ndim = nd;
+    for (int d = 0; d < nd; ++d) out_shape[d] = shape[d];
+    for (int64_t i = 0; i < n_dev * kMaxDim; ++i) {
+        out_lo[i] = lo[i];
+        out_hi[i] = hi[i];
+    }
+    auto same_box = [&](int64_t a, int64_t b) {
+        for (int d = 0; d < nd; ++d)
+            if (lo[a * kMaxDim + d] != lo[b * kMaxDim + d] || hi[a * kMaxDim + d] != hi[b * kMaxDim + d]) return false;
+        return true;
+    };
+    // an input whose own pieces are these boxes
+    for (int k = 0; k < n_in; ++k) {
+        if (in_ndims[k] != nd) continue;
+        bool full = true;
+        for (int d = 0; d < nd; ++d) full &= in_shapes[k][d] == shape[d];
+        if (!full) continue;
+        bool match = true;
+        for (int64_t dev = 0; dev < n_dev && match; ++dev) {
+            const int64_t* L = &plo[(k * n_dev + dev) * kMaxDim];
+            const int64_t* H = &phi[(k * n_dev + dev) * kMaxDim];
+            int64_t vol = 1;
+            for (int d = 0; d < nd; ++d) vol *= H[d] - L[d];
+            if (vol != count[dev]) match = false;
+            for (int d = 0; d < nd && match && count[dev] > 0; ++d)
+                if (L[d] != lo[dev * kMaxDim + d] || H[d] != hi[dev * kMaxDim + d]) match = false;
+        }
+        if (match) {
+            *out_layout = in_layouts[k];
+            *status = 0;
+            return 0;
+        }
+    }
+    // overlapping boxes that differ
+    for (int64_t a = 0; a < n_dev; ++a)
+        for (int64_t b = a + 1; b < n_dev; ++b) {
+            if (!count[a] || !count[b] || same_box(a, b)) continue;
+            bool meet = true;
+            for (int d = 0; d < nd; ++d)
+                meet &= std::max(lo[a * kMaxDim + d], lo[b * kMaxDim + d]) <
+                        std::min(hi[a * kMaxDim + d], hi[b * kMaxDim + d]);
+            if (meet) {
+                *status = 2;
+                return 0;
+            }
+        }
+    for (int64_t f = 0; f < total; ++f)
+        if (!covered[f]) {
+            *status = 1;
+            return 0;
+        }
+    // a grid of cells, each on the same number of devices
+    std::vector<std::vector<std::pair<int64_t, int64_t>>> cuts((size_t)nd);
+    for (int d = 0; d < nd; ++d) {
+        for (int64_t dev = 0; dev < n_dev; ++dev)
+            if (count[dev]) cuts[d].push_back({lo[dev * kMaxDim + d], hi[dev * kMaxDim + d]});
+        std::sort(cuts[d].begin(), cuts[d].end());
+        cuts[d].erase(std::unique(cuts[d].begin(), cuts[d].end()), cuts[d].end());
+    }
+    int64_t cells = 1;
+    for (int d = 0; d < nd; ++d) cells *= (int64_t)cuts[d].size();
+    std::vector<std::vector<int>> holders((size_t)std::max<int64_t>(cells, 1));
+    int64_t distinct = 0;
+    for (int64_t dev = 0; dev < n_dev; ++dev) {
+        if (!count[dev]) {
+            *status = 2;  // a device with nothing to compute
+            return 0;
+        }
+        bool first = true;
+        for (int64_t o = 0; o < dev; ++o)
+            if (count[o] && same_box(o, dev)) first = false;
+        distinct += first ? 1 : 0;
+        int64_t cell = 0;
+        for (int d = 0; d < nd; ++d) {
+            int64_t i = std::find(cuts[d].begin(), cuts[d].end(),
+                                  std::make_pair(lo[dev * kMaxDim + d], hi[dev * kMaxDim + d])) - cuts[d].begin();
+            cell = cell * (int64_t)cuts[d].size() + i;
+        }
+        holders[cell].push_back((int)dev);
+    }
+    if (distinct != cells) {
+        *status = 2;
+        return 0;
+    }
+    size_t rep = holders[0].size();
+    for (auto& h : holders)
+        if (h.size() != rep) {
+            *status = 2;
+            return 0;
+        }
+    OracleLayout L;
+    std::memset(&L, 0, sizeof L);
+    for (int d = 0; d < nd; ++d) {
+        if (cuts[d].size() <= 1) continue;
+        if (L.mesh_ndim == kMaxMesh) return -1;
+        L.mesh_shape[L.mesh_ndim] = (int64_t)cuts[d].size();
+        L.kind[L.mesh_ndim] = 'S';
+        L.axis[L.mesh_ndim] = d;
+        ++L.mesh_ndim;
+    }
+    if (rep > 1 || L.mesh_ndim == 0) {
+        L.mesh_shape[L.mesh_ndim] = (int64_t)rep;
+        L.kind[L.mesh_ndim] = 'B';
+        ++L.mesh_ndim;
+    }
+    for (int64_t c = 0; c < cells; ++c) {
+        std::vector<int> h = holders[c];
+        std::sort(h.begin(), h.end());
+        for (size_t t = 0; t < rep; ++t) L.devices[c * rep + t] = h[t];
+    }
+    for (int64_t dev = 0; dev < n_dev; ++dev) {
+        int64_t c[kMaxMesh], l2[kMaxDim], h2[kMaxDim];
+        coords_of(L, (int)dev, c);
+        slice_of(L, nd, shape, c, l2, h2);
+        for (int d = 0; d < nd; ++d)
+            if (l2[d] != lo[dev * kMaxDim + d] || h2[d] != hi[dev * kMaxDim + d]) {
+                *status = 2;  // not the even split
+                return 0;
+            }
+    }
+    *out_layout = L;
+    *status = 0;
+    return 0;
+}
+
 // ---- scalar helpers exposed for pins -----------------------------------------
 
 uint16_t oracle_bf16_round(double x) { return double_to_bf16_bits(x); }

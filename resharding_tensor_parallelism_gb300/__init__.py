@@ -94,6 +94,7 @@ def _load():
         "rtp_infer_reshape": [c_int, i64p, i32p, c_int, i64p, c_int, i64p, i32p, i32p],
         "rtp_infer_sbp_signature": [c_int, c_int, i64p, c_int, c_int, i32p, i32p, i32p, i32p, i32p, i32p,
                                     P(ctypes.c_double), i32p],
+        "rtp_infer_broadcast": [c_int, i32p, P(i64p), P(Spec), P(c_int), i64p, P(Spec)],
         "rtp_device_error": [vp, u32p],
         "rtp_wait_selftest": [ctypes.c_ulonglong, vp, vp],
         "rtp_tp_mlp_sp": [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vpp, vpp, vpp, vpp,
@@ -350,6 +351,20 @@ def infer_sbp_signature(shape, elem_bytes, inputs, constraint=None):
         k = okind[d]
         sig.append(("S", oaxis[d]) if k == SPLIT else {BROADCAST: "B", PARTIAL: "P"}[k])
     return sig, cost.value, order.value
+
+
+def infer_broadcast(shapes, specs):
+    """ONNX broadcast n-ary element-wise rule: (output shape, output Spec) for
+    inputs of the given shapes and layouts; RtpError -4 when the inputs are
+    sharded incompatibly."""
+    n = len(shapes)
+    nds = (ctypes.c_int32 * n)(*[len(sh) for sh in shapes])
+    arrs = [_i64(sh) for sh in shapes]
+    shp = (ctypes.POINTER(ctypes.c_int64) * n)(*[ctypes.cast(a, ctypes.POINTER(ctypes.c_int64)) for a in arrs])
+    sp = (Spec * n)(*specs)
+    out_nd, oshape, out = ctypes.c_int(), _i64([0] * 8), Spec()
+    _check(_load().rtp_infer_broadcast(n, nds, shp, sp, ctypes.byref(out_nd), oshape, ctypes.byref(out)))
+    return tuple(oshape[d] for d in range(out_nd.value)), out
 
 
 # ---- tensor-parallel MLP ------------------------------------------------------------

@@ -14,6 +14,7 @@
 // rtp_infer_sbp_signature follows the OneFlow page's walk-through of SBP
 // signature inference for add_n: candidate set (split on every axis, partial
 // sum, broadcast), filters, and the sort by OrderValue then CopyCost.
+#include <algorithm>
 #include <cstring>
 #include <string>
 
@@ -273,5 +274,216 @@ extern "C" int rtp_infer_sbp_signature(int n_in, int ndim, const int64_t* shape,
     }
     if (out_cost) *out_cost = best_cost;
     if (out_order) *out_order = best_order;
+    return RTP_OK;
+}
+
+// ---- ONNX sharding checker: broadcast n-ary element-wise operators ----------------
+//
+// "ONNX multi-device proposal", operator groups, broadcast n-ary element-wise
+// operators: inputs must agree on every non-broadcast axis, a broadcast axis
+// of extent 1 must be held whole wherever it is used, and the output shard of
+// a device is what it can compute from the input shards it holds; with two or
+// more broadcast axes a shard's devices are the intersection of the devices of
+// the input shards it reads (the Add([M,1],[1,N]) example).
+
+namespace {
+
+struct Interval {
+    int64_t lo, hi;
+    bool operator<(const Interval& o) const { return lo < o.lo || (lo == o.lo && hi < o.hi); }
+    bool operator==(const Interval& o) const { return lo == o.lo && hi == o.hi; }
+};
+
+}  // namespace
+
+extern "C" int rtp_infer_broadcast(int n_in, const int32_t* in_ndims, const int64_t* const* in_shapes,
+                                   const rtp_spec* in_specs, int* out_ndim, int64_t* out_shape, rtp_spec* out_spec)
+{
+    using namespace rtp;
+    const char* fn = "rtp_infer_broadcast";
+    if (n_in < 1 || !in_ndims || !in_shapes || !in_specs || !out_ndim || !out_shape || !out_spec)
+        return fail(RTP_EINVAL, "%s: NULL argument or no input", fn);
+    int nd = 0;
+    for (int k = 0; k < n_in; ++k) {
+        if (in_ndims[k] < 1 || in_ndims[k] > RTP_MAX_NDIM || !in_shapes[k])
+            return fail(RTP_EINVAL, "%s: input %d has rank %d", fn, k, in_ndims[k]);
+        if (in_ndims[k] > nd) nd = in_ndims[k];
+        int st = check_spec(in_ndims[k], in_specs[k], "input");
+        if (st) return st;
+        for (int d = 0; d < in_specs[k].mesh_ndim; ++d)
+            if (is_partial(in_specs[k].sbp_kind[d]))
+                return fail(RTP_EUNSUPPORTED, "%s: input %d is partial; the ONNX operator rules have no partial "
+                            "layouts", fn, k);
+    }
+    const int64_t R = num_ranks(in_specs[0]);
+    for (int k = 1; k < n_in; ++k)
+        if (num_ranks(in_specs[k]) != R)
+            return fail(RTP_EINVAL, "%s: inputs live on %lld and %lld ranks", fn, (long long)R,
+                        (long long)num_ranks(in_specs[k]));
+    // multidirectional broadcast of the shapes (trailing dims aligned)
+    int64_t shape[RTP_MAX_NDIM];
+    for (int d = 0; d < nd; ++d) {
+        int64_t e = 1;
+        for (int k = 0; k < n_in; ++k) {
+            const int dk = d - (nd - in_ndims[k]);
+            if (dk < 0) continue;
+            const int64_t x = in_shapes[k][dk];
+            if (x < 1) return fail(RTP_ESHAPE, "%s: extent %lld (must be >= 1)", fn, (long long)x);
+            if (x == 1) continue;
+            if (e != 1 && e != x)
+                return fail(RTP_ESHAPE, "%s: extents %lld and %lld on output dim %d do not broadcast", fn, (long long)e,
+                            (long long)x, d);
+            e = x;
+        }
+        shape[d] = e;  // 1 when every input has extent 1 there
+    }
+    // each rank's output box: the intersection over inputs of what its pieces allow
+    std::vector<Box> box((size_t)R);
+    std::vector<bool> empty((size_t)R, false);
+    std::vector<int64_t> coords((size_t)R * RTP_MAX_MESH_NDIM);
+    for (int64_t r = 0; r < R; ++r) {
+        for (int d = 0; d < nd; ++d) {
+            box[r].lo[d] = 0;
+            box[r].hi[d] = shape[d];
+        }
+    }
+    for (int k = 0; k < n_in; ++k) {
+        rank_coords(in_specs[k], coords.data());
+        for (int64_t r = 0; r < R; ++r) {
+            const Box b = rank_box(in_ndims[k], in_shapes[k], in_specs[k], coords.data() + r * RTP_MAX_MESH_NDIM);
+            for (int dk = 0; dk < in_ndims[k]; ++dk) {
+                const int d = dk + (nd - in_ndims[k]);
+                if (in_shapes[k][dk] == shape[d]) {  // a non-broadcast axis: intersect
+                    box[r].lo[d] = std::max(box[r].lo[d], b.lo[dk]);
+                    box[r].hi[d] = std::min(box[r].hi[d], b.hi[dk]);
+                } else if (b.hi[dk] <= b.lo[dk]) {   // extent 1 broadcast, but this rank holds none of it
+                    empty[r] = true;
+                }
+            }
+        }
+    }
+    for (int64_t r = 0; r < R; ++r)
+        for (int d = 0; d < nd; ++d)
+            if (box[r].hi[d] <= box[r].lo[d] && shape[d] > 0) empty[r] = true;
+    // an input laid out over the whole output shape whose pieces are exactly the
+    // boxes is the answer as it stands (the usual case: inputs sharded alike)
+    for (int k = 0; k < n_in; ++k) {
+        if (in_ndims[k] != nd || !std::equal(shape, shape + nd, in_shapes[k])) continue;
+        rank_coords(in_specs[k], coords.data());
+        bool same = true;
+        for (int64_t r = 0; r < R && same; ++r) {
+            const Box b = rank_box(nd, shape, in_specs[k], coords.data() + r * RTP_MAX_MESH_NDIM);
+            // a rank that computes nothing must hold an empty piece; the others the same box
+            const bool none = empty[r] || box_volume(nd, box[r]) == 0;
+            if (none) {
+                same = box_volume(nd, b) == 0;
+            } else {
+                for (int d = 0; d < nd; ++d)
+                    if (b.lo[d] != box[r].lo[d] || b.hi[d] != box[r].hi[d]) same = false;
+            }
+        }
+        if (same) {
+            *out_ndim = nd;
+            for (int d = 0; d < nd; ++d) out_shape[d] = shape[d];
+            *out_spec = in_specs[k];
+            clear_error();
+            return RTP_OK;
+        }
+    }
+    auto same_box = [&](int64_t x, int64_t y) {
+        for (int d = 0; d < nd; ++d)
+            if (box[x].lo[d] != box[y].lo[d] || box[x].hi[d] != box[y].hi[d]) return false;
+        return true;
+    };
+    // distinct boxes must not overlap (else no layout describes them)
+    std::vector<int64_t> distinct;
+    for (int64_t r = 0; r < R; ++r) {
+        if (empty[r]) continue;
+        bool seen = false;
+        for (int64_t x : distinct) seen |= same_box(x, r);
+        if (!seen) distinct.push_back(r);
+    }
+    for (size_t i = 0; i < distinct.size(); ++i)
+        for (size_t j = i + 1; j < distinct.size(); ++j) {
+            bool meet = true;
+            for (int d = 0; d < nd; ++d)
+                meet &= std::max(box[distinct[i]].lo[d], box[distinct[j]].lo[d]) <
+                        std::min(box[distinct[i]].hi[d], box[distinct[j]].hi[d]);
+            if (meet)
+                return fail(RTP_EUNSUPPORTED, "%s: the output pieces of ranks %lld and %lld overlap without being "
+                            "equal", fn, (long long)distinct[i], (long long)distinct[j]);
+        }
+    // disjoint pieces cover the output iff their volumes add up
+    int64_t total = 1, covered = 0;
+    for (int d = 0; d < nd; ++d) total *= shape[d];
+    for (int64_t x : distinct) covered += box_volume(nd, box[x]);
+    if (covered != total)
+        return fail(RTP_ECONFLICT, "%s: some output elements have no device holding all of their inputs (the inputs "
+                    "are sharded incompatibly)", fn);
+    for (int64_t r = 0; r < R; ++r)
+        if (empty[r]) return fail(RTP_EUNSUPPORTED, "%s: rank %lld computes nothing", fn, (long long)r);
+    // a grid of cells, each on the same number of ranks
+    std::vector<std::vector<Interval>> cuts((size_t)nd);
+    int64_t cells = 1;
+    for (int d = 0; d < nd; ++d) {
+        for (int64_t r = 0; r < R; ++r) cuts[d].push_back({box[r].lo[d], box[r].hi[d]});
+        std::sort(cuts[d].begin(), cuts[d].end());
+        cuts[d].erase(std::unique(cuts[d].begin(), cuts[d].end()), cuts[d].end());
+        cells *= (int64_t)cuts[d].size();
+    }
+    if (cells != (int64_t)distinct.size())
+        return fail(RTP_EUNSUPPORTED, "%s: the output pieces do not form a grid", fn);
+    std::vector<std::vector<int>> holders((size_t)cells);
+    for (int64_t r = 0; r < R; ++r) {
+        int64_t cell = 0;
+        for (int d = 0; d < nd; ++d) {
+            const int64_t i = std::lower_bound(cuts[d].begin(), cuts[d].end(), Interval{box[r].lo[d], box[r].hi[d]}) -
+                              cuts[d].begin();
+            cell = cell * (int64_t)cuts[d].size() + i;
+        }
+        holders[cell].push_back((int)r);
+    }
+    const size_t rep = holders[0].size();
+    for (const auto& h : holders)
+        if (h.size() != rep)
+            return fail(RTP_EUNSUPPORTED, "%s: output pieces are held by unequal numbers of ranks", fn);
+    // the output layout: split mesh dims (output axes in order, outer first), then
+    // one broadcast mesh dim for the replicas
+    rtp_spec o;
+    std::memset(&o, 0, sizeof o);
+    for (int d = 0; d < nd; ++d) {
+        if (cuts[d].size() <= 1) continue;
+        if (o.mesh_ndim == RTP_MAX_MESH_NDIM)
+            return fail(RTP_EUNSUPPORTED, "%s: more than %d split output axes", fn, RTP_MAX_MESH_NDIM);
+        o.mesh_shape[o.mesh_ndim] = (int64_t)cuts[d].size();
+        o.sbp_kind[o.mesh_ndim] = RTP_SBP_SPLIT;
+        o.sbp_axis[o.mesh_ndim] = d;
+        ++o.mesh_ndim;
+    }
+    if (rep > 1 || o.mesh_ndim == 0) {
+        if (o.mesh_ndim == RTP_MAX_MESH_NDIM)
+            return fail(RTP_EUNSUPPORTED, "%s: too many mesh dims for the output", fn);
+        o.mesh_shape[o.mesh_ndim] = (int64_t)rep;
+        o.sbp_kind[o.mesh_ndim] = RTP_SBP_BROADCAST;
+        ++o.mesh_ndim;
+    }
+    for (int64_t c = 0; c < cells; ++c) {
+        std::vector<int> h = holders[c];
+        std::sort(h.begin(), h.end());
+        for (size_t t = 0; t < rep; ++t) o.rank_ids[c * rep + t] = h[t];
+    }
+    // the spec must reproduce the boxes (the cuts follow this library's split rule)
+    rank_coords(o, coords.data());
+    for (int64_t r = 0; r < R; ++r) {
+        const Box b = rank_box(nd, shape, o, coords.data() + r * RTP_MAX_MESH_NDIM);
+        for (int d = 0; d < nd; ++d)
+            if (b.lo[d] != box[r].lo[d] || b.hi[d] != box[r].hi[d])
+                return fail(RTP_EUNSUPPORTED, "%s: the output cuts of dim %d are not the even split this library "
+                            "uses", fn, d);
+    }
+    *out_ndim = nd;
+    for (int d = 0; d < nd; ++d) out_shape[d] = shape[d];
+    *out_spec = o;
+    clear_error();
     return RTP_OK;
 }

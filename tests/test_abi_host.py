@@ -2,6 +2,7 @@
 host-only logic (front-ends, shard geometry, inference, reshape rule, planned
 traffic) agrees with the oracle. No GPU needed: nothing here launches work."""
 import itertools
+import json
 import os
 import re
 
@@ -210,3 +211,58 @@ def test_sbp_signature_matches_oracle():
                 assert rtp.infer_sbp_signature(shape, 2, inputs, constraint=cons) == tuple(want[:3])
     assert rtp.infer_sbp_signature((2, 4), 4, [[("S", 0)], [("S", 1)]])[0] == [("S", 0)]
     assert rtp.infer_sbp_signature((2, 4), 4, [[("S", 0)], ["B"]])[0] == ["B"]
+
+
+def test_infer_broadcast_matches_oracle():
+    """ONNX broadcast n-ary rule: the library (box intersection) and the oracle
+    (per element) agree on the status and on every rank's output piece."""
+    import sys
+    sys.path.insert(0, os.path.dirname(__file__))
+    from test_oracle_pins import _random_broadcast_case
+
+    rng = np.random.default_rng(11)
+    counts = {0: 0, 1: 0, 2: 0}
+    for _ in range(300):
+        shapes, layouts = _random_broadcast_case(rng)
+        st, oshape, boxes, _ = oracle.infer_broadcast(shapes, layouts)
+        counts[st] += 1
+        specs = [rtp.spec_nd_sbp(L.mesh, L.entries, L.devices) for L in layouts]
+        if st != 0:
+            with pytest.raises(rtp.RtpError) as e:
+                rtp.infer_broadcast(shapes, specs)
+            assert e.value.status == {1: -4, 2: -3}[st], (shapes, layouts, rtp.last_error())
+            continue
+        shape, spec = rtp.infer_broadcast(shapes, specs)
+        assert shape == oshape
+        for r, (lo, hi) in enumerate(boxes):
+            llo, lhi, _ = rtp.shard_box(shape, spec, r)
+            if any(h <= l for l, h in zip(lo, hi)):
+                assert any(h <= l for l, h in zip(llo, lhi))
+            else:
+                assert (tuple(llo), tuple(lhi)) == (lo, hi)
+    assert min(counts.values()) > 20, counts
+
+
+def test_infer_broadcast_page_examples(golden_dir):
+    cases = json.load(open(os.path.join(golden_dir, "onnx_broadcast_rule_examples.json")))["cases"]
+    comp, bad = cases
+
+    def spec(inp):
+        dm = {int(k): v for k, v in inp["device_map"].items()}
+        return rtp.spec_from_onnx(len(inp["shape"]), inp["device"], dm, [tuple(x) for x in inp["sharded_dim"]])
+
+    shape, o = rtp.infer_broadcast([c["shape"] for c in comp["inputs"]], [spec(c) for c in comp["inputs"]])
+    assert list(shape) == comp["expected_shape"]
+    for dev, (i, j) in enumerate(comp["expected_shard_of_device"]):
+        lo, hi, _ = rtp.shard_box(shape, o, dev)
+        assert tuple(lo) == (2 * i, 3 * j) and tuple(hi) == (2 * i + 2, 3 * j + 3)
+    with pytest.raises(rtp.RtpError) as e:
+        rtp.infer_broadcast([c["shape"] for c in bad["inputs"]], [spec(c) for c in bad["inputs"]])
+    assert e.value.status == -4
+    # partial inputs and shapes that do not broadcast are refused
+    with pytest.raises(rtp.RtpError) as e:
+        rtp.infer_broadcast([(4, 4), (4, 4)], [rtp.spec_nd_sbp((2,), ("P",)), rtp.spec_nd_sbp((2,), ("B",))])
+    assert e.value.status == -3
+    with pytest.raises(rtp.RtpError) as e:
+        rtp.infer_broadcast([(4, 3), (4, 5)], [rtp.spec_nd_sbp((2,), ("B",))] * 2)
+    assert e.value.status == -2

@@ -579,3 +579,104 @@ def test_sbp_signature_invariants():
     assert sig == [("S", 1)] and cost == 64 and order == -20
     with pytest.raises(oracle.OracleError):
         oracle.infer_sbp_signature((4,), 4, [[("S", 0)]], constraint=[("S", 3)])
+
+
+# ---- ONNX broadcast n-ary element-wise rule (ONNX page, operator groups) ----------
+
+def _onnx_layout(inp):
+    dm = {int(k): v for k, v in inp["device_map"].items()}
+    return oracle.layout_from_onnx(len(inp["shape"]), inp["device"], dm, [tuple(x) for x in inp["sharded_dim"]])
+
+
+def test_broadcast_rule_page_examples(golden_dir):
+    cases = json.load(open(os.path.join(golden_dir, "onnx_broadcast_rule_examples.json")))["cases"]
+    comp, bad = cases
+    st, shape, boxes, _ = oracle.infer_broadcast([c["shape"] for c in comp["inputs"]],
+                                                 [_onnx_layout(c) for c in comp["inputs"]])
+    assert st == 0 and list(shape) == comp["expected_shape"]
+    for dev, (i, j) in enumerate(comp["expected_shard_of_device"]):
+        rows, cols = shape[0] // 2, shape[1] // 2
+        assert boxes[dev] == ((i * rows, j * cols), ((i + 1) * rows, (j + 1) * cols))
+    st, _, _, _ = oracle.infer_broadcast([c["shape"] for c in bad["inputs"]], [_onnx_layout(c) for c in bad["inputs"]])
+    assert st == 1
+
+
+def _random_broadcast_case(rng):
+    nd = int(rng.integers(1, 4))
+    out = [int(rng.integers(1, 7)) for _ in range(nd)]
+    meshes = {2: [(2,)], 3: [(3,)], 4: [(4,), (2, 2)], 6: [(6,), (2, 3), (3, 2)]}
+    R = int(rng.choice([2, 3, 4, 6]))
+    shapes, layouts = [], []
+    for _ in range(int(rng.integers(2, 4))):
+        drop = int(rng.integers(0, nd))  # leading dims absent
+        sh = [1 if rng.random() < 0.3 else x for x in out[drop:]]
+        mesh = meshes[R][int(rng.integers(0, len(meshes[R])))]
+        ents = []
+        for _m in mesh:
+            if rng.random() < 0.6:
+                ents.append(("S", int(rng.integers(0, len(sh)))))
+            else:
+                ents.append("B")
+        shapes.append(tuple(sh))
+        layouts.append(Layout(mesh, tuple(ents), tuple(int(v) for v in rng.permutation(R))))
+    return shapes, layouts
+
+
+def test_broadcast_rule_by_execution():
+    """Where the rule infers a layout, every device computes its output box
+    from its own input pieces alone (numpy broadcasting on the local slices) and
+    gets the slice of the global result; where it reports a conflict, some
+    output element is read from input pieces no single device holds together
+    (found by a direct search over elements and devices)."""
+    rng = np.random.default_rng(7)
+    seen = {0: 0, 1: 0, 2: 0}
+    for _ in range(150):
+        shapes, layouts = _random_broadcast_case(rng)
+        st, oshape, boxes, lay = oracle.infer_broadcast(shapes, layouts)
+        seen[st] += 1
+        xs = [rng.standard_normal(sh) for sh in shapes]
+        full = sum((k + 1) * x for k, x in enumerate(xs)) * np.ones(oshape)
+        nd = len(oshape)
+        if st == 0:
+            for dev, (lo, hi) in enumerate(boxes):
+                assert lay is not None
+                llo, lhi, _ = oracle.shard_box(oshape, lay, dev)
+                if any(h <= l for l, h in zip(lo, hi)):  # computes nothing: an empty piece
+                    assert any(h <= l for l, h in zip(llo, lhi))
+                    continue
+                assert (llo, lhi) == (lo, hi)
+                acc = np.zeros([h - l for l, h in zip(lo, hi)])
+                for k, (x, L) in enumerate(zip(xs, layouts)):
+                    plo, phi, _ = oracle.shard_box(x.shape, L, dev)
+                    piece = x[tuple(slice(a, b) for a, b in zip(plo, phi))]
+                    off = nd - x.ndim
+                    sl = []
+                    for dk in range(x.ndim):
+                        d = dk + off
+                        if x.shape[dk] == 1:
+                            assert phi[dk] - plo[dk] == 1
+                            sl.append(slice(0, 1))
+                        else:
+                            assert plo[dk] <= lo[d] and hi[d] <= phi[dk]
+                            sl.append(slice(lo[d] - plo[dk], hi[d] - plo[dk]))
+                    acc = acc + (k + 1) * piece[tuple(sl)]
+                np.testing.assert_array_equal(acc, full[tuple(slice(l, h) for l, h in zip(lo, hi))])
+        elif st == 1:
+            # some element has no device holding every input element it reads
+            found = False
+            for e in np.ndindex(*oshape):
+                ok_any = False
+                for dev in range(layouts[0].num_devices):
+                    ok = True
+                    for x, L in zip(xs, layouts):
+                        plo, phi, _ = oracle.shard_box(x.shape, L, dev)
+                        off = nd - x.ndim
+                        for dk in range(x.ndim):
+                            i = 0 if x.shape[dk] == 1 else e[dk + off]
+                            ok &= plo[dk] <= i < phi[dk]
+                    ok_any |= ok
+                if not ok_any:
+                    found = True
+                    break
+            assert found
+    assert seen[0] > 20 and seen[1] > 10, seen
