@@ -367,6 +367,7 @@ def run_ours(args, rank, world, local_rank):
         "f2_tp_mlp_sequence_parallel": {"ms": round(sp_ms, 4), "tflops": round(MLP_FLOPS / (sp_ms * 1e-3) / 1e12, 1),
                                         "frac_bf16": round(MLP_FLOPS / (sp_ms * 1e-3) / 1e12 / bf16_peak, 4)},
         "f3_infer_sbp_signature": {"us_per_call": host["sbp_signature_us"], "where": "host"},
+        "f3_onnx_broadcast_checker": {"us_per_call": host["infer_broadcast_us"], "where": "host"},
         "f1_tp_mlp_backward": {"ms": round(bwd_ms, 4), "tflops": round(2 * MLP_FLOPS / (bwd_ms * 1e-3) / 1e12, 1),
                                "frac_bf16": round(2 * MLP_FLOPS / (bwd_ms * 1e-3) / 1e12 / bf16_peak, 4),
                                "dX_sum": "fused in the GEMM",
@@ -445,7 +446,15 @@ def host_inference_timings(rtp, reps: int = 2000):
     for _ in range(reps):
         rtp.infer_sbp_signature((2, 4), 4, [[("S", 0)], [("S", 1)]])
     c = (time.perf_counter() - t) / reps * 1e6
-    return {"infer_spmd_us": round(a, 2), "infer_reshape_us": round(b, 2), "sbp_signature_us": round(c, 2)}
+    # ONNX broadcast rule: Add([4096,1],[1,4096]) with the page's composition layouts
+    sa = rtp.spec_nd_sbp((2, 2), (("S", 0), "B"), (0, 1, 2, 3))
+    sb = rtp.spec_nd_sbp((2, 2), (("S", 1), "B"), (0, 2, 1, 3))
+    t = time.perf_counter()
+    for _ in range(reps):
+        rtp.infer_broadcast([(4096, 1), (1, 4096)], [sa, sb])
+    d = (time.perf_counter() - t) / reps * 1e6
+    return {"infer_spmd_us": round(a, 2), "infer_reshape_us": round(b, 2), "sbp_signature_us": round(c, 2),
+            "infer_broadcast_us": round(d, 2)}
 
 
 MLP_FLOPS = 2 * MLP["M"] * MLP["K"] * MLP["F"] + 2 * MLP["M"] * MLP["F"] * MLP["N"]
