@@ -229,7 +229,20 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Waits for this thread's outstanding tcgen05.ld. The registers of the load
+// whose results are used next pass through the asm as read-write operands, so
+// the compiler cannot move their uses above the wait.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
 
 __device__ __forceinline__ void tile_coords(const GemmArgs& a, int tile, int& g, int& mt, int& nt)
 {
@@ -558,30 +571,25 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
                 orow = row - (int64_t)sh * a.out_rows_per_ptr;
             }
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-            if constexpr (EPI == EPI_DGELU_BF16) {
-                // dH = dY * GELU'(H): the accumulator is dY, H is read at the same
-                // place; the next chunk's H is loaded while this chunk is computed
-                const __nv_bfloat16* hrow = static_cast<const __nv_bfloat16*>(a.aux[g]) + orow * a.ldo;
-                auto load_h = [&](int c, uint4 (&h)[4]) {
+            const __nv_bfloat16* hrow = nullptr;
+            if constexpr (EPI == EPI_DGELU_BF16) hrow = static_cast<const __nv_bfloat16*>(a.aux[g]) + orow * a.ldo;
+            // H of chunk c (GELU-gradient epilogue only)
+            auto load_h = [&](int c, uint4 (&h)[4]) {
+                if constexpr (EPI == EPI_DGELU_BF16) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int64_t cq = col + 32 * c + 8 * q;
                         h[q] = (row_ok && cq < a.n_end) ? __ldg(reinterpret_cast<const uint4*>(hrow + cq))
                                                          : make_uint4(0u, 0u, 0u, 0u);
                     }
-                };
-                uint4 hn[4];
-                load_h(c_begin, hn);
-                for (int c = c_begin; c < c_begin + EPI_CHUNKS; ++c) {
-                    uint4 h[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) h[q] = hn[q];
-                    if (c + 1 < c_begin + EPI_CHUNKS) load_h(c + 1, hn);
-                    uint32_t r[32];
-                    tmem_ld_32cols(taddr + 32u * c, r);
-                    tmem_ld_wait();
-                    const int64_t c0 = col + 32 * c;
-                    if (!row_ok || c0 >= a.n_end) continue;
+                }
+            };
+            // writes chunk c (32 columns of this thread's row) from its accumulator values
+            auto emit = [&](int c, const uint32_t (&r)[32], const uint4 (&h)[4]) {
+                const int64_t c0 = col + 32 * c;
+                if (!row_ok || c0 >= a.n_end) return;
+                if constexpr (EPI == EPI_DGELU_BF16) {
+                    // dH = dY * GELU'(H): the accumulator is dY, H was read at the same place
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_base) + orow * a.ldo + c0);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -597,47 +605,59 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
                                         __uint_as_float(r[8 * q + 7]) * gelu_grad(bf16_hi(h[q].w)));
                         __stcs(dst + q, v);
                     }
-                }
-            } else {
-                for (int c = c_begin; c < c_begin + EPI_CHUNKS; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_32cols(taddr + 32u * c, r);
-                    tmem_ld_wait();
-                    const int64_t c0 = col + 32 * c;
-                    if (!row_ok || c0 >= a.n_end) continue;
-                    if constexpr (EPI == EPI_GELU_BF16) {
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_base) + orow * a.ldo + c0);
-                        uint4* hdst = a.out2[g] ? reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out2[g]) +
-                                                                           orow * a.ldo + c0)
-                                                : nullptr;
+                } else if constexpr (EPI == EPI_GELU_BF16) {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_base) + orow * a.ldo + c0);
+                    uint4* hdst = a.out2[g] ? reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out2[g]) +
+                                                                       orow * a.ldo + c0)
+                                            : nullptr;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            if (c0 + 8 * q >= a.n_end) break;
-                            uint4 v;
-                            v.x = pack_bf16(gelu(__uint_as_float(r[8 * q + 0])), gelu(__uint_as_float(r[8 * q + 1])));
-                            v.y = pack_bf16(gelu(__uint_as_float(r[8 * q + 2])), gelu(__uint_as_float(r[8 * q + 3])));
-                            v.z = pack_bf16(gelu(__uint_as_float(r[8 * q + 4])), gelu(__uint_as_float(r[8 * q + 5])));
-                            v.w = pack_bf16(gelu(__uint_as_float(r[8 * q + 6])), gelu(__uint_as_float(r[8 * q + 7])));
-                            __stcs(dst + q, v);
-                            if (hdst) {  // the pre-activation, for the backward pass
-                                uint4 h;
-                                h.x = pack_bf16(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]));
-                                h.y = pack_bf16(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]));
-                                h.z = pack_bf16(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]));
-                                h.w = pack_bf16(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]));
-                                __stcs(hdst + q, h);
-                            }
-                        }
-                    } else {
-                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_base) + orow * a.ldo + c0);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            if (c0 + 4 * q >= a.n_end) break;
-                            __stcs(dst + q, make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
-                                                        __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
+                    for (int q = 0; q < 4; ++q) {
+                        if (c0 + 8 * q >= a.n_end) break;
+                        uint4 v;
+                        v.x = pack_bf16(gelu(__uint_as_float(r[8 * q + 0])), gelu(__uint_as_float(r[8 * q + 1])));
+                        v.y = pack_bf16(gelu(__uint_as_float(r[8 * q + 2])), gelu(__uint_as_float(r[8 * q + 3])));
+                        v.z = pack_bf16(gelu(__uint_as_float(r[8 * q + 4])), gelu(__uint_as_float(r[8 * q + 5])));
+                        v.w = pack_bf16(gelu(__uint_as_float(r[8 * q + 6])), gelu(__uint_as_float(r[8 * q + 7])));
+                        __stcs(dst + q, v);
+                        if (hdst) {  // the pre-activation, for the backward pass
+                            uint4 hv;
+                            hv.x = pack_bf16(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]));
+                            hv.y = pack_bf16(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]));
+                            hv.z = pack_bf16(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]));
+                            hv.w = pack_bf16(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]));
+                            __stcs(hdst + q, hv);
                         }
                     }
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_base) + orow * a.ldo + c0);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        if (c0 + 4 * q >= a.n_end) break;
+                        __stcs(dst + q, make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
+                                                    __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
+                    }
                 }
+            };
+            // the TMEM load (and H load) of the next chunk is in flight while a
+            // chunk is computed and stored (the loads are warp-wide: all lanes)
+            static_assert(EPI_CHUNKS % 2 == 0, "chunks are processed in pairs");
+            const int c_end = c_begin + EPI_CHUNKS;
+            uint32_t ra[32], rb[32];
+            uint4 ha[4], hb[4];
+            load_h(c_begin, ha);
+            tmem_ld_32cols(taddr + 32u * c_begin, ra);
+            tmem_ld_wait(ra);
+            for (int c = c_begin; c < c_end; c += 2) {
+                tmem_ld_32cols(taddr + 32u * (c + 1), rb);
+                load_h(c + 1, hb);
+                emit(c, ra, ha);
+                tmem_ld_wait(rb);
+                if (c + 2 < c_end) {
+                    tmem_ld_32cols(taddr + 32u * (c + 2), ra);
+                    load_h(c + 2, ha);
+                }
+                emit(c + 1, rb, hb);
+                if (c + 2 < c_end) tmem_ld_wait(ra);
             }
             tc_fence_before();
             __syncwarp();
