@@ -393,13 +393,15 @@ int rtp_tp_mlp_noalloc(int P, int64_t M, int64_t K, int64_t F, int64_t N, const 
                        const void* const* B_shards, float* Z, rtp_stream stream);
 
 /*
- * Reads and clears the device word in which the tensor-core kernels of
+ * Reads and clears the device words in which the tensor-core kernels of
  * rtp_tp_mlp record a wait that gave up (no progress for about 4 seconds; the
- * kernel then stops, frees its tensor memory and returns instead of hanging).
+ * kernel then stops, frees its tensor memory and returns instead of hanging),
+ * and in which the resharding kernel records a bulk copy that never completed.
  * Synchronises `stream`. *code == 0: no such event since the last check;
  * otherwise the results of the launches since then are invalid
  * (1 producer, 2 MMA waiting for operands, 3 MMA waiting for an accumulator,
- * 4 epilogue, 5 rtp_wait_selftest).
+ * 4 epilogue, 5 rtp_wait_selftest; 16: a bulk copy of the resharding kernel
+ * did not complete within about 2 seconds, so that launch stopped early).
  */
 int rtp_device_error(rtp_stream stream, uint32_t* code);
 

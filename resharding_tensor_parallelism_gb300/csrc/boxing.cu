@@ -38,6 +38,55 @@ constexpr int kBlock = 256;
 constexpr int64_t kChunkBytes = 32 * 1024;
 constexpr int kMaxTasks = 96;
 constexpr int kMaxPtrs = 640;
+constexpr int kBulkMinRowBytes = 4096;        // shorter rows take the register path (measured: bulk copies of 1-2 KB rows are slower)
+constexpr int64_t kBulkStageBytes = 64 * 1024;  // shared staging of a reduction chunk (all sources)
+constexpr int kBulkDynSmem = 64 * 1024;       // dynamic shared memory a launch may request
+constexpr unsigned long long kBulkWaitNs = 2000000000ull;
+constexpr uint32_t kErrBulkWait = 16;         // device error code: a bulk copy never completed
+
+__device__ unsigned int g_box_error;
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t now_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for phase `parity` of an mbarrier; false (and the error word
+// set) when it does not complete within kBulkWaitNs.
+__device__ __noinline__ bool bar_wait(uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = now_ns();
+    for (uint32_t i = 0;; ++i) {
+        uint32_t done;
+        asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                     : "=r"(done)
+                     : "r"(bar), "r"(parity)
+                     : "memory");
+        if (done) return true;
+        if ((i & 15u) == 15u && now_ns() - t0 > kBulkWaitNs) {
+            atomicCAS(&g_box_error, 0u, kErrBulkWait);
+            return false;
+        }
+    }
+}
+
+// Bulk copies (cp.async.bulk, no tensor map): 16-byte aligned addresses, sizes
+// multiple of 16. Loads complete on an mbarrier; stores form a bulk group.
+__device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst_smem), "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src_smem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src_smem), "r"(bytes)
+                 : "memory");
+}
 
 struct KTask {
     int64_t chunk_begin;  // first chunk index of this task within the launch
@@ -50,7 +99,7 @@ struct KTask {
     int32_t op;           // RED_SUM / RED_MIN / RED_MAX: how several sources combine
     uint32_t fill;        // with no source: the element pattern written (the op's identity),
                           // repeated to 32 bits for 16-bit elements
-    int32_t pad_;
+    int32_t bulk;         // 1: staged through shared memory with bulk (TMA) copies
     int64_t sstr[kMaxOuter], dstr[kMaxOuter];
 };
 
@@ -289,6 +338,81 @@ __device__ __forceinline__ void run_chunk(const void* const* ptrs, const KTask& 
     }
 }
 
+// A chunk staged through shared memory: warp 0 bulk-loads every source's rows
+// (source j, row r at (j nr + r) rowbytes), all threads wait on the block's
+// mbarrier, then a copy is bulk-stored from shared memory to every destination
+// (the same bytes, read once), or a reduction is added up by all threads in
+// float32 in source order and stored with streaming stores. False when a wait
+// gave up (the error word is set).
+template <bool SUM, int ES, int OP>
+__device__ __forceinline__ bool bulk_chunk(const void* const* ptrs, const KTask& t, int nr, uint32_t rowbytes,
+                                           const int64_t* s_off, const int64_t* d_off, uint8_t* stage, uint32_t bar,
+                                           uint32_t parity)
+{
+    const int ns = t.n_src;
+    const void* const* sp = ptrs + t.ptr0;
+    const void* const* dp = sp + ns;
+    const uint32_t st0 = su32(stage);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 0) {
+        if (lane == 0)
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                         "r"((uint32_t)ns * (uint32_t)nr * rowbytes)
+                         : "memory");
+        __syncwarp();
+        for (int j = 0; j < ns; ++j)
+            for (int r = lane; r < nr; r += 32)
+                bulk_load(st0 + (uint32_t)(j * nr + r) * rowbytes, static_cast<const char*>(sp[j]) + s_off[r] * ES,
+                          rowbytes, bar);
+    }
+    if (!__syncthreads_and(bar_wait(bar, parity) ? 1 : 0)) return false;
+    if (ns == 1) {
+        if (warp == 0) {
+            for (int k = 0; k < t.n_dst; ++k)
+                for (int r = lane; r < nr; r += 32)
+                    bulk_store(static_cast<char*>(const_cast<void*>(dp[k])) + d_off[r] * ES, st0 + (uint32_t)r * rowbytes,
+                               rowbytes);
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // shared memory read before reuse
+        }
+        return true;
+    }
+    if constexpr (SUM) {
+        constexpr int NE = 16 / ES;
+        const int vpr = (int)(rowbytes / 16);
+        const int total = nr * vpr;
+        const float inv = 1.0f / (float)vpr;
+        const float ident = OP == RED_SUM ? 0.0f : (OP == RED_MIN ? __int_as_float(0x7F800000) : __int_as_float(0xFF800000));
+        for (int i = threadIdx.x; i < total; i += kBlock) {
+            int r, v;
+            divmod(i, vpr, inv, r, v);
+            float acc[NE];
+#pragma unroll
+            for (int e = 0; e < NE; ++e) acc[e] = ident;
+            for (int j = 0; j < ns; ++j) {
+                Lanes<16> x;
+                x.v = *reinterpret_cast<const uint4*>(stage + (size_t)(j * nr + r) * rowbytes + (size_t)v * 16);
+#pragma unroll
+                for (int e = 0; e < NE; ++e) {
+                    float y;
+                    if constexpr (ES == 4) y = __uint_as_float(x.w[e]);
+                    else y = __uint_as_float((uint32_t)x.h[e] << 16);
+                    acc[e] = combine<OP>(acc[e], y);
+                }
+            }
+            Lanes<16> out;
+#pragma unroll
+            for (int e = 0; e < NE; ++e) {
+                if constexpr (ES == 4) out.w[e] = __float_as_uint(acc[e]);
+                else out.h[e] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[e]));
+            }
+            for (int k = 0; k < t.n_dst; ++k)
+                __stcs(reinterpret_cast<uint4*>(static_cast<char*>(const_cast<void*>(dp[k])) + d_off[r] * ES) + v, out.v);
+        }
+    }
+    return true;
+}
+
 // SUM = false: copies and fills only; SUM = true: also multi-source
 // reductions with OP (every reduction of one launch has the same op, that of
 // the source spec). ES: element size in bytes.
@@ -296,6 +420,14 @@ template <class PP, bool SUM, int ES, int OP>
 __global__ void __launch_bounds__(kBlock, 4) boxing_kernel(const __grid_constant__ PP p)
 {
     __shared__ int64_t s_off[kBlock], d_off[kBlock];
+    __shared__ __align__(8) uint64_t bar;
+    extern __shared__ __align__(128) uint8_t stage[];  // bulk staging; sized by the launch
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bar)) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    uint32_t parity = 0;  // phase of `bar` for the next bulk chunk of this block
     for (int64_t c = blockIdx.x; c < p.total_chunks; c += gridDim.x) {
         const KTask& t = p.tasks[find_task(p, c)];
         const int64_t lc = c - t.chunk_begin;
@@ -311,6 +443,13 @@ __global__ void __launch_bounds__(kBlock, 4) boxing_kernel(const __grid_constant
             d_off[threadIdx.x] = dof + c0;
         }
         __syncthreads();
+        if (t.bulk) {  // block-uniform
+            if (!bulk_chunk<SUM, ES, OP>(p.ptrs, t, nr, (uint32_t)(len * ES), s_off, d_off, stage, su32(&bar), parity))
+                return;  // a bulk copy never completed: the error word is set
+            parity ^= 1u;
+            __syncthreads();
+            continue;
+        }
         const int nv = (int)(len * ES / t.vec);
         switch (t.vec) {
         case 16: run_chunk<16, ES, SUM, OP>(p.ptrs, t, nr, nv, s_off, d_off); break;
@@ -352,7 +491,7 @@ int pick_vec(const PlanTask& t, const void* const* src, void* const* dst, int es
 
 // Chunking: rows longer than a chunk are cut into segments (one row per
 // chunk); shorter rows are grouped, up to one row per thread of the block.
-int64_t fill_task(KTask& k, const PlanTask& t, int vec, int es)
+int64_t fill_task(KTask& k, const PlanTask& t, int vec, int es, bool allow_bulk)
 {
     std::memset(&k, 0, sizeof k);
     k.rows = t.rows;
@@ -372,10 +511,18 @@ int64_t fill_task(KTask& k, const PlanTask& t, int vec, int es)
     else k.fill = t.op == RED_MIN ? 0x7F807F80u : t.op == RED_MAX ? 0xFF80FF80u : 0u;
     const int64_t row_bytes = t.cols * es;
     const int64_t epv = vec / es;
-    // a copy to several destinations writes each chunk several times: keep the
-    // bytes a block moves near 2 x 32 KB by shrinking its chunks (4 KB at least)
-    const int64_t chunk_bytes =
-        t.src.size() <= 1 ? std::max<int64_t>(4096, 2 * kChunkBytes / (int64_t)(1 + t.dst.size())) : kChunkBytes;
+    const int64_t ns = (int64_t)t.src.size();
+    // Staged through shared memory (bulk copies) when vectors are 16 bytes, the
+    // rows or segments are long, and every source's chunk fits the staging.
+    const int64_t bulk_chunk_bytes = ns <= 1 ? kChunkBytes : std::max<int64_t>(4096, kBulkStageBytes / std::max<int64_t>(ns, 1));
+    k.bulk = allow_bulk && vec == 16 && ns >= 1 && ns * bulk_chunk_bytes <= kBulkStageBytes &&
+             std::min(row_bytes, bulk_chunk_bytes) >= kBulkMinRowBytes;
+    // Register path: a copy to several destinations writes each chunk several
+    // times, so its chunks shrink to keep the bytes a block moves near 2 x 32 KB
+    // (4 KB at least).
+    const int64_t chunk_bytes = k.bulk ? bulk_chunk_bytes
+                                : ns <= 1 ? std::max<int64_t>(4096, 2 * kChunkBytes / (int64_t)(1 + t.dst.size()))
+                                          : kChunkBytes;
     if (row_bytes >= chunk_bytes) {
         const int64_t seg = std::min(t.cols, std::max<int64_t>(epv, (chunk_bytes / es) / epv * epv));
         k.seg = seg;
@@ -390,6 +537,13 @@ int64_t fill_task(KTask& k, const PlanTask& t, int vec, int es)
     return (t.rows + k.rpc - 1) / k.rpc * k.nseg;
 }
 
+// Shared staging a bulk task's chunk needs (0 for the register path).
+int64_t stage_bytes(const KTask& k, int es)
+{
+    if (!k.bulk) return 0;
+    return (int64_t)k.n_src * (k.rpc == 1 ? k.seg * es : (int64_t)k.rpc * k.cols * es);
+}
+
 // Copies the used part of a full parameter block into a smaller form.
 template <class PP>
 const PP& shrink(const KParams& full, int nt, int np, PP* out)
@@ -402,24 +556,52 @@ const PP& shrink(const KParams& full, int nt, int np, PP* out)
     return *out;
 }
 
+template <class PP, bool SUM, int ES, int OP>
+int launch_one(const PP& prm, int grid, int smem, cudaStream_t st)
+{
+    static bool configured[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(RTP_ECUDA, "reshard: no CUDA device");
+    if (smem > 0 && !configured[dev]) {
+        if (cudaFuncSetAttribute(boxing_kernel<PP, SUM, ES, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kBulkDynSmem) != cudaSuccess)
+            return fail(RTP_ECUDA, "reshard: cudaFuncSetAttribute failed");
+        configured[dev] = true;
+    }
+    boxing_kernel<PP, SUM, ES, OP><<<grid, kBlock, smem, st>>>(prm);
+    return RTP_OK;
+}
+
 template <class PP>
-void launch_boxing(const PP& prm, int grid, cudaStream_t st, bool any_sum, int sum_op, int es)
+int launch_boxing(const PP& prm, int grid, int smem, cudaStream_t st, bool any_sum, int sum_op, int es)
 {
     if (!any_sum) {
-        if (es == 4) boxing_kernel<PP, false, 4, RED_SUM><<<grid, kBlock, 0, st>>>(prm);
-        else boxing_kernel<PP, false, 2, RED_SUM><<<grid, kBlock, 0, st>>>(prm);
-    } else if (es == 4) {
-        if (sum_op == RED_MIN) boxing_kernel<PP, true, 4, RED_MIN><<<grid, kBlock, 0, st>>>(prm);
-        else if (sum_op == RED_MAX) boxing_kernel<PP, true, 4, RED_MAX><<<grid, kBlock, 0, st>>>(prm);
-        else boxing_kernel<PP, true, 4, RED_SUM><<<grid, kBlock, 0, st>>>(prm);
-    } else {
-        if (sum_op == RED_MIN) boxing_kernel<PP, true, 2, RED_MIN><<<grid, kBlock, 0, st>>>(prm);
-        else if (sum_op == RED_MAX) boxing_kernel<PP, true, 2, RED_MAX><<<grid, kBlock, 0, st>>>(prm);
-        else boxing_kernel<PP, true, 2, RED_SUM><<<grid, kBlock, 0, st>>>(prm);
+        if (es == 4) return launch_one<PP, false, 4, RED_SUM>(prm, grid, smem, st);
+        return launch_one<PP, false, 2, RED_SUM>(prm, grid, smem, st);
     }
+    if (es == 4) {
+        if (sum_op == RED_MIN) return launch_one<PP, true, 4, RED_MIN>(prm, grid, smem, st);
+        if (sum_op == RED_MAX) return launch_one<PP, true, 4, RED_MAX>(prm, grid, smem, st);
+        return launch_one<PP, true, 4, RED_SUM>(prm, grid, smem, st);
+    }
+    if (sum_op == RED_MIN) return launch_one<PP, true, 2, RED_MIN>(prm, grid, smem, st);
+    if (sum_op == RED_MAX) return launch_one<PP, true, 2, RED_MAX>(prm, grid, smem, st);
+    return launch_one<PP, true, 2, RED_SUM>(prm, grid, smem, st);
 }
 
 }  // namespace
+
+int take_boxing_error(void* stream, uint32_t* code)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_box_error, sizeof v, 0, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_box_error, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return fail(RTP_ECUDA, "rtp_device_error: %s", cudaGetErrorString(cudaGetLastError()));
+    *code = v;
+    return RTP_OK;
+}
 
 int count_launches(const std::vector<PlanTask>& tasks)
 {
@@ -462,7 +644,8 @@ int launch_tasks(int dtype, const std::vector<PlanTask>& tasks, const void* cons
             const int need = (int)(t.src.size() + t.dst.size());
             if (np + need > kMaxPtrs) break;
             KTask& k = prm.tasks[nt];
-            int64_t nc = fill_task(k, t, pick_vec(t, src, dst, es), es);
+            // beside another kernel the staging would keep the blocks off its SMs
+            int64_t nc = fill_task(k, t, pick_vec(t, src, dst, es), es, blocks_per_sm >= 4);
             k.chunk_begin = chunks;
             k.ptr0 = np;
             for (const auto& r : t.src) prm.ptrs[np++] = static_cast<const char*>(src[r.rank]) + r.offset * es;
@@ -490,15 +673,19 @@ int launch_tasks(int dtype, const std::vector<PlanTask>& tasks, const void* cons
         const int64_t grid64 = blocks_per_sm >= 4 ? std::min<int64_t>(chunks, 0x7fffffff) : std::min<int64_t>(chunks, max_grid);
         const int grid = (int)grid64;
         cudaStream_t st = static_cast<cudaStream_t>(stream);
+        int64_t smem = 0;
+        for (int k = 0; k < nt; ++k) smem = std::max(smem, stage_bytes(prm.tasks[k], es));
+        int st_ok;
         if (nt <= kSmallTasks && np <= kSmallPtrs) {
             static thread_local KParamsSmall small;
-            launch_boxing(shrink(prm, nt, np, &small), grid, st, any_sum, sum_op, es);
+            st_ok = launch_boxing(shrink(prm, nt, np, &small), grid, (int)smem, st, any_sum, sum_op, es);
         } else if (nt <= kMediumTasks && np <= kMediumPtrs) {
             static thread_local KParamsMedium medium;
-            launch_boxing(shrink(prm, nt, np, &medium), grid, st, any_sum, sum_op, es);
+            st_ok = launch_boxing(shrink(prm, nt, np, &medium), grid, (int)smem, st, any_sum, sum_op, es);
         } else {
-            launch_boxing(prm, grid, st, any_sum, sum_op, es);
+            st_ok = launch_boxing(prm, grid, (int)smem, st, any_sum, sum_op, es);
         }
+        if (st_ok) return st_ok;
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return fail(RTP_ECUDA, "boxing kernel launch failed: %s", cudaGetErrorString(e));
         ++launches;

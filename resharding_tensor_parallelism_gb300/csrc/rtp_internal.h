@@ -71,5 +71,7 @@ int launch_tasks(int dtype, const std::vector<PlanTask>& tasks, const void* cons
                  void* stream, int* n_launches_out, int blocks_per_sm = 4);
 // Number of launches the tasks need (host only).
 int count_launches(const std::vector<PlanTask>& tasks);
+// Reads and clears the boxing kernel's device error word (synchronises `stream`).
+int take_boxing_error(void* stream, uint32_t* code);
 
 }  // namespace rtp

@@ -1138,7 +1138,10 @@ int rtp_device_error(rtp_stream stream, uint32_t* code)
         cudaMemcpyToSymbolAsync(g_tp_error, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return fail(RTP_ECUDA, "rtp_device_error: %s", cudaGetErrorString(cudaGetLastError()));
-    *code = v;
+    uint32_t box = 0;
+    int st = take_boxing_error(stream, &box);
+    if (st) return st;
+    *code = v ? v : box;
     return RTP_OK;
 }
 
