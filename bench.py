@@ -165,6 +165,23 @@ def _traffic(kernel: str, workload: str):
     return None
 
 
+def reduce_over_ranks(dist, x: float, device, op: str = "max") -> float:
+    """Max (or sum) of one float over the process group (x itself without one).
+    Replicas report the slowest rank's time and the sum of their bytes."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank: float, world: int, max_ms: float) -> float:
+    """Whole-job throughput of N replicas: every rank moves bytes_per_rank;
+    the job takes as long as the slowest rank."""
+    return bytes_per_rank * world / (max_ms * 1e-3) / 1e9
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import resharding_tensor_parallelism_gb300 as rtp
@@ -349,11 +366,7 @@ def run_ours(args, rank, world, local_rank):
     bwo_ms = per[("bwd_overlap", "bwd_overlap")][0] / args.steps
 
     def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_over_ranks(dist, x, dev, "max")
 
     def gbs_of(kind, pred=lambda label: True):
         ms = sum(v[0] for (k, l), v in per.items() if k == kind and pred(l))
@@ -392,7 +405,7 @@ def run_ours(args, rank, world, local_rank):
     reshard_ms = max_over_ranks(reshard_ms)
     mlp_ms = max_over_ranks(mlp_ms)
     wall_ms = max_over_ranks(wall_ms)
-    gbs = reshard_bytes * world / (reshard_ms * 1e-3) / 1e9
+    gbs = whole_job_gbs(reshard_bytes, world, reshard_ms)
     tflops = MLP_FLOPS * args.steps * world / (mlp_ms * 1e-3) / 1e12
     per_launch_gbs = reshard_bytes / (reshard_ms * 1e-3) / 1e9
 
