@@ -22,6 +22,8 @@
 //     min / max members combine with fminf / fmaxf (exact);
 //   * a task with no source fills its destinations with the identity of the
 //     destination's partial reduction (0, +inf or -inf).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -88,6 +90,23 @@ __device__ __forceinline__ void bulk_store(void* dst, uint32_t src_smem, uint32_
                  : "memory");
 }
 
+// TMA tiles over a 3D view [rows][mid][inner] of a strided row region; the
+// box is rows-per-chunk x mid x inner, i.e. whole rows, dense in shared memory.
+// Rows past the region are zero-filled on load (and count toward the bytes)
+// and skipped on store.
+__device__ __forceinline__ void tile_load(uint32_t dst_smem, const CUtensorMap* map, int row, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+                 ::"r"(dst_smem), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(row), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void tile_store(const CUtensorMap* map, int row, uint32_t src_smem)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(row), "r"(src_smem)
+                 : "memory");
+}
+
 struct KTask {
     int64_t chunk_begin;  // first chunk index of this task within the launch
     int64_t rows, cols;   // region: rows runs of cols contiguous elements
@@ -100,6 +119,9 @@ struct KTask {
     uint32_t fill;        // with no source: the element pattern written (the op's identity),
                           // repeated to 32 bits for 16-bit elements
     int32_t bulk;         // 1: staged through shared memory with bulk (TMA) copies
+    int32_t tile;         // 1: sources read as TMA tiles (rows strided), destination rows contiguous;
+                          // 2: source rows contiguous, destinations written as TMA tiles
+    int32_t map0;         // first tensor map of the task (sources for tile 1, destinations for tile 2)
     int64_t sstr[kMaxOuter], dstr[kMaxOuter];
 };
 
@@ -113,8 +135,23 @@ struct KParamsT {
     int64_t total_chunks;
     KTask tasks[MT];
     const void* ptrs[MP];  // per task: n_src source bases, then n_dst destination bases
+    static constexpr int kMaps = 0;
 };
 using KParams = KParamsT<kMaxTasks, kMaxPtrs>;
+
+// The form for launches with TMA-tile tasks: the tensor maps of their strided
+// sides travel with the tasks.
+constexpr int kTileTasks = 64, kTilePtrs = 256, kTileMaps = 64;
+struct KParamsTile {
+    int32_t n_tasks;
+    int32_t dtype;
+    int64_t total_chunks;
+    KTask tasks[kTileTasks];
+    const void* ptrs[kTilePtrs];
+    CUtensorMap maps[kTileMaps];
+    static constexpr int kMaps = kTileMaps;
+};
+static_assert(sizeof(KParamsTile) <= 32000, "kernel parameter block too large");
 constexpr int kSmallTasks = 16, kSmallPtrs = 128, kMediumTasks = 64, kMediumPtrs = 256;
 using KParamsSmall = KParamsT<kSmallTasks, kSmallPtrs>;
 using KParamsMedium = KParamsT<kMediumTasks, kMediumPtrs>;
@@ -413,6 +450,89 @@ __device__ __forceinline__ bool bulk_chunk(const void* const* ptrs, const KTask&
     return true;
 }
 
+// Staging bytes of one source's box in shared memory (128-byte aligned slots).
+__device__ __host__ __forceinline__ uint32_t tile_slot(int64_t rpc, int64_t row_bytes)
+{
+    return (uint32_t)((rpc * row_bytes + 127) / 128 * 128);
+}
+
+// A chunk of rows r0 .. r0+nr of a one-outer-dim region, staged through shared
+// memory. tile 1: each source's rows arrive as one TMA tile (its rows are
+// strided), the destination rows are contiguous: a copy is one bulk store per
+// destination, a reduction is added up by all threads and stored with
+// streaming stores. tile 2 (copies): the source rows are contiguous (one bulk
+// load), each destination is written as one TMA tile. False when a wait gave
+// up (the error word is set).
+template <class PP, bool SUM, int ES, int OP>
+__device__ __forceinline__ bool tile_chunk(const PP& p, const KTask& t, int64_t r0, int nr, uint32_t row_bytes,
+                                           uint8_t* stage, uint32_t bar, uint32_t parity)
+{
+    const int ns = t.n_src;
+    const void* const* sp = p.ptrs + t.ptr0;
+    const void* const* dp = sp + ns;
+    const uint32_t st0 = su32(stage);
+    const uint32_t slot = tile_slot(t.rpc, row_bytes);
+    const bool first = threadIdx.x == 0;
+    if (first) {
+        if (t.tile == 1) {
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                         "r"((uint32_t)ns * (uint32_t)t.rpc * row_bytes)
+                         : "memory");
+            for (int j = 0; j < ns; ++j) tile_load(st0 + (uint32_t)j * slot, &p.maps[t.map0 + j], (int)r0, bar);
+        } else {
+            const uint32_t bytes = (uint32_t)nr * row_bytes;
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+            bulk_load(st0, static_cast<const char*>(sp[0]) + r0 * t.sstr[0] * ES, bytes, bar);
+        }
+    }
+    if (!__syncthreads_and(bar_wait(bar, parity) ? 1 : 0)) return false;
+    if (ns == 1) {
+        if (first) {
+            for (int k = 0; k < t.n_dst; ++k) {
+                if (t.tile == 1)
+                    bulk_store(static_cast<char*>(const_cast<void*>(dp[k])) + r0 * t.dstr[0] * ES, st0,
+                               (uint32_t)nr * row_bytes);
+                else
+                    tile_store(&p.maps[t.map0 + k], (int)r0, st0);
+            }
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        }
+        return true;
+    }
+    if constexpr (SUM) {
+        constexpr int NE = 16 / ES;
+        const int total = (int)((uint32_t)nr * row_bytes / 16);  // vectors; destination rows are contiguous
+        const float ident = OP == RED_SUM ? 0.0f : (OP == RED_MIN ? __int_as_float(0x7F800000) : __int_as_float(0xFF800000));
+        for (int i = threadIdx.x; i < total; i += kBlock) {
+            float acc[NE];
+#pragma unroll
+            for (int e = 0; e < NE; ++e) acc[e] = ident;
+            for (int j = 0; j < ns; ++j) {
+                Lanes<16> x;
+                x.v = *reinterpret_cast<const uint4*>(stage + (size_t)j * slot + (size_t)i * 16);
+#pragma unroll
+                for (int e = 0; e < NE; ++e) {
+                    float y;
+                    if constexpr (ES == 4) y = __uint_as_float(x.w[e]);
+                    else y = __uint_as_float((uint32_t)x.h[e] << 16);
+                    acc[e] = combine<OP>(acc[e], y);
+                }
+            }
+            Lanes<16> out;
+#pragma unroll
+            for (int e = 0; e < NE; ++e) {
+                if constexpr (ES == 4) out.w[e] = __float_as_uint(acc[e]);
+                else out.h[e] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[e]));
+            }
+            for (int k = 0; k < t.n_dst; ++k)
+                __stcs(reinterpret_cast<uint4*>(static_cast<char*>(const_cast<void*>(dp[k])) + r0 * t.dstr[0] * ES) + i,
+                       out.v);
+        }
+    }
+    return true;
+}
+
 // SUM = false: copies and fills only; SUM = true: also multi-source
 // reductions with OP (every reduction of one launch has the same op, that of
 // the source spec). ES: element size in bytes.
@@ -436,6 +556,15 @@ __global__ void __launch_bounds__(kBlock, 4) boxing_kernel(const __grid_constant
         const int64_t r0 = rb * t.rpc;
         const int nr = (int)min((int64_t)t.rpc, t.rows - r0);
         const int64_t len = min(t.seg, t.cols - c0);
+        if constexpr (PP::kMaps > 0) {
+            if (t.tile) {  // block-uniform
+                if (!tile_chunk<PP, SUM, ES, OP>(p, t, r0, nr, (uint32_t)(t.cols * ES), stage, su32(&bar), parity))
+                    return;  // a bulk copy never completed: the error word is set
+                parity ^= 1u;
+                __syncthreads();
+                continue;
+            }
+        }
         if ((int)threadIdx.x < nr) {
             int64_t so, dof;
             row_offsets(t, r0 + threadIdx.x, so, dof);
@@ -489,6 +618,34 @@ int pick_vec(const PlanTask& t, const void* const* src, void* const* dst, int es
     return es;
 }
 
+// Inner extent of the 3D tile view [rows][cols / inner][inner] of a row of
+// `cols` elements: the largest divisor of cols of at most 256 elements whose
+// bytes are a multiple of 16, with cols / inner at most 256 (0: none).
+int64_t tile_inner(int64_t cols, int es)
+{
+    for (int64_t d = std::min<int64_t>(cols, 256); d >= 1; --d)
+        if (cols % d == 0 && (d * es) % 16 == 0) return cols / d <= 256 ? d : 0;
+    return 0;
+}
+
+// The tensor map of a tile task's strided side: base `ptr`, `rows` rows of
+// `cols` elements, `stride` elements apart; box: rpc whole rows.
+int encode_tile_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t stride, int64_t rpc, int es)
+{
+    auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+    if (!fn) return fail(RTP_ECUDA, "reshard: cuTensorMapEncodeTiled is unavailable");
+    const int64_t inner = tile_inner(cols, es);
+    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)(cols / inner), (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)(inner * es), (cuuint64_t)(stride * es)};
+    cuuint32_t box[3] = {(cuuint32_t)inner, (cuuint32_t)(cols / inner), (cuuint32_t)rpc};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = fn(m, es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                    const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(RTP_ECUDA, "reshard: cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return RTP_OK;
+}
+
 // Chunking: rows longer than a chunk are cut into segments (one row per
 // chunk); shorter rows are grouped, up to one row per thread of the block.
 int64_t fill_task(KTask& k, const PlanTask& t, int vec, int es, bool allow_bulk)
@@ -517,6 +674,20 @@ int64_t fill_task(KTask& k, const PlanTask& t, int vec, int es, bool allow_bulk)
     const int64_t bulk_chunk_bytes = ns <= 1 ? kChunkBytes : std::max<int64_t>(4096, kBulkStageBytes / std::max<int64_t>(ns, 1));
     k.bulk = allow_bulk && vec == 16 && ns >= 1 && ns * bulk_chunk_bytes <= kBulkStageBytes &&
              std::min(row_bytes, bulk_chunk_bytes) >= kBulkMinRowBytes;
+    // Shorter rows of a one-outer-dim region whose destination rows (or, for a
+    // copy, source rows) are contiguous: TMA tiles for the strided side.
+    int64_t inner = 0;
+    if (allow_bulk && !k.bulk && vec == 16 && ns >= 1 && t.n_outer == 1 && row_bytes <= 4096 &&
+        (t.dstr[0] == t.cols || (ns == 1 && t.sstr[0] == t.cols)))
+        inner = tile_inner(t.cols, es);
+    const int64_t budget = ns <= 1 ? kChunkBytes : kBulkStageBytes / std::max<int64_t>(ns, 1) - 128;
+    if (inner > 0 && budget >= row_bytes) {
+        k.tile = t.dstr[0] == t.cols ? 1 : 2;
+        k.seg = t.cols;
+        k.nseg = 1;
+        k.rpc = (int32_t)std::min<int64_t>({(int64_t)kBlock, budget / row_bytes, t.rows});
+        return (t.rows + k.rpc - 1) / k.rpc;
+    }
     // Register path: a copy to several destinations writes each chunk several
     // times, so its chunks shrink to keep the bytes a block moves near 2 x 32 KB
     // (4 KB at least).
@@ -537,9 +708,10 @@ int64_t fill_task(KTask& k, const PlanTask& t, int vec, int es, bool allow_bulk)
     return (t.rows + k.rpc - 1) / k.rpc * k.nseg;
 }
 
-// Shared staging a bulk task's chunk needs (0 for the register path).
+// Shared staging a bulk or tile task's chunk needs (0 for the register path).
 int64_t stage_bytes(const KTask& k, int es)
 {
+    if (k.tile) return (int64_t)std::max(1, k.n_src) * tile_slot(k.rpc, k.cols * es);
     if (!k.bulk) return 0;
     return (int64_t)k.n_src * (k.rpc == 1 ? k.seg * es : (int64_t)k.rpc * k.cols * es);
 }
@@ -590,6 +762,19 @@ int launch_boxing(const PP& prm, int grid, int smem, cudaStream_t st, bool any_s
 }
 
 }  // namespace
+
+void* tensor_map_encoder()
+{
+    static void* fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = p;
+    }
+    return fn;
+}
 
 int take_boxing_error(void* stream, uint32_t* code)
 {
@@ -673,10 +858,33 @@ int launch_tasks(int dtype, const std::vector<PlanTask>& tasks, const void* cons
         const int64_t grid64 = blocks_per_sm >= 4 ? std::min<int64_t>(chunks, 0x7fffffff) : std::min<int64_t>(chunks, max_grid);
         const int grid = (int)grid64;
         cudaStream_t st = static_cast<cudaStream_t>(stream);
+        // TMA-tile tasks need their tensor maps in the launch's parameters
+        int n_maps = 0;
+        for (int k = 0; k < nt; ++k)
+            if (prm.tasks[k].tile) n_maps += prm.tasks[k].tile == 1 ? prm.tasks[k].n_src : prm.tasks[k].n_dst;
+        const bool tiles = n_maps > 0 && nt <= kTileTasks && np <= kTilePtrs && n_maps <= kTileMaps;
+        if (!tiles)
+            for (int k = 0; k < nt; ++k) prm.tasks[k].tile = 0;  // their chunks also suit the register path
         int64_t smem = 0;
         for (int k = 0; k < nt; ++k) smem = std::max(smem, stage_bytes(prm.tasks[k], es));
         int st_ok;
-        if (nt <= kSmallTasks && np <= kSmallPtrs) {
+        if (tiles) {
+            static thread_local KParamsTile tp;
+            shrink(prm, nt, np, &tp);
+            int m = 0;
+            for (int k = 0; k < nt; ++k) {
+                KTask& kt = tp.tasks[k];
+                if (!kt.tile) continue;
+                kt.map0 = m;
+                const int n = kt.tile == 1 ? kt.n_src : kt.n_dst;
+                const int base = kt.tile == 1 ? kt.ptr0 : kt.ptr0 + kt.n_src;
+                const int64_t stride = kt.tile == 1 ? kt.sstr[0] : kt.dstr[0];
+                for (int j = 0; j < n; ++j)
+                    if ((st_ok = encode_tile_map(&tp.maps[m++], tp.ptrs[base + j], kt.rows, kt.cols, stride, kt.rpc, es)))
+                        return st_ok;
+            }
+            st_ok = launch_boxing(tp, grid, (int)smem, st, any_sum, sum_op, es);
+        } else if (nt <= kSmallTasks && np <= kSmallPtrs) {
             static thread_local KParamsSmall small;
             st_ok = launch_boxing(shrink(prm, nt, np, &small), grid, (int)smem, st, any_sum, sum_op, es);
         } else if (nt <= kMediumTasks && np <= kMediumPtrs) {

@@ -73,5 +73,7 @@ int launch_tasks(int dtype, const std::vector<PlanTask>& tasks, const void* cons
 int count_launches(const std::vector<PlanTask>& tasks);
 // Reads and clears the boxing kernel's device error word (synchronises `stream`).
 int take_boxing_error(void* stream, uint32_t* code);
+// The driver's cuTensorMapEncodeTiled (a PFN_cuTensorMapEncodeTiled_v12000), or NULL.
+void* tensor_map_encoder();
 
 }  // namespace rtp
