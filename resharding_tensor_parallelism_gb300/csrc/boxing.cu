@@ -90,21 +90,36 @@ __device__ __forceinline__ void bulk_store(void* dst, uint32_t src_smem, uint32_
                  : "memory");
 }
 
-// TMA tiles over a 3D view [rows][mid][inner] of a strided row region; the
-// box is rows-per-chunk x mid x inner, i.e. whole rows, dense in shared memory.
-// Rows past the region are zero-filled on load (and count toward the bytes)
-// and skipped on store.
-__device__ __forceinline__ void tile_load(uint32_t dst_smem, const CUtensorMap* map, int row, uint32_t bar)
+// TMA tiles over a view [outer][rows][mid][inner] of a strided row region (4D;
+// 3D without the outer dim); the box is rows-per-chunk x mid x inner of one
+// outer index, i.e. whole rows, dense in shared memory. Rows past the region
+// are zero-filled on load (and count toward the bytes) and skipped on store.
+template <int R>
+__device__ __forceinline__ void tile_load(uint32_t dst_smem, const CUtensorMap* map, int n_outer, int row, int outer,
+                                          uint32_t bar)
 {
-    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-                 ::"r"(dst_smem), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(row), "r"(bar)
-                 : "memory");
+    const uint64_t m = reinterpret_cast<uint64_t>(map);
+    if (R == 3 || n_outer == 1)
+        asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+                     ::"r"(dst_smem), "l"(m), "r"(0), "r"(0), "r"(row), "r"(bar)
+                     : "memory");
+    else
+        asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+                     ::"r"(dst_smem), "l"(m), "r"(0), "r"(0), "r"(row), "r"(outer), "r"(bar)
+                     : "memory");
 }
-__device__ __forceinline__ void tile_store(const CUtensorMap* map, int row, uint32_t src_smem)
+template <int R>
+__device__ __forceinline__ void tile_store(const CUtensorMap* map, int n_outer, int row, int outer, uint32_t src_smem)
 {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
-                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(row), "r"(src_smem)
-                 : "memory");
+    const uint64_t m = reinterpret_cast<uint64_t>(map);
+    if (R == 3 || n_outer == 1)
+        asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
+                     ::"l"(m), "r"(0), "r"(0), "r"(row), "r"(src_smem)
+                     : "memory");
+    else
+        asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];"
+                     ::"l"(m), "r"(0), "r"(0), "r"(row), "r"(outer), "r"(src_smem)
+                     : "memory");
 }
 
 struct KTask {
@@ -141,8 +156,10 @@ using KParams = KParamsT<kMaxTasks, kMaxPtrs>;
 
 // The form for launches with TMA-tile tasks: the tensor maps of their strided
 // sides travel with the tasks.
+// R = 3: every tile task has one outer dim (3D maps); R = 4: some have two.
 constexpr int kTileTasks = 64, kTilePtrs = 256, kTileMaps = 64;
-struct KParamsTile {
+template <int R>
+struct KParamsTileT {
     int32_t n_tasks;
     int32_t dtype;
     int64_t total_chunks;
@@ -150,8 +167,11 @@ struct KParamsTile {
     const void* ptrs[kTilePtrs];
     CUtensorMap maps[kTileMaps];
     static constexpr int kMaps = kTileMaps;
+    static constexpr int kTileRank = R;
 };
-static_assert(sizeof(KParamsTile) <= 32000, "kernel parameter block too large");
+using KParamsTile3 = KParamsTileT<3>;
+using KParamsTile4 = KParamsTileT<4>;
+static_assert(sizeof(KParamsTile4) <= 32000, "kernel parameter block too large");
 constexpr int kSmallTasks = 16, kSmallPtrs = 128, kMediumTasks = 64, kMediumPtrs = 256;
 using KParamsSmall = KParamsT<kSmallTasks, kSmallPtrs>;
 using KParamsMedium = KParamsT<kMediumTasks, kMediumPtrs>;
@@ -456,17 +476,31 @@ __device__ __host__ __forceinline__ uint32_t tile_slot(int64_t rpc, int64_t row_
     return (uint32_t)((rpc * row_bytes + 127) / 128 * 128);
 }
 
-// A chunk of rows r0 .. r0+nr of a one-outer-dim region, staged through shared
-// memory. tile 1: each source's rows arrive as one TMA tile (its rows are
-// strided), the destination rows are contiguous: a copy is one bulk store per
-// destination, a reduction is added up by all threads and stored with
-// streaming stores. tile 2 (copies): the source rows are contiguous (one bulk
-// load), each destination is written as one TMA tile. False when a wait gave
-// up (the error word is set).
+// Chunk `lc` of a region with one or two outer dims: rows r1 .. r1+nr of the
+// inner row dim at outer index o (o = 0 with one outer dim), staged through
+// shared memory. tile 1: each source's rows arrive as one TMA tile (its rows
+// are strided), the destination rows are contiguous within an outer index: a
+// copy is one bulk store per destination, a reduction is added up by all
+// threads and stored with streaming stores. tile 2 (copies): the source rows
+// are contiguous (one bulk load), each destination is written as one TMA
+// tile. False when a wait gave up (the error word is set).
 template <class PP, bool SUM, int ES, int OP>
-__device__ __forceinline__ bool tile_chunk(const PP& p, const KTask& t, int64_t r0, int nr, uint32_t row_bytes,
-                                           uint8_t* stage, uint32_t bar, uint32_t parity)
+__device__ __forceinline__ bool tile_chunk(const PP& p, const KTask& t, int64_t lc, uint32_t row_bytes, uint8_t* stage,
+                                           uint32_t bar, uint32_t parity)
 {
+    constexpr int R = PP::kTileRank;
+    const int inn = R == 3 ? 0 : t.n_outer - 1;  // the inner row dim
+    const int64_t ext_in = t.ext[inn];
+    int64_t o = 0, r1 = lc * t.rpc;
+    if (R == 4 && inn > 0) {  // chunks never straddle two outer indices
+        const int64_t nb = (ext_in + t.rpc - 1) / t.rpc;
+        o = lc / nb;
+        r1 = (lc - o * nb) * t.rpc;
+    }
+    const int nr = (int)min((int64_t)t.rpc, ext_in - r1);
+    // element offsets of the chunk's first row on the contiguous sides
+    const int64_t soff = (R == 4 && inn > 0 ? o * t.sstr[0] : 0) + r1 * t.sstr[inn];
+    const int64_t doff = (R == 4 && inn > 0 ? o * t.dstr[0] : 0) + r1 * t.dstr[inn];
     const int ns = t.n_src;
     const void* const* sp = p.ptrs + t.ptr0;
     const void* const* dp = sp + ns;
@@ -478,11 +512,12 @@ __device__ __forceinline__ bool tile_chunk(const PP& p, const KTask& t, int64_t 
             asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                          "r"((uint32_t)ns * (uint32_t)t.rpc * row_bytes)
                          : "memory");
-            for (int j = 0; j < ns; ++j) tile_load(st0 + (uint32_t)j * slot, &p.maps[t.map0 + j], (int)r0, bar);
+            for (int j = 0; j < ns; ++j)
+                tile_load<R>(st0 + (uint32_t)j * slot, &p.maps[t.map0 + j], t.n_outer, (int)r1, (int)o, bar);
         } else {
             const uint32_t bytes = (uint32_t)nr * row_bytes;
             asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-            bulk_load(st0, static_cast<const char*>(sp[0]) + r0 * t.sstr[0] * ES, bytes, bar);
+            bulk_load(st0, static_cast<const char*>(sp[0]) + soff * ES, bytes, bar);
         }
     }
     if (!__syncthreads_and(bar_wait(bar, parity) ? 1 : 0)) return false;
@@ -490,10 +525,9 @@ __device__ __forceinline__ bool tile_chunk(const PP& p, const KTask& t, int64_t 
         if (first) {
             for (int k = 0; k < t.n_dst; ++k) {
                 if (t.tile == 1)
-                    bulk_store(static_cast<char*>(const_cast<void*>(dp[k])) + r0 * t.dstr[0] * ES, st0,
-                               (uint32_t)nr * row_bytes);
+                    bulk_store(static_cast<char*>(const_cast<void*>(dp[k])) + doff * ES, st0, (uint32_t)nr * row_bytes);
                 else
-                    tile_store(&p.maps[t.map0 + k], (int)r0, st0);
+                    tile_store<R>(&p.maps[t.map0 + k], t.n_outer, (int)r1, (int)o, st0);
             }
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
@@ -526,8 +560,7 @@ __device__ __forceinline__ bool tile_chunk(const PP& p, const KTask& t, int64_t 
                 else out.h[e] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[e]));
             }
             for (int k = 0; k < t.n_dst; ++k)
-                __stcs(reinterpret_cast<uint4*>(static_cast<char*>(const_cast<void*>(dp[k])) + r0 * t.dstr[0] * ES) + i,
-                       out.v);
+                __stcs(reinterpret_cast<uint4*>(static_cast<char*>(const_cast<void*>(dp[k])) + doff * ES) + i, out.v);
         }
     }
     return true;
@@ -558,7 +591,7 @@ __global__ void __launch_bounds__(kBlock, 4) boxing_kernel(const __grid_constant
         const int64_t len = min(t.seg, t.cols - c0);
         if constexpr (PP::kMaps > 0) {
             if (t.tile) {  // block-uniform
-                if (!tile_chunk<PP, SUM, ES, OP>(p, t, r0, nr, (uint32_t)(t.cols * ES), stage, su32(&bar), parity))
+                if (!tile_chunk<PP, SUM, ES, OP>(p, t, lc, (uint32_t)(t.cols * ES), stage, su32(&bar), parity))
                     return;  // a bulk copy never completed: the error word is set
                 parity ^= 1u;
                 __syncthreads();
@@ -628,18 +661,23 @@ int64_t tile_inner(int64_t cols, int es)
     return 0;
 }
 
-// The tensor map of a tile task's strided side: base `ptr`, `rows` rows of
-// `cols` elements, `stride` elements apart; box: rpc whole rows.
-int encode_tile_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t stride, int64_t rpc, int es)
+// The tensor map of a tile task's strided side: base `ptr`, rows of `cols`
+// elements in n_outer (1 or 2) outer dims of extents ext and element strides
+// str (outer first); box: rpc whole rows of one outer index.
+int encode_tile_map(CUtensorMap* m, const void* ptr, int n_outer, const int32_t* ext, const int64_t* str, int64_t cols,
+                    int64_t rpc, int es)
 {
     auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
     if (!fn) return fail(RTP_ECUDA, "reshard: cuTensorMapEncodeTiled is unavailable");
     const int64_t inner = tile_inner(cols, es);
-    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)(cols / inner), (cuuint64_t)rows};
-    cuuint64_t strides[2] = {(cuuint64_t)(inner * es), (cuuint64_t)(stride * es)};
-    cuuint32_t box[3] = {(cuuint32_t)inner, (cuuint32_t)(cols / inner), (cuuint32_t)rpc};
-    cuuint32_t estr[3] = {1u, 1u, 1u};
-    CUresult r = fn(m, es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+    const int rank = 2 + n_outer;
+    cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)(cols / inner), (cuuint64_t)ext[n_outer - 1],
+                          n_outer == 2 ? (cuuint64_t)ext[0] : 1u};
+    cuuint64_t strides[3] = {(cuuint64_t)(inner * es), (cuuint64_t)(str[n_outer - 1] * es),
+                             n_outer == 2 ? (cuuint64_t)(str[0] * es) : 0u};
+    cuuint32_t box[4] = {(cuuint32_t)inner, (cuuint32_t)(cols / inner), (cuuint32_t)rpc, 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    CUresult r = fn(m, es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
                     const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(RTP_ECUDA, "reshard: cuTensorMapEncodeTiled failed (%d)", (int)r);
@@ -677,16 +715,18 @@ int64_t fill_task(KTask& k, const PlanTask& t, int vec, int es, bool allow_bulk)
     // Shorter rows of a one-outer-dim region whose destination rows (or, for a
     // copy, source rows) are contiguous: TMA tiles for the strided side.
     int64_t inner = 0;
-    if (allow_bulk && !k.bulk && vec == 16 && ns >= 1 && t.n_outer == 1 && row_bytes <= 4096 &&
-        (t.dstr[0] == t.cols || (ns == 1 && t.sstr[0] == t.cols)))
+    const int inn = t.n_outer - 1;  // the inner row dim
+    if (allow_bulk && !k.bulk && vec == 16 && ns >= 1 && (t.n_outer == 1 || t.n_outer == 2) && row_bytes <= 4096 &&
+        (t.dstr[inn] == t.cols || (ns == 1 && t.sstr[inn] == t.cols)))
         inner = tile_inner(t.cols, es);
     const int64_t budget = ns <= 1 ? kChunkBytes : kBulkStageBytes / std::max<int64_t>(ns, 1) - 128;
     if (inner > 0 && budget >= row_bytes) {
-        k.tile = t.dstr[0] == t.cols ? 1 : 2;
+        k.tile = t.dstr[inn] == t.cols ? 1 : 2;
         k.seg = t.cols;
         k.nseg = 1;
-        k.rpc = (int32_t)std::min<int64_t>({(int64_t)kBlock, budget / row_bytes, t.rows});
-        return (t.rows + k.rpc - 1) / k.rpc;
+        k.rpc = (int32_t)std::min<int64_t>({(int64_t)kBlock, budget / row_bytes, t.ext[inn]});
+        const int64_t nb = (t.ext[inn] + k.rpc - 1) / k.rpc;
+        return (inn > 0 ? t.ext[0] : 1) * nb;
     }
     // Register path: a copy to several destinations writes each chunk several
     // times, so its chunks shrink to keep the bytes a block moves near 2 x 32 KB
@@ -868,8 +908,10 @@ int launch_tasks(int dtype, const std::vector<PlanTask>& tasks, const void* cons
         int64_t smem = 0;
         for (int k = 0; k < nt; ++k) smem = std::max(smem, stage_bytes(prm.tasks[k], es));
         int st_ok;
+        bool rank4 = false;
+        for (int k = 0; k < nt; ++k) rank4 |= prm.tasks[k].tile && prm.tasks[k].n_outer == 2;
         if (tiles) {
-            static thread_local KParamsTile tp;
+            static thread_local KParamsTile4 tp;  // the rank-3 form has the same layout
             shrink(prm, nt, np, &tp);
             int m = 0;
             for (int k = 0; k < nt; ++k) {
@@ -878,12 +920,15 @@ int launch_tasks(int dtype, const std::vector<PlanTask>& tasks, const void* cons
                 kt.map0 = m;
                 const int n = kt.tile == 1 ? kt.n_src : kt.n_dst;
                 const int base = kt.tile == 1 ? kt.ptr0 : kt.ptr0 + kt.n_src;
-                const int64_t stride = kt.tile == 1 ? kt.sstr[0] : kt.dstr[0];
+                const int64_t* str = kt.tile == 1 ? kt.sstr : kt.dstr;
                 for (int j = 0; j < n; ++j)
-                    if ((st_ok = encode_tile_map(&tp.maps[m++], tp.ptrs[base + j], kt.rows, kt.cols, stride, kt.rpc, es)))
+                    if ((st_ok = encode_tile_map(&tp.maps[m++], tp.ptrs[base + j], kt.n_outer, kt.ext, str, kt.cols,
+                                                 kt.rpc, es)))
                         return st_ok;
             }
-            st_ok = launch_boxing(tp, grid, (int)smem, st, any_sum, sum_op, es);
+            st_ok = rank4 ? launch_boxing(tp, grid, (int)smem, st, any_sum, sum_op, es)
+                          : launch_boxing(reinterpret_cast<const KParamsTile3&>(tp), grid, (int)smem, st, any_sum,
+                                          sum_op, es);
         } else if (nt <= kSmallTasks && np <= kSmallPtrs) {
             static thread_local KParamsSmall small;
             st_ok = launch_boxing(shrink(prm, nt, np, &small), grid, (int)smem, st, any_sum, sum_op, es);
