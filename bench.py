@@ -663,6 +663,7 @@ PROFILE_CASES = {
     "reshard_f32_p8b": ("reshard", ("1x8", 3, "f32")),
     "reshard_f32_p8s2": ("reshard", ("1x8", 4, "f32")),
     "reshard_f32_s0s2b": ("reshard", ("1x8", 2, "f32")),
+    "reshard_bf16_s2s1": ("reshard", ("1x8", 1, "bf16")),
     "sweep": ("sweep", None),
     "mlp_fused": ("mlp", MLP),
     "domino_fused": ("mlp", DOMINO),

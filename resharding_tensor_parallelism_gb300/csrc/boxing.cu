@@ -439,16 +439,18 @@ __device__ __forceinline__ bool bulk_chunk(const void* const* ptrs, const KTask&
         const int vpr = (int)(rowbytes / 16);
         const int total = nr * vpr;
         const float inv = 1.0f / (float)vpr;
+        const size_t src_stride = (size_t)nr * rowbytes;  // a source's rows are dense in the staging
         const float ident = OP == RED_SUM ? 0.0f : (OP == RED_MIN ? __int_as_float(0x7F800000) : __int_as_float(0xFF800000));
         for (int i = threadIdx.x; i < total; i += kBlock) {
-            int r, v;
-            divmod(i, vpr, inv, r, v);
+            int r = 0, v = i;
+            if (nr > 1) divmod(i, vpr, inv, r, v);  // block-uniform: segments have one row
             float acc[NE];
 #pragma unroll
             for (int e = 0; e < NE; ++e) acc[e] = ident;
+#pragma unroll 8
             for (int j = 0; j < ns; ++j) {
                 Lanes<16> x;
-                x.v = *reinterpret_cast<const uint4*>(stage + (size_t)(j * nr + r) * rowbytes + (size_t)v * 16);
+                x.v = *reinterpret_cast<const uint4*>(stage + (size_t)j * src_stride + (size_t)i * 16);
 #pragma unroll
                 for (int e = 0; e < NE; ++e) {
                     float y;
@@ -542,6 +544,7 @@ __device__ __forceinline__ bool tile_chunk(const PP& p, const KTask& t, int64_t 
             float acc[NE];
 #pragma unroll
             for (int e = 0; e < NE; ++e) acc[e] = ident;
+#pragma unroll 8
             for (int j = 0; j < ns; ++j) {
                 Lanes<16> x;
                 x.v = *reinterpret_cast<const uint4*>(stage + (size_t)j * slot + (size_t)i * 16);
@@ -589,6 +592,17 @@ __global__ void __launch_bounds__(kBlock, 4) boxing_kernel(const __grid_constant
         const int64_t r0 = rb * t.rpc;
         const int nr = (int)min((int64_t)t.rpc, t.rows - r0);
         const int64_t len = min(t.seg, t.cols - c0);
+        if (t.bulk && nr == 1) {  // one segment: every thread derives its offsets, no row table
+            int64_t so, dof;
+            row_offsets(t, r0, so, dof);
+            so += c0;
+            dof += c0;
+            if (!bulk_chunk<SUM, ES, OP>(p.ptrs, t, 1, (uint32_t)(len * ES), &so, &dof, stage, su32(&bar), parity))
+                return;  // a bulk copy never completed: the error word is set
+            parity ^= 1u;
+            __syncthreads();
+            continue;
+        }
         if constexpr (PP::kMaps > 0) {
             if (t.tile) {  // block-uniform
                 if (!tile_chunk<PP, SUM, ES, OP>(p, t, lc, (uint32_t)(t.cols * ES), stage, su32(&bar), parity))
