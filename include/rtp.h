@@ -406,19 +406,24 @@ int rtp_tp_mlp_noalloc(int P, int64_t M, int64_t K, int64_t F, int64_t N, const 
 int rtp_device_error(rtp_stream stream, uint32_t* code);
 
 /*
- * Self-test of the bounded waits that rtp_tp_mlp's kernels use (no page
- * counterpart: it checks this library's failure detection without a fault).
- * One block, two waiting threads, one mbarrier that nothing completes: the
- * first waiter gives up after limit_ns of %globaltimer, records code 5 in the
- * device word that rtp_device_error reads and raises the block's abort flag;
- * the second waiter (own limit 4 x limit_ns) leaves on that flag. The kernel
+ * Self-test of the bounded waits of this library's kernels (no page
+ * counterpart: it checks failure detection without a fault). A wait on an
+ * mbarrier that nothing completes gives up after limit_ns of %globaltimer and
+ * records a code in the device word that rtp_device_error reads; the kernel
  * then returns normally and the context stays usable.
+ *   kernel    0: the wait of rtp_tp_mlp's tensor-core kernel. One block, two
+ *             waiting threads: the first gives up after limit_ns, records code
+ *             5 and raises the block's abort flag; the second (own limit
+ *             4 x limit_ns) leaves on that flag. out[w] = 1 when waiter w gave
+ *             up (both, when the test works).
+ *             1: the wait of the resharding kernel's staged copies. One block
+ *             of 64 threads waits for 16 announced bytes that never arrive; the
+ *             waits give up, record code 16 and the block stops: out[0] = 1.
  *   limit_ns  in [1e6, 1e9] (1 ms to 1 s), else RTP_EINVAL
- *   out       device pointer to 2 uint32 (16-byte aligned, caller-owned):
- *             out[w] = 1 when waiter w gave up (both, when the test works)
+ *   out       device pointer to 2 uint32 (16-byte aligned, caller-owned)
  * Asynchronous on `stream`.
  */
-int rtp_wait_selftest(unsigned long long limit_ns, uint32_t* out, rtp_stream stream);
+int rtp_wait_selftest(int kernel, unsigned long long limit_ns, uint32_t* out, rtp_stream stream);
 
 /* Text of the last error on the calling thread ("" if none). */
 const char* rtp_last_error(void);

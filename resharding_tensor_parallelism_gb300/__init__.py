@@ -96,7 +96,7 @@ def _load():
                                     P(ctypes.c_double), i32p],
         "rtp_infer_broadcast": [c_int, i32p, P(i64p), P(Spec), P(c_int), i64p, P(Spec)],
         "rtp_device_error": [vp, u32p],
-        "rtp_wait_selftest": [ctypes.c_ulonglong, vp, vp],
+        "rtp_wait_selftest": [c_int, ctypes.c_ulonglong, vp, vp],
         "rtp_tp_mlp_sp": [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vpp, vpp, vpp, vpp,
                           vpp, vp],
         "rtp_tp_mlp_noalloc": [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vpp, vpp,
@@ -501,15 +501,16 @@ def device_error(stream=None) -> int:
     return code.value
 
 
-def wait_selftest(limit_ns: int, out=None, stream=None):
-    """Runs the bounded-wait self-test kernel (a wait on a barrier that nothing
-    completes, given up after limit_ns). Returns the 2-element uint32 device
-    tensor of outcomes (1 = that waiter gave up)."""
+def wait_selftest(limit_ns: int, out=None, stream=None, kernel: int = 0):
+    """Runs a bounded-wait self-test kernel (a wait on a barrier that nothing
+    completes, given up after limit_ns): kernel 0 the tensor-core kernel's
+    wait, 1 the resharding kernel's. Returns the uint32 device tensor of
+    outcomes (1 = that waiter gave up)."""
     torch = _torch()
     if out is None:
         out = torch.zeros(4, dtype=torch.int32, device="cuda")
     _check_cuda([out], "wait_selftest")
-    _check(_load().rtp_wait_selftest(int(limit_ns), out.data_ptr(), _stream_ptr(stream)))
+    _check(_load().rtp_wait_selftest(int(kernel), int(limit_ns), out.data_ptr(), _stream_ptr(stream)))
     return out
 
 

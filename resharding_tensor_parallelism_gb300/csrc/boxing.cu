@@ -59,7 +59,7 @@ __device__ __forceinline__ uint64_t now_ns()
 
 // Bounded wait for phase `parity` of an mbarrier; false (and the error word
 // set) when it does not complete within kBulkWaitNs.
-__device__ __noinline__ bool bar_wait(uint32_t bar, uint32_t parity)
+__device__ __noinline__ bool bar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns = kBulkWaitNs)
 {
     const uint64_t t0 = now_ns();
     for (uint32_t i = 0;; ++i) {
@@ -69,11 +69,29 @@ __device__ __noinline__ bool bar_wait(uint32_t bar, uint32_t parity)
                      : "r"(bar), "r"(parity)
                      : "memory");
         if (done) return true;
-        if ((i & 15u) == 15u && now_ns() - t0 > kBulkWaitNs) {
+        if ((i & 15u) == 15u && now_ns() - t0 > limit_ns) {
             atomicCAS(&g_box_error, 0u, kErrBulkWait);
             return false;
         }
     }
+}
+
+// Self-test of the bounded wait above: every thread of one block waits (as a
+// staged chunk does) on an mbarrier whose transaction bytes never arrive; the
+// waits give up after limit_ns, record kErrBulkWait, and the block agrees to
+// stop. out[0] = 1 when the block stopped on the failed wait.
+__global__ void bulk_wait_selftest_kernel(unsigned long long limit_ns, uint32_t* out)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bar)) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        // 16 bytes announced, none sent: the phase cannot complete
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(&bar)), "r"(16u) : "memory");
+    }
+    __syncthreads();
+    const int ok = __syncthreads_and(bar_wait(su32(&bar), 0, limit_ns) ? 1 : 0);
+    if (threadIdx.x == 0) out[0] = ok ? 0u : 1u;
 }
 
 // Bulk copies (cp.async.bulk, no tensor map): 16-byte aligned addresses, sizes
@@ -828,6 +846,14 @@ void* tensor_map_encoder()
             fn = p;
     }
     return fn;
+}
+
+int bulk_wait_selftest(unsigned long long limit_ns, uint32_t* out, void* stream)
+{
+    bulk_wait_selftest_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns, out);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(RTP_ECUDA, "rtp_wait_selftest: launch failed: %s", cudaGetErrorString(e));
+    return RTP_OK;
 }
 
 int take_boxing_error(void* stream, uint32_t* code)

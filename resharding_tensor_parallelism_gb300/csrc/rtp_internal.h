@@ -73,6 +73,9 @@ int launch_tasks(int dtype, const std::vector<PlanTask>& tasks, const void* cons
 int count_launches(const std::vector<PlanTask>& tasks);
 // Reads and clears the boxing kernel's device error word (synchronises `stream`).
 int take_boxing_error(void* stream, uint32_t* code);
+// Launches the resharding kernel's bounded-wait self-test (a wait that never
+// completes, given up after limit_ns); out[0] = 1 when the block stopped on it.
+int bulk_wait_selftest(unsigned long long limit_ns, uint32_t* out, void* stream);
 // The driver's cuTensorMapEncodeTiled (a PFN_cuTensorMapEncodeTiled_v12000), or NULL.
 void* tensor_map_encoder();
 

@@ -1109,12 +1109,14 @@ int rtp_tp_mlp_sp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void*
     return launch_gemm(g2, stream);
 }
 
-int rtp_wait_selftest(unsigned long long limit_ns, uint32_t* out, rtp_stream stream)
+int rtp_wait_selftest(int kernel, unsigned long long limit_ns, uint32_t* out, rtp_stream stream)
 {
+    if (kernel != 0 && kernel != 1) return fail(RTP_EINVAL, "rtp_wait_selftest: kernel %d not 0 or 1", kernel);
     if (!out) return fail(RTP_EINVAL, "rtp_wait_selftest: NULL out");
     if (limit_ns < 1000000ull || limit_ns > 1000000000ull)
         return fail(RTP_EINVAL, "rtp_wait_selftest: limit %llu ns outside [1 ms, 1 s]", limit_ns);
     if (!aligned16(out)) return fail(RTP_EINVAL, "rtp_wait_selftest: out must be 16-byte aligned");
+    if (kernel == 1) return bulk_wait_selftest(limit_ns, out, stream);
     wait_selftest_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns, out);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(RTP_ECUDA, "rtp_wait_selftest: launch failed: %s", cudaGetErrorString(e));

@@ -59,9 +59,11 @@ def test_version_and_errors():
         rtp.infer_reshape([2, 3], [0, -1], [7], [2])
     # the wait self-test checks its limit on the host, before any launch
     lib = rtp.lib()
-    for bad in (0, 999_999, 1_000_000_001):
-        assert lib.rtp_wait_selftest(bad, 16, None) == -1
-    assert lib.rtp_wait_selftest(5_000_000, None, None) == -1
+    for kernel in (0, 1):
+        for bad in (0, 999_999, 1_000_000_001):
+            assert lib.rtp_wait_selftest(kernel, bad, 16, None) == -1
+        assert lib.rtp_wait_selftest(kernel, 5_000_000, None, None) == -1
+    assert lib.rtp_wait_selftest(2, 5_000_000, 16, None) == -1
 
 
 def _same_layout(spec, lay, shape):

@@ -56,6 +56,35 @@ def test_context_usable_after_the_timeout():
     assert rtp.device_error() == 0
 
 
+@pytest.mark.parametrize("limit_ms", [5, 50])
+def test_staged_copy_wait_gives_up_and_reports(limit_ms):
+    """The resharding kernel's bounded wait (staged bulk copies): 16 bytes
+    announced on the block's mbarrier never arrive; the wait gives up, records
+    code 16, and the block stops."""
+    assert rtp.device_error() == 0
+    out = torch.zeros(4, dtype=torch.int32, device="cuda")
+    rtp.wait_selftest(1_000_000, out=out, kernel=1)  # first launch loads the kernel
+    torch.cuda.synchronize()
+    assert rtp.device_error() == 16
+    out.zero_()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    rtp.wait_selftest(limit_ms * 1_000_000, out=out, kernel=1)
+    e1.record()
+    torch.cuda.synchronize()
+    assert int(out[0]) == 1
+    assert rtp.device_error() == 16
+    assert rtp.device_error() == 0
+    assert limit_ms <= e0.elapsed_time(e1) < 2.5 * limit_ms + 2
+    # a reshard right after runs correctly
+    x = torch.arange(64 * 1024, dtype=torch.float32, device="cuda").view(64, 1024)
+    s0, s1 = rtp.spec_nd_sbp((4,), (("S", 0),)), rtp.spec_nd_sbp((4,), (("S", 1),))
+    back = rtp.reshard(rtp.reshard(rtp.shard(x, s0), x.shape, s0, s1), x.shape, s1, s0)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(back, 0), x)
+    assert rtp.device_error() == 0
+
+
 def test_limit_outside_range_is_rejected():
     out = torch.zeros(4, dtype=torch.int32, device="cuda")
     for bad in (0, 999_999, 1_000_000_001):
