@@ -833,6 +833,28 @@ int launch_boxing(const PP& prm, int grid, int smem, cudaStream_t st, bool any_s
     return launch_one<PP, true, 2, RED_SUM>(prm, grid, smem, st);
 }
 
+// Fills a tile-form parameter block from the full one, encodes the tensor maps
+// of the tile tasks' strided sides, and launches.
+template <class PP>
+int launch_tiles(const KParams& prm, int nt, int np, int es, PP* tp, int grid, int smem, cudaStream_t st, bool any_sum,
+                 int sum_op)
+{
+    shrink(prm, nt, np, tp);
+    int m = 0, rc;
+    for (int k = 0; k < nt; ++k) {
+        KTask& kt = tp->tasks[k];
+        if (!kt.tile) continue;
+        kt.map0 = m;
+        const int n = kt.tile == 1 ? kt.n_src : kt.n_dst;
+        const int base = kt.tile == 1 ? kt.ptr0 : kt.ptr0 + kt.n_src;
+        const int64_t* str = kt.tile == 1 ? kt.sstr : kt.dstr;
+        for (int j = 0; j < n; ++j)
+            if ((rc = encode_tile_map(&tp->maps[m++], tp->ptrs[base + j], kt.n_outer, kt.ext, str, kt.cols, kt.rpc, es)))
+                return rc;
+    }
+    return launch_boxing(*tp, grid, smem, st, any_sum, sum_op, es);
+}
+
 }  // namespace
 
 void* tensor_map_encoder()
@@ -951,24 +973,13 @@ int launch_tasks(int dtype, const std::vector<PlanTask>& tasks, const void* cons
         bool rank4 = false;
         for (int k = 0; k < nt; ++k) rank4 |= prm.tasks[k].tile && prm.tasks[k].n_outer == 2;
         if (tiles) {
-            static thread_local KParamsTile4 tp;  // the rank-3 form has the same layout
-            shrink(prm, nt, np, &tp);
-            int m = 0;
-            for (int k = 0; k < nt; ++k) {
-                KTask& kt = tp.tasks[k];
-                if (!kt.tile) continue;
-                kt.map0 = m;
-                const int n = kt.tile == 1 ? kt.n_src : kt.n_dst;
-                const int base = kt.tile == 1 ? kt.ptr0 : kt.ptr0 + kt.n_src;
-                const int64_t* str = kt.tile == 1 ? kt.sstr : kt.dstr;
-                for (int j = 0; j < n; ++j)
-                    if ((st_ok = encode_tile_map(&tp.maps[m++], tp.ptrs[base + j], kt.n_outer, kt.ext, str, kt.cols,
-                                                 kt.rpc, es)))
-                        return st_ok;
+            if (rank4) {
+                static thread_local KParamsTile4 tp4;
+                st_ok = launch_tiles(prm, nt, np, es, &tp4, grid, (int)smem, st, any_sum, sum_op);
+            } else {
+                static thread_local KParamsTile3 tp3;
+                st_ok = launch_tiles(prm, nt, np, es, &tp3, grid, (int)smem, st, any_sum, sum_op);
             }
-            st_ok = rank4 ? launch_boxing(tp, grid, (int)smem, st, any_sum, sum_op, es)
-                          : launch_boxing(reinterpret_cast<const KParamsTile3&>(tp), grid, (int)smem, st, any_sum,
-                                          sum_op, es);
         } else if (nt <= kSmallTasks && np <= kSmallPtrs) {
             static thread_local KParamsSmall small;
             st_ok = launch_boxing(shrink(prm, nt, np, &small), grid, (int)smem, st, any_sum, sum_op, es);
