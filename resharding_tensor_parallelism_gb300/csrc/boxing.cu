@@ -2,26 +2,37 @@
 // fills) for shard() and reshard().
 //
 // Design for GB300 (HBM-bound, no tensor-core work):
-//   * the task table travels in the kernel parameters (up to ~26 KB per
-//     launch, __grid_constant__), so no device memory is allocated or copied
-//     per call and the launch can be captured in a CUDA graph;
-//   * blocks of 256 threads (4 resident per SM) take ~32 KB chunks: a chunk is
-//     a segment of one long row or a group of up to 256 short rows (smaller
-//     chunks for copies to several destinations); the block stages each row's
-//     offsets in shared memory once and spreads the (row, vector) items over
-//     its threads, so every thread keeps several loads in flight even for 1 KB
-//     rows. Alone on the GPU the grid has one block per chunk; beside another
+//   * the task table travels in the kernel parameters (3 to 26 KB per launch,
+//     __grid_constant__, sized to the launch's tasks), so no device memory is
+//     allocated or copied per call and the launch can be captured in a CUDA
+//     graph;
+//   * blocks of 256 threads (up to 4 resident per SM) each take one chunk of
+//     a task. Alone on the GPU the grid has one block per chunk; beside another
 //     kernel it is a persistent grid of a few blocks per SM;
-//   * loads and stores are 16-byte vectors whenever every pointer, stride and
-//     run length allows it (else 8, 4 or 2 bytes), with streaming cache hints
-//     since every byte is touched once;
+//   * three forms, chosen per task on the host:
+//       - bulk staging: runs of 4 KB or more are loaded into shared memory
+//         with cp.async.bulk (the TMA engine, no tensor map) and stored from
+//         there, or summed from there;
+//       - TMA tiles: shorter rows whose one side is contiguous move the strided
+//         side as one cp.async.bulk.tensor tile of a 3D / 4D tensor map per
+//         source (or destination) and chunk (the axis-changing S(i) -> S(j)
+//         moves, the P -> S reduce-scatter);
+//       - registers: every other task; the block stages each row's offsets in
+//         shared memory and spreads (row, vector) items over its threads, so
+//         every thread keeps several loads in flight even for short rows;
+//   * 16-byte vectors whenever every pointer, stride and run length allows it
+//     (else 8, 4 or 2 bytes), streaming cache hints since every byte is
+//     touched once;
 //   * a task with several destinations (broadcast pieces) reads its source
-//     once and writes every destination from registers;
+//     once and writes every destination from the same registers or shared
+//     memory;
 //   * a task with several sources (partial sums) adds them in float32 in a
 //     fixed order (partial coordinates row-major) and rounds once; partial
 //     min / max members combine with fminf / fmaxf (exact);
 //   * a task with no source fills its destinations with the identity of the
-//     destination's partial reduction (0, +inf or -inf).
+//     destination's partial reduction (0, +inf or -inf);
+//   * every wait on a bulk or tile copy is bounded (about 2 s); a wait that
+//     gives up records a code in a device word and the block returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
