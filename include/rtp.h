@@ -185,6 +185,19 @@ int rtp_reshard_cost(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_
                      int64_t* bytes_read, int64_t* bytes_written, int32_t* n_tasks, int32_t* n_launches);
 
 /*
+ * How rtp_reshard would run the same request: counts[4] receives the number of
+ * planned tasks in each form of the resharding kernel: [0] registers
+ * (16-byte or narrower vectors), [1] bulk staging through shared memory (runs
+ * of 4 KB or more), [2] TMA tiles of a 3D tensor map, [3] TMA tiles of a 4D
+ * tensor map (short strided rows). Host only; assumes 256-byte aligned rank
+ * buffers (as cudaMalloc returns) and the kernel alone on the GPU (beside
+ * another kernel every task takes the register form). Same errors as
+ * rtp_reshard_cost.
+ */
+int rtp_reshard_forms(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_spec* src, const rtp_spec* dst,
+                      int32_t* counts);
+
+/*
  * infer_spmd(einsum, dims_mappings) (Paddle "SPMD rules" note, steps 1-3:
  * einsum notation, ShardingMergeForTensors, GetDimsMappingForAxes; ONNX
  * sharding formalism, reduction operators). Host only.

@@ -90,6 +90,7 @@ def _load():
         "rtp_shard": [c_int, c_int, i64p, vp, P(Spec), vpp, vp],
         "rtp_reshard": [c_int, c_int, i64p, vpp, P(Spec), vpp, P(Spec), vp],
         "rtp_reshard_cost": [c_int, c_int, i64p, P(Spec), P(Spec), i64p, i64p, i32p, i32p],
+        "rtp_reshard_forms": [c_int, c_int, i64p, P(Spec), P(Spec), i32p],
         "rtp_infer_spmd": [ctypes.c_char_p, c_int, P(i32p), c_int, i32p, u32p, u32p, P(i32p)],
         "rtp_infer_reshape": [c_int, i64p, i32p, c_int, i64p, c_int, i64p, i32p, i32p],
         "rtp_infer_sbp_signature": [c_int, c_int, i64p, c_int, c_int, i32p, i32p, i32p, i32p, i32p, i32p,
@@ -280,6 +281,14 @@ def reshard(pieces, shape: Sequence[int], src: Spec, dst: Spec, out=None, stream
                                ctypes.byref(src), _ptrs([o.data_ptr() for o in outs]), ctypes.byref(dst),
                                _stream_ptr(stream)))
     return outs
+
+
+def reshard_forms(dtype_code: int, shape: Sequence[int], src: Spec, dst: Spec):
+    """Tasks per kernel form a reshard would use: (registers, bulk staging,
+    TMA tiles 3D, TMA tiles 4D), for 256-byte aligned buffers."""
+    c = (ctypes.c_int32 * 4)()
+    _check(_load().rtp_reshard_forms(dtype_code, len(shape), _i64(shape), ctypes.byref(src), ctypes.byref(dst), c))
+    return tuple(c)
 
 
 def reshard_cost(dtype_code: int, shape: Sequence[int], src: Spec, dst: Spec):

@@ -889,6 +889,35 @@ int bulk_wait_selftest(unsigned long long limit_ns, uint32_t* out, void* stream)
     return RTP_OK;
 }
 
+int classify_tasks(int dtype, const std::vector<PlanTask>& tasks, int32_t* counts)
+{
+    const int es = dtype == RTP_F32 ? 4 : 2;
+    for (int f = 0; f < 4; ++f) counts[f] = 0;
+    // buffers as cudaMalloc returns them: 256-byte aligned bases
+    std::vector<const void*> fake(RTP_MAX_RANKS, reinterpret_cast<const void*>(uintptr_t(256)));
+    size_t i = 0;
+    while (i < tasks.size()) {
+        KTask ks[kMaxTasks];
+        int nt = 0, np = 0, n_maps = 0;
+        for (; i < tasks.size() && nt < kMaxTasks; ++i) {
+            const PlanTask& t = tasks[i];
+            const int need = (int)(t.src.size() + t.dst.size());
+            if (np + need > kMaxPtrs) break;
+            fill_task(ks[nt], t, pick_vec(t, fake.data(), const_cast<void* const*>(fake.data()), es), es, true);
+            if (ks[nt].tile) n_maps += ks[nt].tile == 1 ? ks[nt].n_src : ks[nt].n_dst;
+            np += need;
+            ++nt;
+        }
+        const bool tiles = n_maps > 0 && nt <= kTileTasks && np <= kTilePtrs && n_maps <= kTileMaps;
+        for (int k = 0; k < nt; ++k) {
+            if (ks[k].tile && tiles) ++counts[ks[k].n_outer == 2 ? 3 : 2];
+            else if (ks[k].bulk) ++counts[1];
+            else ++counts[0];
+        }
+    }
+    return RTP_OK;
+}
+
 int take_boxing_error(void* stream, uint32_t* code)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -261,4 +261,18 @@ int rtp_reshard_cost(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_
     return RTP_OK;
 }
 
+int rtp_reshard_forms(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_spec* src, const rtp_spec* dst,
+                      int32_t* counts)
+{
+    const char* fn = "rtp_reshard_forms";
+    int st = check_common(fn, dtype, ndim, shape);
+    if (st) return st;
+    if (!src || !dst || !counts) return fail(RTP_EINVAL, "%s: NULL argument", fn);
+    if ((st = check_spec(ndim, *src, "rtp_reshard_forms (src)"))) return st;
+    if ((st = check_spec(ndim, *dst, "rtp_reshard_forms (dst)"))) return st;
+    std::vector<PlanTask> tasks;
+    if ((st = plan_reshard(ndim, shape, *src, *dst, &tasks))) return st;
+    return classify_tasks(dtype, tasks, counts);
+}
+
 }  // extern "C"

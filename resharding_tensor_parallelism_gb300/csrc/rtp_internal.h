@@ -71,6 +71,10 @@ int launch_tasks(int dtype, const std::vector<PlanTask>& tasks, const void* cons
                  void* stream, int* n_launches_out, int blocks_per_sm = 4);
 // Number of launches the tasks need (host only).
 int count_launches(const std::vector<PlanTask>& tasks);
+// How many of the tasks a reshard would run in each form of the boxing kernel:
+// counts[0] registers, [1] bulk staging, [2] TMA tiles (3D), [3] TMA tiles (4D),
+// for 256-byte aligned buffers and the kernel alone on the GPU (host only).
+int classify_tasks(int dtype, const std::vector<PlanTask>& tasks, int32_t* counts);
 // Reads and clears the boxing kernel's device error word (synchronises `stream`).
 int take_boxing_error(void* stream, uint32_t* code);
 // Launches the resharding kernel's bounded-wait self-test (a wait that never

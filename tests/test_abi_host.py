@@ -268,3 +268,23 @@ def test_infer_broadcast_page_examples(golden_dir):
     with pytest.raises(rtp.RtpError) as e:
         rtp.infer_broadcast([(4, 3), (4, 5)], [rtp.spec_nd_sbp((2,), ("B",))] * 2)
     assert e.value.status == -2
+
+
+def test_forms_cover_the_sweep():
+    """The resharding sweep needs no register form on 256-byte aligned buffers:
+    long runs are staged by bulk copies, short strided rows move as TMA tiles
+    (3D and 4D tensor maps)."""
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    seen = [0, 0, 0, 0]
+    for mesh in ("1x8", "2x4"):
+        for _, src, dst, _ in bench.sweep_specs(rtp, mesh):
+            for code in (rtp.F32, rtp.BF16):
+                c = rtp.reshard_forms(code, bench.SWEEP_SHAPE, src, dst)
+                assert c[0] == 0 and sum(c) == rtp.reshard_cost(code, bench.SWEEP_SHAPE, src, dst)[2]
+                seen = [a + b for a, b in zip(seen, c)]
+    assert seen[1] > 0 and seen[2] > 0 and seen[3] > 0
+    # narrow rows and 8-byte vectors take the register form
+    s, d = rtp.spec_nd_sbp((4,), (("S", 0),)), rtp.spec_nd_sbp((4,), (("S", 1),))
+    assert rtp.reshard_forms(rtp.F32, (64, 36), s, d)[0] > 0
