@@ -394,6 +394,7 @@ def run_ours(args, rank, world, local_rank):
                                         "frac_bf16": round(MLP_FLOPS / (sp_ms * 1e-3) / 1e12 / bf16_peak, 4)},
         "f3_infer_sbp_signature": {"us_per_call": host["sbp_signature_us"], "where": "host"},
         "f3_onnx_broadcast_checker": {"us_per_call": host["infer_broadcast_us"], "where": "host"},
+        "a2_small_reshard_latency": small_reshard_latency(rtp, torch, dev),
         "f1_tp_mlp_backward": {"ms": round(bwd_ms, 4), "tflops": round(2 * MLP_FLOPS / (bwd_ms * 1e-3) / 1e12, 1),
                                "frac_bf16": round(2 * MLP_FLOPS / (bwd_ms * 1e-3) / 1e12 / bf16_peak, 4),
                                "dX_sum": "fused in the GEMM",
@@ -456,6 +457,47 @@ def run_ours(args, rank, world, local_rank):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def small_reshard_latency(rtp, torch, dev, n: int = 100):
+    """Latency of a small reshard (a [8,64,512] float32 activation, S(0) -> S(2)
+    on the 1x8 mesh, 1 MiB) issued back to back: direct calls (host planning
+    and launch on every call) against the same calls replayed from a CUDA
+    graph; microseconds per call."""
+    shape = (8, 64, 512)
+    s0, s2 = rtp.spec_nd_sbp((8,), (("S", 0),)), rtp.spec_nd_sbp((8,), (("S", 2),))
+    src = rtp.shard(torch.randn(shape, device=dev), s0)
+    out = [torch.empty(rtp.shard_shape(shape, s2, r), device=dev) for r in range(8)]
+    stream = torch.cuda.Stream(device=dev)
+    E = lambda: torch.cuda.Event(enable_timing=True)
+
+    def calls():
+        for _ in range(n):
+            rtp.reshard(src, shape, s0, s2, out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        calls()
+    torch.cuda.synchronize()
+    e0, e1 = E(), E()
+    e0.record(stream)
+    calls()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    direct = e0.elapsed_time(e1) * 1e3 / n
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        calls()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = E(), E()
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    replay = e0.elapsed_time(e1) * 1e3 / n
+    return {"us_per_call_direct": round(direct, 2), "us_per_call_graph": round(replay, 2),
+            "shape": "[8,64,512] f32, S(0)->S(2) on 1x8, calls back to back"}
 
 
 def host_inference_timings(rtp, reps: int = 2000):
