@@ -40,6 +40,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <unordered_map>
 
 #include "rtp_internal.h"
 
@@ -704,6 +705,36 @@ int64_t tile_inner(int64_t cols, int es)
     return 0;
 }
 
+// Everything a tile map is encoded from (the rank follows from dims[3]).
+struct MapKey {
+    uintptr_t ptr;
+    uint64_t dims[4];
+    uint64_t strides[3];
+    uint32_t rpc;
+    int es;
+    bool operator==(const MapKey& o) const
+    {
+        return ptr == o.ptr && std::memcmp(dims, o.dims, sizeof dims) == 0 &&
+               std::memcmp(strides, o.strides, sizeof strides) == 0 && rpc == o.rpc && es == o.es;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey& k) const
+    {
+        uint64_t h = k.ptr * 0x9E3779B97F4A7C15ull;
+        for (uint64_t v : k.dims) h = (h ^ v) * 0x100000001B3ull;
+        for (uint64_t v : k.strides) h = (h ^ v) * 0x100000001B3ull;
+        return (size_t)(h ^ ((uint64_t)k.rpc << 3) ^ (uint64_t)k.es);
+    }
+};
+
+// Per thread, like the rest of the launch state (no locking).
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash>& map_cache()
+{
+    static thread_local std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
+    return cache;
+}
+
 // The tensor map of a tile task's strided side: base `ptr`, rows of `cols`
 // elements in n_outer (1 or 2) outer dims of extents ext and element strides
 // str (outer first); box: rpc whole rows of one outer index.
@@ -720,10 +751,22 @@ int encode_tile_map(CUtensorMap* m, const void* ptr, int n_outer, const int32_t*
                              n_outer == 2 ? (cuuint64_t)(str[0] * es) : 0u};
     cuuint32_t box[4] = {(cuuint32_t)inner, (cuuint32_t)(cols / inner), (cuuint32_t)rpc, 1u};
     cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    // Repeated reshards of the same buffers reuse their maps (encoding one takes
+    // a fraction of a microsecond; a 64-task launch needs 64).
+    MapKey key{reinterpret_cast<uintptr_t>(ptr), {dims[0], dims[1], dims[2], dims[3]}, {strides[0], strides[1], strides[2]},
+               (uint32_t)rpc, es};
+    auto& cache = map_cache();
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+        *m = it->second;
+        return RTP_OK;
+    }
     CUresult r = fn(m, es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
                     const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(RTP_ECUDA, "reshard: cuTensorMapEncodeTiled failed (%d)", (int)r);
+    if (cache.size() >= 4096) cache.clear();
+    cache.emplace(key, *m);
     return RTP_OK;
 }
 
