@@ -280,6 +280,9 @@ def run_ours(args, rank, world, local_rank):
     def run_serial():
         rtp.tp_mlp(dom["X"], dom["A"], dom["B"], Y=dom["Y"], partials=dom["parts"], Z=dom["Z"], mode=0, chunks=1)
 
+    def run_dom_fused():
+        rtp.tp_mlp(dom["X"], dom["A"], dom["B"], Y=dom["Y"], Z=dom["Z"], mode=1)
+
     def run_reduce():
         rtp.reshard(dom["parts"], dom_shape, dom_red_src, dom_red_dst, out=[dom["Z"]])
 
@@ -299,9 +302,9 @@ def run_ours(args, rank, world, local_rank):
     shard_ops = [(label, (lambda T=T, sp=sp, o=o: rtp.shard(T, sp, out=o)), nbytes, nl)
                  for (label, T, sp, o, nbytes, nl) in shards]
     launches_per_step = (sum(x[3] for x in ops) + sum(x[3] for x in shard_ops) +
-                         2 + 2 + 6 + 3 + 1 + 2 + 4 + 5)
-    # mlp 2, sequence parallel 2, domino 2x3, serial 3, reduce 1, training forward 2, backward 4, backward with
-    # the separate, overlapped dX sum 5
+                         2 + 2 + 6 + 3 + 2 + 1 + 2 + 4 + 5)
+    # mlp 2, sequence parallel 2, domino 2x3, serial 3, fused on the Domino shape 2, reduce 1, training forward 2,
+    # backward 4, backward with the separate, overlapped dX sum 5
     E = lambda: torch.cuda.Event(enable_timing=True)
 
     def step(record):
@@ -320,7 +323,7 @@ def run_ours(args, rank, world, local_rank):
             e1.record()
             record.append(("reshard", label, e0, e1, nbytes))
         for kind, fn in (("mlp", run_mlp), ("sp", run_sp), ("domino", run_domino), ("serial", run_serial),
-                         ("reduce", run_reduce), ("train_fwd", run_train_fwd), ("bwd", run_bwd),
+                         ("dom_fused", run_dom_fused), ("reduce", run_reduce), ("train_fwd", run_train_fwd), ("bwd", run_bwd),
                          ("bwd_overlap", run_bwd_overlap)):
             flush.zero_()
             e0, e1 = E(), E()
@@ -359,6 +362,7 @@ def run_ours(args, rank, world, local_rank):
     mlp_ms = per[("mlp", "mlp")][0]
     dom_ms = per[("domino", "domino")][0] / args.steps
     ser_ms = per[("serial", "serial")][0] / args.steps
+    dfu_ms = per[("dom_fused", "dom_fused")][0] / args.steps
     red_ms = per[("reduce", "reduce")][0] / args.steps
     sp_ms = per[("sp", "sp")][0] / args.steps
     tf_ms = per[("train_fwd", "train_fwd")][0] / args.steps
@@ -390,6 +394,8 @@ def run_ours(args, rank, world, local_rank):
                                "shape": "8 float32 partials [4096,8192] -> Z"},
         "a6_a7_separate_schedule": {"ms": round(ser_ms, 4), "tflops": round(DOMINO_FLOPS / (ser_ms * 1e-3) / 1e12, 1)},
         "a8_domino": {"ms": round(dom_ms, 4), "hiding": round((ser_ms - dom_ms) / red_ms, 3) if red_ms > 0 else None},
+        "a5_a7_fused_domino_shape": {"ms": round(dfu_ms, 4), "tflops": round(DOMINO_FLOPS / (dfu_ms * 1e-3) / 1e12, 1),
+                                     "frac_bf16": round(DOMINO_FLOPS / (dfu_ms * 1e-3) / 1e12 / bf16_peak, 4)},
         "f2_tp_mlp_sequence_parallel": {"ms": round(sp_ms, 4), "tflops": round(MLP_FLOPS / (sp_ms * 1e-3) / 1e12, 1),
                                         "frac_bf16": round(MLP_FLOPS / (sp_ms * 1e-3) / 1e12 / bf16_peak, 4)},
         "f3_infer_sbp_signature": {"us_per_call": host["sbp_signature_us"], "where": "host"},
@@ -439,6 +445,7 @@ def run_ours(args, rank, world, local_rank):
                                 "frac_of_sustained": round(tflops / world / bf16_sust, 4), "peak_source": peak_src,
                                 "traffic": _traffic("tp_gemm_kernel", "mlp")}},
         "domino": {"ms_serial": round(ser_ms, 4), "ms_overlap_2_chunks": round(dom_ms, 4),
+                   "ms_fused": round(dfu_ms, 4),
                    "ms_reduce_alone": round(red_ms, 4),
                    "hiding": round((ser_ms - dom_ms) / red_ms, 3) if red_ms > 0 else None,
                    "tflops_overlap": round(DOMINO_FLOPS / (dom_ms * 1e-3) / 1e12, 1)},
