@@ -586,15 +586,14 @@ def e2e_sweep(rtp, torch, dev, sweep):
 
 # ---- CPU oracle (baseline and reference arm) ---------------------------------------------
 
-CPU_SAMPLE_SHAPE = (8, 64, 4096)
+CPU_SAMPLE_SHAPE = (8, 256, 4096)
 
 
-def cpu_baseline(max_seconds: float = 20.0, steps: int = 1, with_mlp: bool = False):
-    """The oracle (single-threaded C++) on a bounded sample of the sweep: the
-    twelve float32 transitions on a [8,64,4096] slice of the activation
-    tensor (same meshes and specs), GB/s of algorithmic bytes."""
-    import numpy as np
-
+def cpu_sample_cases():
+    """The bounded sample the oracle runs: the twelve float32 transitions of
+    the sweep (meshes 1x8 and 2x4) on a [8,256,4096] slice of the activation
+    tensor (32 MiB per tensor, 256 MiB of partials, so it does not sit in the
+    host caches). Returns (label, pieces, src, dst, distinct source bytes)."""
     import oracle
     import synth
 
@@ -606,27 +605,40 @@ def cpu_baseline(max_seconds: float = 20.0, steps: int = 1, with_mlp: bool = Fal
         for name, sdm, ddm, partial in TRANSITIONS:
             src, dst = _oracle_specs(oracle, mesh_name, sdm, ddm, partial)
             pieces = parts if partial else oracle.shard(T, src)
-            cases.append((mesh_name + " " + name, pieces, src, dst))
+            nbytes = sum(p.nbytes for p in _distinct_reads(pieces, src, oracle, shape))
+            cases.append((mesh_name + " " + name, pieces, src, dst, nbytes))
+    return cases
+
+
+def cpu_baseline(max_seconds: float = 12.0, with_mlp: bool = False, cases=None):
+    """The oracle (single-threaded C++) on the bounded sample of
+    `cpu_sample_cases`, call after call through the twelve transitions until
+    about `max_seconds` of oracle time (at least one whole pass). GB/s of
+    algorithmic bytes: distinct source bytes read plus destination bytes
+    written."""
+    import oracle
+
+    if cases is None:
+        cases = cpu_sample_cases()
+    shape = CPU_SAMPLE_SHAPE
     total_bytes, total_s, done = 0, 0.0, 0
-    t_start = time.perf_counter()
-    for _ in range(steps):
-        for label, pieces, src, dst in cases:
-            t = time.perf_counter()
-            outs = oracle.reshard(pieces, shape, src, dst)
-            total_s += time.perf_counter() - t
-            total_bytes += sum(p.nbytes for p in _distinct_reads(pieces, src, oracle, shape)) + sum(o.nbytes for o in outs)
-            done += 1
-            if time.perf_counter() - t_start > max_seconds:
-                break
+    while done < len(cases) or total_s < max_seconds:
+        label, pieces, src, dst, nread = cases[done % len(cases)]
+        t = time.perf_counter()
+        outs = oracle.reshard(pieces, shape, src, dst)
+        total_s += time.perf_counter() - t
+        total_bytes += nread + sum(o.nbytes for o in outs)
+        done += 1
     out = {"value": round(total_bytes / total_s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-           "sample": "%d float32 reshard calls of the sweep on a [8,64,4096] slice (meshes 1x8 and 2x4)" % done,
+           "sample": "%d float32 reshard calls (the sweep's 12 transitions, meshes 1x8 and 2x4, in turn) on a "
+                     "[%d,%d,%d] slice of the activation tensor" % ((done,) + tuple(shape)),
            "seconds": round(total_s, 2), "host_cores": os.cpu_count()}
     if with_mlp:
         out["tp_mlp"] = cpu_mlp_baseline()
     return out
 
 
-def cpu_mlp_baseline(rows: int = 2):
+def cpu_mlp_baseline(rows: int = 64):
     """The oracle's TP-MLP (float64) on `rows` rows of the 8192x4096x16384x4096
     configuration, all columns; TFLOP/s of the sample (its full-size time is
     the sample time x 8192 / rows)."""
@@ -687,10 +699,11 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    cases = cpu_sample_cases()
     for _ in range(args.warmup):
-        cpu_baseline(max_seconds=per_step)
+        cpu_baseline(max_seconds=per_step, cases=cases)
     t = time.perf_counter()
-    vals = [cpu_baseline(max_seconds=per_step) for _ in range(args.steps)]
+    vals = [cpu_baseline(max_seconds=per_step, cases=cases) for _ in range(args.steps)]
     wall = time.perf_counter() - t
     v = statistics.median(x["value"] for x in vals)
     cb = dict(vals[-1])
@@ -699,7 +712,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(wall / args.steps * 1e3, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded generator)",
-        "config": {"workload": "resharding sweep transitions on a [8,64,4096] float32 slice, meshes 1x8 and 2x4, "
+        "config": {"workload": "resharding sweep transitions on a [8,256,4096] float32 slice, meshes 1x8 and 2x4, "
                                "by the single-threaded CPU oracle"},
         "cpu_baseline": cb, "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
@@ -799,7 +812,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     if args.profile_case:
         run_profile_case(args.profile_case)

@@ -1,7 +1,7 @@
 """Python binding of librtp (resharding and 1D tensor parallelism on a virtual
 mesh inside one GB300).
 
-Argument marshalling only: every step of the path runs in the library's CUDA
+Argument marshalling and buffer checks only: every step of the path runs in the library's CUDA
 kernels. PyTorch supplies device memory and streams. Loading fails loudly if
 the compiled library is missing; there is no fallback.
 
@@ -244,12 +244,26 @@ def _stream_ptr(stream) -> Optional[int]:
     return stream.cuda_stream or None
 
 
-def _alloc_pieces(shape, spec: Spec, like, out):
+_PIECE_SHAPES: dict = {}
+
+
+def piece_shapes(shape: Sequence[int], spec: Spec) -> List[Tuple[int, ...]]:
+    """shard_shape of every rank, cached per (shape, spec)."""
+    key = (tuple(shape), bytes(spec))
+    got = _PIECE_SHAPES.get(key)
+    if got is None:
+        got = [shard_shape(shape, spec, r) for r in range(spec.num_ranks)]
+        if len(_PIECE_SHAPES) > 4096:
+            _PIECE_SHAPES.clear()
+        _PIECE_SHAPES[key] = got
+    return got
+
+
+def _alloc_pieces(shapes, like, out):
     torch = _torch()
     if out is not None:
         return list(out)
-    return [torch.empty(shard_shape(shape, spec, r), dtype=like.dtype, device=like.device)
-            for r in range(spec.num_ranks)]
+    return [torch.empty(s, dtype=like.dtype, device=like.device) for s in shapes]
 
 
 def _check_cuda(ts, what):
@@ -261,12 +275,54 @@ def _check_cuda(ts, what):
                 raise RtpError(-1, "%s: tensors must be contiguous (row-major)" % what)
 
 
+def _check_buffers(what, device: int, groups):
+    """The library gets raw pointers and cannot see buffer sizes, so every
+    buffer is checked here against the shape and dtype the call will read or
+    write: a wrong buffer raises instead of reaching the GPU. device: the CUDA
+    device index the call runs on. groups: (name, tensors, shape, dtype), shape
+    one tuple for all the tensors or a list of one tuple per tensor (which also
+    fixes their count)."""
+    for name, ts, shape, dtype in groups:
+        per = isinstance(shape, list)
+        if per and len(ts) != len(shape):
+            raise RtpError(-1, "%s: %d %s buffers given, %d expected" % (what, len(ts), name, len(shape)))
+        for i, t in enumerate(ts):
+            s = shape[i] if per else shape
+            if t.dtype is not dtype or t.shape != s or not t.is_contiguous() or t.get_device() != device:
+                _buffer_error(what, name, i, t, s, dtype, device)
+
+
+def _buffer_error(what, name, i, t, shape, dtype, device):
+    if t.dtype is not dtype or tuple(t.shape) != tuple(shape):
+        raise RtpError(-2, "%s: %s[%d] is %s %s, expected %s %s" % (
+            what, name, i, t.dtype, tuple(t.shape), dtype, tuple(shape)))
+    if t.numel() == 0:
+        return  # an empty piece is never touched, wherever it lives
+    if not t.is_contiguous():
+        raise RtpError(-1, "%s: %s[%d] must be contiguous (row-major)" % (what, name, i))
+    raise RtpError(-1, "%s: %s[%d] is on %s, the call runs on device %d" % (what, name, i, t.device, device))
+
+
+def _device_of(t) -> int:
+    """Index of the current CUDA device, which must hold `t`."""
+    torch = _torch()
+    if not t.is_cuda:
+        raise RtpError(-1, "tensors must live on the GPU")
+    if t.get_device() != torch.cuda.current_device():
+        raise RtpError(-1, "tensors are on %s but the current CUDA device is %d" % (t.device,
+                                                                                  torch.cuda.current_device()))
+    return t.get_device()
+
+
 def shard(full, spec: Spec, out=None, stream=None):
     """Rank pieces of the logical tensor `full` (a CUDA tensor) under `spec`."""
     shape = tuple(full.shape)
-    pieces = _alloc_pieces(shape, spec, full, out)
-    _check_cuda([full] + pieces, "shard")
-    _check(_load().rtp_shard(_dtype_code(full), len(shape), _i64(shape), full.data_ptr(), ctypes.byref(spec),
+    shapes = piece_shapes(shape, spec)
+    code = _dtype_code(full)
+    pieces = _alloc_pieces(shapes, full, out)
+    _check_buffers("shard", _device_of(full), [("full", [full], shape, full.dtype),
+                                               ("out", pieces, shapes, full.dtype)])
+    _check(_load().rtp_shard(code, len(shape), _i64(shape), full.data_ptr(), ctypes.byref(spec),
                              _ptrs([p.data_ptr() for p in pieces]), _stream_ptr(stream)))
     return pieces
 
@@ -275,9 +331,12 @@ def reshard(pieces, shape: Sequence[int], src: Spec, dst: Spec, out=None, stream
     """Pieces laid out by `dst`, from `pieces` laid out by `src`."""
     shape = tuple(int(s) for s in shape)
     like = pieces[0]
-    outs = _alloc_pieces(shape, dst, like, out)
-    _check_cuda(list(pieces) + outs, "reshard")
-    _check(_load().rtp_reshard(_dtype_code(like), len(shape), _i64(shape), _ptrs([p.data_ptr() for p in pieces]),
+    dshapes = piece_shapes(shape, dst)
+    code = _dtype_code(like)
+    outs = _alloc_pieces(dshapes, like, out)
+    _check_buffers("reshard", _device_of(like), [("pieces", pieces, piece_shapes(shape, src), like.dtype),
+                                                 ("out", outs, dshapes, like.dtype)])
+    _check(_load().rtp_reshard(code, len(shape), _i64(shape), _ptrs([p.data_ptr() for p in pieces]),
                                ctypes.byref(src), _ptrs([o.data_ptr() for o in outs]), ctypes.byref(dst),
                                _stream_ptr(stream)))
     return outs
@@ -395,7 +454,11 @@ def tp_mlp(X, A_shards, B_shards, Y=None, partials=None, Z=None, mode: int = 1, 
         Z = torch.empty((M, N), dtype=torch.float32, device=dev)
     if mode == 0 and partials is None:
         partials = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in range(P)]
-    _check_cuda([X, Z] + list(A_shards) + list(B_shards) + list(Y) + list(partials or []), "tp_mlp")
+    bf16, f32 = torch.bfloat16, torch.float32
+    _check_buffers("tp_mlp", _device_of(X), [
+        ("X", [X], (M, K), bf16), ("A_shards", A_shards, (K, Fp), bf16), ("B_shards", B_shards, [(Fp, N)] * P, bf16),
+        ("Y", Y, [(M, Fp)] * P, bf16), ("partials", partials or [], [(M, N)] * (P if partials is not None else 0), f32),
+        ("Z", [Z], (M, N), f32)])
     if s0 is None:
         s0 = torch.cuda.current_stream()
     if s1 is None:
@@ -422,7 +485,10 @@ def tp_mlp_train_forward(X, A_shards, B_shards, Y=None, H=None, Z=None, stream=N
         H = [torch.empty((M, Fp), dtype=torch.bfloat16, device=dev) for _ in range(P)]
     if Z is None:
         Z = torch.empty((M, N), dtype=torch.float32, device=dev)
-    _check_cuda([X, Z] + list(A_shards) + list(B_shards) + list(Y) + list(H), "tp_mlp_train_forward")
+    bf16, f32 = torch.bfloat16, torch.float32
+    _check_buffers("tp_mlp_train_forward", _device_of(X), [
+        ("X", [X], (M, K), bf16), ("A_shards", A_shards, (K, Fp), bf16), ("B_shards", B_shards, [(Fp, N)] * P, bf16),
+        ("Y", Y, [(M, Fp)] * P, bf16), ("H", H, [(M, Fp)] * P, bf16), ("Z", [Z], (M, N), f32)])
     _check(_load().rtp_tp_mlp_train_forward(P, M, K, Fp * P, N, X.data_ptr(), _ptrs([a.data_ptr() for a in A_shards]),
                                             _ptrs([b.data_ptr() for b in B_shards]), _ptrs([y.data_ptr() for y in Y]),
                                             _ptrs([h.data_ptr() for h in H]), Z.data_ptr(), _stream_ptr(stream)))
@@ -451,8 +517,12 @@ def tp_mlp_backward(X, A_shards, B_shards, H, Y, dZ, dH=None, dX_partials=None, 
         dB = [torch.empty((Fp, N), dtype=f32, device=dev) for _ in range(P)]
     if mode == 0 and dX_partials is None:
         dX_partials = [torch.empty((M, K), dtype=f32, device=dev) for _ in range(P)]
-    _check_cuda([X, dZ, dX] + list(A_shards) + list(B_shards) + list(H) + list(Y) + list(dH) + list(dA) + list(dB)
-                + list(dX_partials or []), "tp_mlp_backward")
+    nparts = P if dX_partials is not None else 0
+    _check_buffers("tp_mlp_backward", _device_of(X), [
+        ("X", [X], (M, K), bf16), ("A_shards", A_shards, (K, Fp), bf16), ("B_shards", B_shards, [(Fp, N)] * P, bf16),
+        ("H", H, [(M, Fp)] * P, bf16), ("Y", Y, [(M, Fp)] * P, bf16), ("dZ", [dZ], (M, N), bf16),
+        ("dH", dH, [(M, Fp)] * P, bf16), ("dX_partials", dX_partials or [], [(M, K)] * nparts, f32),
+        ("dX", [dX], (M, K), f32), ("dA", dA, [(K, Fp)] * P, f32), ("dB", dB, [(Fp, N)] * P, f32)])
     if s0 is None:
         s0 = torch.cuda.current_stream()
     if s1 is None:
@@ -479,7 +549,11 @@ def tp_mlp_sp(X_shards, A_shards, B_shards, Y=None, Z_shards=None, stream=None):
         Y = [torch.empty((M, Fp), dtype=torch.bfloat16, device=dev) for _ in range(P)]
     if Z_shards is None:
         Z_shards = [torch.empty((Mr, N), dtype=torch.float32, device=dev) for _ in range(P)]
-    _check_cuda(list(X_shards) + list(A_shards) + list(B_shards) + list(Y) + list(Z_shards), "tp_mlp_sp")
+    bf16, f32 = torch.bfloat16, torch.float32
+    _check_buffers("tp_mlp_sp", _device_of(X_shards[0]), [
+        ("X_shards", X_shards, [(Mr, K)] * P, bf16), ("A_shards", A_shards, (K, Fp), bf16),
+        ("B_shards", B_shards, [(Fp, N)] * P, bf16), ("Y", Y, [(M, Fp)] * P, bf16),
+        ("Z_shards", Z_shards, [(Mr, N)] * P, f32)])
     _check(_load().rtp_tp_mlp_sp(P, M, K, Fp * P, N, _ptrs([x.data_ptr() for x in X_shards]),
                                  _ptrs([a.data_ptr() for a in A_shards]), _ptrs([b.data_ptr() for b in B_shards]),
                                  _ptrs([y.data_ptr() for y in Y]), _ptrs([z.data_ptr() for z in Z_shards]),
@@ -497,7 +571,10 @@ def tp_mlp_noalloc(X, A_shards, B_shards, Z=None, stream=None):
     N = B_shards[0].shape[1]
     if Z is None:
         Z = torch.empty((M, N), dtype=torch.float32, device=X.device)
-    _check_cuda([X, Z] + list(A_shards) + list(B_shards), "tp_mlp_noalloc")
+    bf16 = torch.bfloat16
+    _check_buffers("tp_mlp_noalloc", _device_of(X), [
+        ("X", [X], (M, K), bf16), ("A_shards", A_shards, (K, Fp), bf16), ("B_shards", B_shards, [(Fp, N)] * P, bf16),
+        ("Z", [Z], (M, N), torch.float32)])
     _check(_load().rtp_tp_mlp_noalloc(P, M, K, Fp * P, N, X.data_ptr(), _ptrs([a.data_ptr() for a in A_shards]),
                                       _ptrs([b.data_ptr() for b in B_shards]), Z.data_ptr(), _stream_ptr(stream)))
     return Z
@@ -518,6 +595,8 @@ def wait_selftest(limit_ns: int, out=None, stream=None, kernel: int = 0):
     torch = _torch()
     if out is None:
         out = torch.zeros(4, dtype=torch.int32, device="cuda")
+    if out.numel() < 2 or out.element_size() != 4 or out.dtype.is_floating_point:
+        raise RtpError(-1, "wait_selftest: out must hold at least 2 int32 values")
     _check_cuda([out], "wait_selftest")
     _check(_load().rtp_wait_selftest(int(kernel), int(limit_ns), out.data_ptr(), _stream_ptr(stream)))
     return out

@@ -288,3 +288,36 @@ def test_forms_cover_the_sweep():
     # narrow rows and 8-byte vectors take the register form
     s, d = rtp.spec_nd_sbp((4,), (("S", 0),)), rtp.spec_nd_sbp((4,), (("S", 1),))
     assert rtp.reshard_forms(rtp.F32, (64, 36), s, d)[0] > 0
+
+
+def test_binding_checks_buffers_before_any_launch():
+    """The library sees raw pointers only, so the binding checks every buffer's
+    count, shape, dtype and device against what the call will touch; a wrong
+    buffer raises RtpError and nothing reaches the GPU."""
+    import torch
+
+    spec = rtp.spec_nd_sbp((3,), (("S", 0),))
+    shapes = rtp.piece_shapes((13, 7), spec)
+    assert shapes == [rtp.shard_shape((13, 7), spec, r) for r in range(3)] == [(5, 7), (5, 7), (3, 7)]
+    assert rtp.piece_shapes((13, 7), spec) is shapes  # cached per (shape, spec)
+
+    cpu, f32 = -1, torch.float32  # get_device() of a host tensor
+    good = [torch.zeros(s) for s in shapes]
+    rtp._check_buffers("t", cpu, [("out", good, shapes, f32)])
+    cases = [
+        (good[:2], -1),                                                # one piece missing
+        ([good[0], torch.zeros((5, 7)), torch.zeros((5, 7))], -2),     # last piece too large
+        ([good[0], good[1], torch.zeros((3, 7), dtype=torch.bfloat16)], -2),  # wrong dtype
+        ([good[0], good[1], torch.zeros((7, 3)).t()], -1),              # right shape, not row-major
+    ]
+    for pieces, status in cases:
+        with pytest.raises(rtp.RtpError) as e:
+            rtp._check_buffers("t", cpu, [("out", pieces, shapes, f32)])
+        assert e.value.status == status
+    # the public calls refuse host tensors before launching anything
+    with pytest.raises(rtp.RtpError):
+        rtp.shard(torch.zeros((13, 7)), spec)
+    with pytest.raises(rtp.RtpError):
+        rtp.reshard(good, (13, 7), spec, rtp.spec_nd_sbp((3,), (("S", 1),)))
+    with pytest.raises(TypeError):
+        rtp.shard(torch.zeros((13, 7), dtype=torch.float64), spec)
