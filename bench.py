@@ -277,6 +277,14 @@ def run_ours(args, rank, world, local_rank):
         rtp.tp_mlp(dom["X"], dom["A"], dom["B"], Y=dom["Y"], partials=dom["parts"], Z=dom["Z"], mode=0, chunks=2,
                    s1=s1)
 
+    def run_domino4():
+        rtp.tp_mlp(dom["X"], dom["A"], dom["B"], Y=dom["Y"], partials=dom["parts"], Z=dom["Z"], mode=0, chunks=4,
+                   s1=s1)
+
+    def run_domino2d():
+        rtp.tp_mlp(dom["X"], dom["A"], dom["B"], Y=dom["Y"], partials=dom["parts"], Z=dom["Z"], mode=0, chunks=2,
+                   col_blocks=2, s1=s1)
+
     def run_serial():
         rtp.tp_mlp(dom["X"], dom["A"], dom["B"], Y=dom["Y"], partials=dom["parts"], Z=dom["Z"], mode=0, chunks=1)
 
@@ -302,9 +310,10 @@ def run_ours(args, rank, world, local_rank):
     shard_ops = [(label, (lambda T=T, sp=sp, o=o: rtp.shard(T, sp, out=o)), nbytes, nl)
                  for (label, T, sp, o, nbytes, nl) in shards]
     launches_per_step = (sum(x[3] for x in ops) + sum(x[3] for x in shard_ops) +
-                         2 + 2 + 6 + 3 + 2 + 1 + 2 + 4 + 5)
-    # mlp 2, sequence parallel 2, domino 2x3, serial 3, fused on the Domino shape 2, reduce 1, training forward 2,
-    # backward 4, backward with the separate, overlapped dX sum 5
+                         2 + 2 + 6 + 12 + 10 + 3 + 2 + 1 + 2 + 4 + 5)
+    # mlp 2, sequence parallel 2, domino 2 chunks x 3, 4 chunks x 3, 2 chunks x (1 + 2 column blocks x 2), serial 3,
+    # fused on the Domino shape 2, reduce 1, training forward 2, backward 4, backward with the separate, overlapped
+    # dX sum 5
     E = lambda: torch.cuda.Event(enable_timing=True)
 
     def step(record):
@@ -322,7 +331,8 @@ def run_ours(args, rank, world, local_rank):
             fn()
             e1.record()
             record.append(("reshard", label, e0, e1, nbytes))
-        for kind, fn in (("mlp", run_mlp), ("sp", run_sp), ("domino", run_domino), ("serial", run_serial),
+        for kind, fn in (("mlp", run_mlp), ("sp", run_sp), ("domino", run_domino), ("domino4", run_domino4),
+                         ("domino2d", run_domino2d), ("serial", run_serial),
                          ("dom_fused", run_dom_fused), ("reduce", run_reduce), ("train_fwd", run_train_fwd), ("bwd", run_bwd),
                          ("bwd_overlap", run_bwd_overlap)):
             flush.zero_()
@@ -361,6 +371,8 @@ def run_ours(args, rank, world, local_rank):
     reshard_bytes = sum(v[2] * v[1] for (k, _), v in per.items() if k == "reshard")
     mlp_ms = per[("mlp", "mlp")][0]
     dom_ms = per[("domino", "domino")][0] / args.steps
+    dom4_ms = per[("domino4", "domino4")][0] / args.steps
+    dom2d_ms = per[("domino2d", "domino2d")][0] / args.steps
     ser_ms = per[("serial", "serial")][0] / args.steps
     dfu_ms = per[("dom_fused", "dom_fused")][0] / args.steps
     red_ms = per[("reduce", "reduce")][0] / args.steps
@@ -393,7 +405,11 @@ def run_ours(args, rank, world, local_rank):
                                "frac_hbm": round(red_bytes / (red_ms * 1e-3) / 1e9 / hbm_peak, 4),
                                "shape": "8 float32 partials [4096,8192] -> Z"},
         "a6_a7_separate_schedule": {"ms": round(ser_ms, 4), "tflops": round(DOMINO_FLOPS / (ser_ms * 1e-3) / 1e12, 1)},
-        "a8_domino": {"ms": round(dom_ms, 4), "hiding": round((ser_ms - dom_ms) / red_ms, 3) if red_ms > 0 else None},
+        "a8_domino": {"ms": round(dom_ms, 4), "hiding": round((ser_ms - dom_ms) / red_ms, 3) if red_ms > 0 else None,
+                      "ms_4_chunks": round(dom4_ms, 4),
+                      "hiding_4_chunks": round((ser_ms - dom4_ms) / red_ms, 3) if red_ms > 0 else None,
+                      "ms_2_chunks_2_column_blocks": round(dom2d_ms, 4),
+                      "hiding_2_chunks_2_column_blocks": round((ser_ms - dom2d_ms) / red_ms, 3) if red_ms > 0 else None},
         "a5_a7_fused_domino_shape": {"ms": round(dfu_ms, 4), "tflops": round(DOMINO_FLOPS / (dfu_ms * 1e-3) / 1e12, 1),
                                      "frac_bf16": round(DOMINO_FLOPS / (dfu_ms * 1e-3) / 1e12 / bf16_peak, 4)},
         "f2_tp_mlp_sequence_parallel": {"ms": round(sp_ms, 4), "tflops": round(MLP_FLOPS / (sp_ms * 1e-3) / 1e12, 1),
@@ -445,6 +461,7 @@ def run_ours(args, rank, world, local_rank):
                                 "frac_of_sustained": round(tflops / world / bf16_sust, 4), "peak_source": peak_src,
                                 "traffic": _traffic("tp_gemm_kernel", "mlp")}},
         "domino": {"ms_serial": round(ser_ms, 4), "ms_overlap_2_chunks": round(dom_ms, 4),
+                   "ms_overlap_4_chunks": round(dom4_ms, 4), "ms_overlap_2_chunks_2_column_blocks": round(dom2d_ms, 4),
                    "ms_fused": round(dfu_ms, 4),
                    "ms_reduce_alone": round(red_ms, 4),
                    "hiding": round((ser_ms - dom_ms) / red_ms, 3) if red_ms > 0 else None,
@@ -542,11 +559,20 @@ def e2e_sweep(rtp, torch, dev, sweep):
     buffers: pinned host -> device copy of the source pieces, reshard, device
     -> pinned host copy of the destination pieces, all inside the timed region
     (2 timed steps after 1 warm-up). The six transitions of a step are
-    pipelined on three streams, as a caller would: the host-to-device copy of
+    pipelined on three streams, as a caller would, in the order that keeps both
+    copy directions busy: the host-to-device copy of
     transition i+1 and the device-to-host copy of transition i-1 run while
     transition i reshards (the two copy directions use separate copy engines).
     Device buffers are allocated once, outside the timed region."""
     sel = [s for s in sweep if s[0].startswith("bfloat16 1x8")]
+    # Order for a two-stage pipeline (upload, then download; the reshard in
+    # between is short) by Johnson's rule: transitions that upload less than
+    # they download first, by increasing upload; then the rest by decreasing
+    # download. Both copy directions then stay busy from start to end.
+    nb = lambda ps: sum(p.numel() * p.element_size() for p in ps)
+    up = [x for x in sel if nb(x[2]) < nb(x[4])]
+    rest = [x for x in sel if nb(x[2]) >= nb(x[4])]
+    sel = sorted(up, key=lambda x: nb(x[2])) + sorted(rest, key=lambda x: -nb(x[4]))
     host_in = [[torch.empty(p.shape, dtype=p.dtype, pin_memory=True).copy_(p) for p in s[2]] for s in sel]
     host_out = [[torch.empty(p.shape, dtype=p.dtype, pin_memory=True) for p in s[4]] for s in sel]
     dev_in = [[torch.empty_like(p, device=dev) for p in hs] for hs in host_in]

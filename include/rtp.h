@@ -18,7 +18,14 @@
  *     take a stream are asynchronous with respect to the host and ordered on
  *     that stream (NULL = the legacy default stream). Host-only calls (the
  *     front-ends, shapes, inference) touch no GPU state.
- *   - Source and destination buffers must not overlap.
+ *   - Source and destination buffers must not overlap: rtp_shard and
+ *     rtp_reshard return RTP_EINVAL, before any launch, when a source piece
+ *     they would read and a destination piece share bytes.
+ *   - Calls may come from several host threads at once. Launch parameters,
+ *     cached tensor maps and the events that order a call's two streams are
+ *     kept per thread, so concurrent calls on their own streams do not wait
+ *     on, or overwrite, each other's state. Buffers that two concurrent calls
+ *     both write are the caller's to order.
  *
  * Readings of the pages that the semantics rely on (pages are cited by title
  * and section):

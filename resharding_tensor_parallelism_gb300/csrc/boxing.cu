@@ -39,6 +39,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <unordered_map>
 
@@ -671,15 +672,15 @@ __global__ void __launch_bounds__(kBlock, 4) boxing_kernel(const __grid_constant
 
 int sm_count()
 {
-    static int cached[64] = {};
+    static std::atomic<int> cached[64];  // 0 = not yet queried
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (!cached[dev]) {
-        int n = 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (!n) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-        cached[dev] = n;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return n;
 }
 
 int pick_vec(const PlanTask& t, const void* const* src, void* const* dst, int es)
@@ -857,14 +858,14 @@ const PP& shrink(const KParams& full, int nt, int np, PP* out)
 template <class PP, bool SUM, int ES, int OP>
 int launch_one(const PP& prm, int grid, int smem, cudaStream_t st)
 {
-    static bool configured[64] = {};
+    static std::atomic<bool> configured[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(RTP_ECUDA, "reshard: no CUDA device");
-    if (smem > 0 && !configured[dev]) {
+    if (smem > 0 && !configured[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(boxing_kernel<PP, SUM, ES, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kBulkDynSmem) != cudaSuccess)
             return fail(RTP_ECUDA, "reshard: cudaFuncSetAttribute failed");
-        configured[dev] = true;
+        configured[dev].store(true, std::memory_order_release);
     }
     boxing_kernel<PP, SUM, ES, OP><<<grid, kBlock, smem, st>>>(prm);
     return RTP_OK;
@@ -913,15 +914,16 @@ int launch_tiles(const KParams& prm, int nt, int np, int es, PP* tp, int grid, i
 
 void* tensor_map_encoder()
 {
-    static void* fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
+    static std::atomic<void*> fn{nullptr};
+    void* f = fn.load(std::memory_order_acquire);
+    if (!f) {
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = p;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn.store(f, std::memory_order_release);
     }
-    return fn;
+    return f;
 }
 
 int bulk_wait_selftest(unsigned long long limit_ns, uint32_t* out, void* stream)

@@ -198,6 +198,38 @@ int check_pointers(const char* fn, const char* which, const std::vector<PlanTask
     return RTP_OK;
 }
 
+// Byte ranges [begin, end) of the non-empty pieces of `spec`, one per rank.
+void piece_ranges(int ndim, const int64_t* shape, const rtp_spec& spec, const void* const* bufs, int es, bool src,
+                  std::vector<std::pair<uintptr_t, uintptr_t>>* out)
+{
+    int64_t coords[RTP_MAX_RANKS * RTP_MAX_MESH_NDIM];
+    rank_coords(spec, coords);
+    for (int64_t r = 0; r < num_ranks(spec); ++r) {
+        const Box b = rank_box(ndim, shape, spec, coords + r * RTP_MAX_MESH_NDIM);
+        const int64_t v = box_volume(ndim, b);
+        if (v == 0 || !bufs[r] || (src && !b.b_rep)) continue;
+        const uintptr_t p = (uintptr_t)bufs[r];
+        out->emplace_back(p, p + (uintptr_t)v * (uintptr_t)es);
+    }
+}
+
+// Source and destination pieces must not share memory: the kernel reads
+// sources while it writes destinations, in no fixed order.
+int check_no_overlap(const char* fn, std::vector<std::pair<uintptr_t, uintptr_t>> srcs,
+                     std::vector<std::pair<uintptr_t, uintptr_t>> dsts)
+{
+    std::sort(srcs.begin(), srcs.end());
+    std::sort(dsts.begin(), dsts.end());
+    size_t i = 0, j = 0;
+    while (i < srcs.size() && j < dsts.size()) {
+        if (srcs[i].first < dsts[j].second && dsts[j].first < srcs[i].second)
+            return fail(RTP_EINVAL, "%s: a source buffer overlaps a destination buffer", fn);
+        if (srcs[i].second <= dsts[j].second) ++i;
+        else ++j;
+    }
+    return RTP_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -216,6 +248,10 @@ int rtp_reshard(rtp_dtype dtype, int ndim, const int64_t* shape, const void* con
     int es = element_size(dtype);
     if ((st = check_pointers(fn, "source", tasks, src_dev, true, es))) return st;
     if ((st = check_pointers(fn, "destination", tasks, (const void* const*)dst_dev, false, es))) return st;
+    std::vector<std::pair<uintptr_t, uintptr_t>> sr, dr;
+    piece_ranges(ndim, shape, *src, src_dev, es, true, &sr);
+    piece_ranges(ndim, shape, *dst, (const void* const*)dst_dev, es, false, &dr);
+    if ((st = check_no_overlap(fn, std::move(sr), std::move(dr)))) return st;
     return launch_tasks(dtype, tasks, src_dev, dst_dev, stream, nullptr);
 }
 
@@ -234,6 +270,10 @@ int rtp_shard(rtp_dtype dtype, int ndim, const int64_t* shape, const void* full,
     int es = element_size(dtype);
     if ((st = check_pointers(fn, "full-tensor", tasks, srcs, true, es))) return st;
     if ((st = check_pointers(fn, "shard", tasks, (const void* const*)shard_dev, false, es))) return st;
+    std::vector<std::pair<uintptr_t, uintptr_t>> sr, dr;
+    piece_ranges(ndim, shape, whole, srcs, es, true, &sr);
+    piece_ranges(ndim, shape, *spec, (const void* const*)shard_dev, es, false, &dr);
+    if ((st = check_no_overlap(fn, std::move(sr), std::move(dr)))) return st;
     return launch_tasks(dtype, tasks, srcs, shard_dev, stream, nullptr);
 }
 

@@ -48,6 +48,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstring>
 #include <vector>
 
@@ -703,8 +704,9 @@ int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int bo
 template <int CFG>
 int launch_gemm_t(GemmArgs& args, cudaStream_t stream)
 {
-    static bool configured[64] = {};
-    static int max_clusters[64] = {};
+    // per device: resident 2-SM clusters (0 = not yet queried); racing first
+    // calls compute the same value
+    static std::atomic<int> max_clusters[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(RTP_ECUDA, "tp_mlp: no CUDA device");
     cudaLaunchConfig_t cfg = {};
@@ -718,18 +720,19 @@ int launch_gemm_t(GemmArgs& args, cudaStream_t stream)
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (!configured[dev]) {
+    int nclusters = max_clusters[dev].load(std::memory_order_acquire);
+    if (!nclusters) {
         cudaError_t e = cudaFuncSetAttribute(tp_gemm_kernel<CFG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM2_BYTES);
         if (e != cudaSuccess) return fail(RTP_ECUDA, "tp_mlp: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         cfg.gridDim = dim3(2 * 64);
         int n = 0;
         e = cudaOccupancyMaxActiveClusters(&n, tp_gemm_kernel<CFG>, &cfg);
         if (e != cudaSuccess || n <= 0) return fail(RTP_ECUDA, "tp_mlp: cudaOccupancyMaxActiveClusters: %s", cudaGetErrorString(e));
-        max_clusters[dev] = n;
-        configured[dev] = true;
+        max_clusters[dev].store(n, std::memory_order_release);
+        nclusters = n;
     }
     args.total_tiles = (args.fused ? 1 : args.groups) * args.m_tiles * args.n_tiles;
-    const int clusters = args.total_tiles < max_clusters[dev] ? args.total_tiles : max_clusters[dev];
+    const int clusters = args.total_tiles < nclusters ? args.total_tiles : nclusters;
     if (clusters <= 0) return RTP_OK;
     cfg.gridDim = dim3(2 * clusters);
     cudaError_t e = cudaLaunchKernelEx(&cfg, tp_gemm_kernel<CFG>, args);
@@ -758,9 +761,13 @@ struct Events {
     cudaEvent_t fwd = nullptr, back = nullptr;
 };
 
+// One pair per host thread and device: a call records an event on its own s0
+// and makes its own s1 wait on it, so two threads calling at once (on their
+// own streams) must not share the event, or one would wait on the other's
+// record. The events live until the process exits.
 int events(Events** out)
 {
-    static Events ev[64];
+    static thread_local Events ev[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(RTP_ECUDA, "tp_mlp: no CUDA device");
     Events& e = ev[dev];

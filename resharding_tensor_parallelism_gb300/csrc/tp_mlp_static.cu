@@ -18,6 +18,8 @@
 // library's code for it is loaded, until the process exits.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "rtp_internal.h"
 
 namespace {
@@ -27,8 +29,9 @@ constexpr size_t kAlign = 256;
 
 static __device__ __align__(256) unsigned char g_tp_static_scratch[kStaticScratchBytes];
 
-// Device address of the array, per device, found once with that device current.
-void* g_scratch_addr[64];
+// Device address of the array, per device, found once with that device current
+// (threads racing on a first call find the same address).
+std::atomic<void*> g_scratch_addr[64];
 
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -53,16 +56,16 @@ extern "C" int rtp_tp_mlp_noalloc(int P, int64_t M, int64_t K, int64_t F, int64_
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return rtp::fail(RTP_ECUDA, "%s: cudaGetDevice: %s", fn, cudaGetErrorString(e));
     if (dev < 0 || dev >= 64) return rtp::fail(RTP_EUNSUPPORTED, "%s: device %d", fn, dev);
-    if (!g_scratch_addr[dev]) {
+    void* addr = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (!addr) {
         // Set-up, once per device, with that device current. In host code the
         // array's name is only a stand-in, so the kernels get this address.
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_tp_static_scratch);
-        if (e != cudaSuccess || !p)
+        e = cudaGetSymbolAddress(&addr, g_tp_static_scratch);
+        if (e != cudaSuccess || !addr)
             return rtp::fail(RTP_ECUDA, "%s: cudaGetSymbolAddress: %s", fn, cudaGetErrorString(e));
-        g_scratch_addr[dev] = p;
+        g_scratch_addr[dev].store(addr, std::memory_order_release);
     }
-    char* base = static_cast<char*>(g_scratch_addr[dev]);
+    char* base = static_cast<char*>(addr);
     void* Y[8];
     for (int i = 0; i < P; ++i) Y[i] = base + (size_t)i * per_rank;
     // The same path as rtp_tp_mlp, fused reduction, one stream. Y is written

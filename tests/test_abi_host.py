@@ -321,3 +321,24 @@ def test_binding_checks_buffers_before_any_launch():
         rtp.reshard(good, (13, 7), spec, rtp.spec_nd_sbp((3,), (("S", 1),)))
     with pytest.raises(TypeError):
         rtp.shard(torch.zeros((13, 7), dtype=torch.float64), spec)
+
+
+def test_overlapping_source_and_destination_are_rejected():
+    """rtp_shard / rtp_reshard refuse buffers where a source piece and a
+    destination piece share bytes (the kernel reads and writes them in no fixed
+    order). The check runs on the host before any launch, so fake, never
+    dereferenced addresses serve here."""
+    import ctypes
+
+    lib = rtp.lib()
+    shape = rtp._i64([4, 4])
+    s0 = rtp.spec_nd_sbp((2,), (("S", 0),))
+    s1 = rtp.spec_nd_sbp((2,), (("S", 1),))
+    src = rtp._ptrs([0x10000, 0x10100])  # two [2,4] float32 pieces: 32 bytes each
+    dst = rtp._ptrs([0x20000, 0x10110])  # rank 1's [4,2] piece starts inside source piece 1
+    rc = lib.rtp_reshard(rtp.F32, 2, shape, src, ctypes.byref(s0), dst, ctypes.byref(s1), None)
+    assert rc == -1 and "overlaps" in rtp.last_error()
+    full = ctypes.c_void_p(0x30000)      # the whole [4,4] tensor: 64 bytes
+    pieces = rtp._ptrs([0x30020, 0x40000])  # rank 0's piece inside the full tensor
+    rc = lib.rtp_shard(rtp.F32, 2, shape, full, ctypes.byref(s0), pieces, None)
+    assert rc == -1 and "overlaps" in rtp.last_error()

@@ -138,6 +138,49 @@ def test_domino_configuration_full_size():
     np.testing.assert_array_equal(Z4, Z2)
 
 
+def test_domino_from_two_host_threads():
+    """Two host threads run the two-stream Domino schedule at once, each on its
+    own pair of streams: each call orders its own second stream after its own
+    GEMMs (the ordering events are per thread), so both keep producing the
+    single-threaded result bit for bit."""
+    import threading
+
+    cases = [_inputs(512, 256, 1024, 512, 4, seed=s) for s in (500, 600)]
+    dev_cases = [(to_dev(X), [to_dev(a) for a in As], [to_dev(b) for b in Bs]) for X, As, Bs in cases]
+    want = []
+    for X, As, Bs in dev_cases:
+        Z, _ = rtp.tp_mlp(X, As, Bs, mode=0, chunks=2, col_blocks=2, s1=torch.cuda.Stream())
+        torch.cuda.synchronize()
+        want.append(Z.clone())
+    errors = []
+
+    def worker(k):
+        try:
+            torch.cuda.set_device(0)
+            X, As, Bs = dev_cases[k]
+            s0, s1 = torch.cuda.Stream(), torch.cuda.Stream()
+            M, N = X.shape[0], Bs[0].shape[1]
+            with torch.cuda.stream(s0):  # every allocation, fill and comparison ordered on s0
+                Y = [torch.empty((M, As[0].shape[1]), dtype=torch.bfloat16, device="cuda") for _ in As]
+                parts = [torch.empty((M, N), dtype=torch.float32, device="cuda") for _ in As]
+                for it in range(40):
+                    Z = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+                    rtp.tp_mlp(X, As, Bs, Y=Y, partials=parts, Z=Z, mode=0, chunks=2, col_blocks=2, s0=s0, s1=s1)
+                    if not torch.equal(Z, want[k]):
+                        errors.append("thread %d, call %d: Z differs" % (k, it))
+                        return
+        except Exception as e:  # reported by the main thread
+            errors.append("thread %d: %r" % (k, e))
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    assert rtp.device_error() == 0
+
+
 def test_argument_errors():
     dev = lambda *s: torch.zeros(s, dtype=torch.bfloat16, device="cuda")
     X = dev(256, 64)
