@@ -308,3 +308,41 @@ def test_sweep_full_size(sweep_inputs, dt, mesh, name, sdm, spart, ddm, dpart):
         torch.cuda.synchronize()
         for a, b in zip(first, again):
             np.testing.assert_array_equal(a, to_host(b))
+
+
+# ---- beyond 2^31 elements -------------------------------------------------------
+
+def test_more_than_2_to_the_31_elements():
+    """Tensors of more than 2^31 elements (offsets past 4 GiB and 8 GiB): a
+    ragged S(0) -> S(1) -> S(0) round trip in bf16, and a P-sum of two float32
+    partials to B. Too large for the oracle, so the checks are properties that
+    hold at any size: each piece is its slice of the logical tensor (bit for
+    bit), the round trip is the identity, the B replicas are identical, and
+    sampled sums (including the last elements) are within the P-sum bound."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(31)
+    shape = (65537, 32771)  # 2,147,713,027 elements > 2^31; both splits ragged
+    assert shape[0] * shape[1] > 2 ** 31
+    T = torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    s0, s1 = rtp.spec_nd_sbp((2,), (("S", 0),)), rtp.spec_nd_sbp((2,), (("S", 1),))
+    a = rtp.shard(T, s0)
+    assert torch.equal(a[0], T[:32769]) and torch.equal(a[1], T[32769:])
+    b = rtp.reshard(a, shape, s0, s1)
+    assert torch.equal(b[0], T[:, :16386]) and torch.equal(b[1], T[:, 16386:])
+    c = rtp.reshard(b, shape, s1, s0)
+    assert all(torch.equal(x, y) for x, y in zip(c, a))
+    del T, a, b, c
+    torch.cuda.empty_cache()
+
+    shape = (46341, 46341)  # 2,147,488,281 float32 elements (8.6 GB) per partial
+    parts = [torch.randn(shape, generator=g, device="cuda") for _ in range(2)]
+    outs = rtp.reshard(parts, shape, rtp.spec_nd_sbp((2,), ("P",)), rtp.spec_nd_sbp((2,), ("B",)))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+    n = shape[0] * shape[1]
+    idx = torch.cat([torch.randint(0, n, (1 << 20,), generator=g, device="cuda"),
+                     torch.arange(n - 4096, n, device="cuda")])
+    x = [p.view(-1)[idx].double().cpu().numpy() for p in parts]
+    got = outs[0].view(-1)[idx].double().cpu().numpy()
+    assert np.all(np.abs(got - (x[0] + x[1])) <= 1e-6 * (np.abs(x[0]) + np.abs(x[1])))
+    assert rtp.device_error() == 0
