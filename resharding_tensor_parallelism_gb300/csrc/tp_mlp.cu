@@ -81,6 +81,7 @@ enum { EPI_GELU_BF16 = 0, EPI_F32 = 1, EPI_DGELU_BF16 = 2 };
 //   CFG_B_K     B is K-major in memory (a transposed operand: A_i^T, B_i^T)
 //   bits 4-5    the epilogue (EPI_*)
 enum : int { CFG_SP_A = 1, CFG_SP_OUT = 2, CFG_A_MN = 4, CFG_B_K = 8, CFG_EPI_SHIFT = 4 };
+enum : int { RANKS_OUTER = 0, RANKS_IN_N = 1, RANKS_IN_M = 2 };
 
 
 struct GemmArgs {
@@ -103,6 +104,14 @@ struct GemmArgs {
     int32_t a_rows_per_map, a_maps;
     int32_t out_rows_per_ptr, out_ptrs;
     int32_t cfg;                 // kernel configuration (CFG_* operand bits), chosen by the host
+    // Tile order of a non-fused launch over several groups (ranks):
+    //   RANKS_OUTER  group by group;
+    //   RANKS_IN_N   the groups' N tiles form one N range (every group has the
+    //                same A operand, e.g. X in X A_i: each block of A rows then
+    //                stays in L2 while all groups' B columns stream past it);
+    //   RANKS_IN_M   the groups' M tiles form one M range (every group has the
+    //                same B operand, e.g. dZ in Y_i^T dZ).
+    int32_t rank_fold;
 };
 
 __device__ unsigned int g_tp_error;
@@ -245,17 +254,33 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32])
                  : "memory");
 }
 
+// Tile index -> (group, M tile, N tile). Within an (M range, N range) the
+// tiles go in blocks of GROUP_M M tiles, N tile after N tile within a block,
+// so the tiles in flight at once share their A rows and B columns in L2. The
+// group is the outermost index, or part of the N range or of the M range
+// (rank_fold). Every map is a bijection of [0, groups * m_tiles * n_tiles).
 __device__ __forceinline__ void tile_coords(const GemmArgs& a, int tile, int& g, int& mt, int& nt)
 {
-    const int per_group = a.m_tiles * a.n_tiles;
-    g = a.fused ? 0 : tile / per_group;
-    const int r = tile - (a.fused ? 0 : g * per_group);
-    const int span = GROUP_M * a.n_tiles;
+    const bool in_n = !a.fused && a.rank_fold == RANKS_IN_N, in_m = !a.fused && a.rank_fold == RANKS_IN_M;
+    const int groups_outer = a.fused || in_n || in_m ? 1 : a.groups;
+    const int per_group = a.m_tiles * a.n_tiles * (a.fused ? 1 : a.groups / groups_outer);
+    g = groups_outer > 1 ? tile / per_group : 0;
+    const int r = tile - g * per_group;
+    const int mtiles = in_m ? a.groups * a.m_tiles : a.m_tiles;
+    const int ntiles = in_n ? a.groups * a.n_tiles : a.n_tiles;
+    const int span = GROUP_M * ntiles;
     const int first_m = (r / span) * GROUP_M;
-    const int rows = min(a.m_tiles - first_m, GROUP_M);
+    const int rows = min(mtiles - first_m, GROUP_M);
     const int w = r % span;
     mt = first_m + w % rows;
     nt = w / rows;
+    if (in_n) {
+        g = nt / a.n_tiles;
+        nt -= g * a.n_tiles;
+    } else if (in_m) {
+        g = mt / a.m_tiles;
+        mt -= g * a.m_tiles;
+    }
 }
 
 __device__ __forceinline__ float gelu(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752440f)); }
@@ -847,6 +872,7 @@ int tp_mlp_impl(const char* fn, int P, int64_t M, int64_t K, int64_t F, int64_t 
     g1.ldo = Fp;
     g1.groups = P;
     g1.fused = 0;
+    g1.rank_fold = RANKS_IN_N;  // every rank multiplies the same X
     g1.epi = EPI_GELU_BF16;
     const int bm = BM2;
     g1.m_tiles = (int)((Mc + bm - 1) / bm);
@@ -1033,6 +1059,9 @@ int rtp_tp_mlp_backward(int P, int64_t M, int64_t K, int64_t F, int64_t N, const
     shape(gx, M, K, Fp, EPI_F32, CFG_B_K, mode == 1);
     shape(ga, K, Fp, M, EPI_F32, CFG_A_MN, 0);
     shape(gb, Fp, N, M, EPI_F32, CFG_A_MN, 0);
+    gh.rank_fold = RANKS_IN_N;  // dZ shared by every rank
+    ga.rank_fold = RANKS_IN_N;  // X^T shared
+    gb.rank_fold = RANKS_IN_M;  // dZ shared (B side)
     if ((st = launch_gemm(gh, s0)) || (st = launch_gemm(gx, s0))) return st;
     if (mode == 0) {
         // The rank sum of dX, beside the weight-gradient GEMMs when a second stream is given.
@@ -1099,6 +1128,7 @@ int rtp_tp_mlp_sp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void*
     g1.a_rows_per_map = (int)Mr;
     g1.a_maps = P;
     g1.cfg = CFG_SP_A;
+    g1.rank_fold = RANKS_IN_N;  // every rank multiplies the same (gathered) X
     if ((st = launch_gemm(g1, stream))) return st;
     // row-parallel GEMM: ranks summed in TMEM, rows scattered to their shard
     g2.ldo = N;
