@@ -81,7 +81,7 @@ enum { EPI_GELU_BF16 = 0, EPI_F32 = 1, EPI_DGELU_BF16 = 2 };
 //   CFG_B_K     B is K-major in memory (a transposed operand: A_i^T, B_i^T)
 //   bits 4-5    the epilogue (EPI_*)
 enum : int { CFG_SP_A = 1, CFG_SP_OUT = 2, CFG_A_MN = 4, CFG_B_K = 8, CFG_EPI_SHIFT = 4 };
-enum : int { RANKS_OUTER = 0, RANKS_IN_N = 1, RANKS_IN_M = 2 };
+enum : int { RANKS_OUTER = 0, RANKS_IN_N = 1 };
 
 
 struct GemmArgs {
@@ -106,11 +106,10 @@ struct GemmArgs {
     int32_t cfg;                 // kernel configuration (CFG_* operand bits), chosen by the host
     // Tile order of a non-fused launch over several groups (ranks):
     //   RANKS_OUTER  group by group;
-    //   RANKS_IN_N   the groups' N tiles form one N range (every group has the
-    //                same A operand, e.g. X in X A_i: each block of A rows then
-    //                stays in L2 while all groups' B columns stream past it);
-    //   RANKS_IN_M   the groups' M tiles form one M range (every group has the
-    //                same B operand, e.g. dZ in Y_i^T dZ).
+    //   RANKS_IN_N   the groups' N tiles form one N range. For groups with the
+    //                same A operand (X in X A_i): each block of GROUP_M A row
+    //                tiles then stays in L2 while every group's B columns stream
+    //                past it, instead of being fetched again for every group.
     int32_t rank_fold;
 };
 
@@ -257,29 +256,24 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32])
 // Tile index -> (group, M tile, N tile). Within an (M range, N range) the
 // tiles go in blocks of GROUP_M M tiles, N tile after N tile within a block,
 // so the tiles in flight at once share their A rows and B columns in L2. The
-// group is the outermost index, or part of the N range or of the M range
-// (rank_fold). Every map is a bijection of [0, groups * m_tiles * n_tiles).
+// group is the outermost index, or part of the N range (rank_fold). Both maps
+// are bijections of [0, groups * m_tiles * n_tiles).
 __device__ __forceinline__ void tile_coords(const GemmArgs& a, int tile, int& g, int& mt, int& nt)
 {
-    const bool in_n = !a.fused && a.rank_fold == RANKS_IN_N, in_m = !a.fused && a.rank_fold == RANKS_IN_M;
-    const int groups_outer = a.fused || in_n || in_m ? 1 : a.groups;
-    const int per_group = a.m_tiles * a.n_tiles * (a.fused ? 1 : a.groups / groups_outer);
-    g = groups_outer > 1 ? tile / per_group : 0;
+    const bool in_n = !a.fused && a.rank_fold == RANKS_IN_N;
+    const int per_group = a.fused || in_n ? 0 : a.m_tiles * a.n_tiles;
+    g = per_group ? tile / per_group : 0;
     const int r = tile - g * per_group;
-    const int mtiles = in_m ? a.groups * a.m_tiles : a.m_tiles;
     const int ntiles = in_n ? a.groups * a.n_tiles : a.n_tiles;
     const int span = GROUP_M * ntiles;
     const int first_m = (r / span) * GROUP_M;
-    const int rows = min(mtiles - first_m, GROUP_M);
+    const int rows = min(a.m_tiles - first_m, GROUP_M);
     const int w = r % span;
     mt = first_m + w % rows;
     nt = w / rows;
     if (in_n) {
         g = nt / a.n_tiles;
         nt -= g * a.n_tiles;
-    } else if (in_m) {
-        g = mt / a.m_tiles;
-        mt -= g * a.m_tiles;
     }
 }
 
@@ -1059,9 +1053,12 @@ int rtp_tp_mlp_backward(int P, int64_t M, int64_t K, int64_t F, int64_t N, const
     shape(gx, M, K, Fp, EPI_F32, CFG_B_K, mode == 1);
     shape(ga, K, Fp, M, EPI_F32, CFG_A_MN, 0);
     shape(gb, Fp, N, M, EPI_F32, CFG_A_MN, 0);
-    gh.rank_fold = RANKS_IN_N;  // dZ shared by every rank
-    ga.rank_fold = RANKS_IN_N;  // X^T shared
-    gb.rank_fold = RANKS_IN_M;  // dZ shared (B side)
+    // dZ and X^T are the A operands of every rank's dH and dA. dB (long K,
+    // shared B operand) keeps the rank-outer order: with K = M its operand
+    // panels do not survive in L2 between waves, and rank by rank its waves
+    // are already near square (8 x 9.5 tiles on the 8192x4096x16384x4096 MLP).
+    gh.rank_fold = RANKS_IN_N;
+    ga.rank_fold = RANKS_IN_N;
     if ((st = launch_gemm(gh, s0)) || (st = launch_gemm(gx, s0))) return st;
     if (mode == 0) {
         // The rank sum of dX, beside the weight-gradient GEMMs when a second stream is given.
