@@ -417,6 +417,7 @@ def run_ours(args, rank, world, local_rank):
         "f3_infer_sbp_signature": {"us_per_call": host["sbp_signature_us"], "where": "host"},
         "f3_onnx_broadcast_checker": {"us_per_call": host["infer_broadcast_us"], "where": "host"},
         "a2_small_reshard_latency": small_reshard_latency(rtp, torch, dev),
+        "cfg_tiny_latency": tiny_configuration_latency(rtp, torch, dev),
         "f1_tp_mlp_backward": {"ms": round(bwd_ms, 4), "tflops": round(2 * MLP_FLOPS / (bwd_ms * 1e-3) / 1e12, 1),
                                "frac_bf16": round(2 * MLP_FLOPS / (bwd_ms * 1e-3) / 1e12 / bf16_peak, 4),
                                "dX_sum": "fused in the GEMM",
@@ -481,6 +482,98 @@ def run_ours(args, rank, world, local_rank):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def tiny_cases(torch, dev):
+    """The tiny exactness configuration on the device: the [[1,2],[3,4]] ONNX
+    splits, broadcast and split+broadcast, the OneFlow S(1) -> S(0) reshard of
+    the add example's second input, a P-sum of 4 [4,6] partials to B, and the
+    [4,8] x [8,16] x [16,8] MLP on 2 ranks (bf16)."""
+    import resharding_tensor_parallelism_gb300 as rtp
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    T = torch.tensor([[1.0, 2.0], [3.0, 4.0]], device=dev)
+    T8 = torch.arange(1, 9, dtype=torch.float32, device=dev).view(2, 4)
+    onnx = {"split axes 0 and 1 on 4 devices": ([0, 1, 2, 3], {}, [(0, 2), (1, 2)]),
+            "broadcast through device_map": ([-1], {-1: [0, 1]}, []),
+            "split axis 0, each piece broadcast to its group": ([-1, -2], {-1: [0, 1], -2: [2, 3]}, [(0, 2)])}
+    ops = {}
+    for name, (device, dmap, sd) in onnx.items():
+        spec = rtp.spec_from_onnx(2, device, dmap, sd)
+        out = rtp.shard(T, spec)
+        ops["shard: " + name] = lambda spec=spec, out=out: rtp.shard(T, spec, out=out)
+    s0, s1 = rtp.spec_nd_sbp((2,), (("S", 0),)), rtp.spec_nd_sbp((2,), (("S", 1),))
+    t2 = rtp.shard(T8, s1)
+    t2o = rtp.reshard(t2, (2, 4), s1, s0)
+    ops["reshard S(1) -> S(0), [2,4] on 2 ranks"] = lambda: rtp.reshard(t2, (2, 4), s1, s0, out=t2o)
+    parts = [torch.randn((4, 6), generator=g, device=dev) for _ in range(4)]
+    sp, sb = rtp.spec_nd_sbp((4,), ("P",)), rtp.spec_nd_sbp((4,), ("B",))
+    pb = rtp.reshard(parts, (4, 6), sp, sb)
+    ops["reshard P -> B, 4 partials [4,6]"] = lambda: rtp.reshard(parts, (4, 6), sp, sb, out=pb)
+    X = torch.randn((4, 8), generator=g, device=dev).bfloat16()
+    A = [torch.randn((8, 8), generator=g, device=dev).bfloat16() for _ in range(2)]
+    B = [torch.randn((8, 8), generator=g, device=dev).bfloat16() for _ in range(2)]
+    Z, Y = rtp.tp_mlp(X, A, B)
+    ops["tp_mlp [4,8] x [8,16] x [16,8], P=2"] = lambda: rtp.tp_mlp(X, A, B, Y=Y, Z=Z, mode=1)
+    return ops
+
+
+def tiny_configuration_latency(rtp, torch, dev, n: int = 100):
+    """Latency of each call of the tiny configuration, issued back to back as
+    direct calls (host checks, planning and launch every call): microseconds
+    per call from CUDA events. Latency-bound, so no roofline applies."""
+    out = {}
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    for name, fn in tiny_cases(torch, dev).items():
+        for _ in range(10):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = E(), E()
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        out[name] = round(e0.elapsed_time(e1) * 1e3 / n, 2)
+    return {"us_per_call": out, "calls_each": n}
+
+
+def cpu_tiny_baseline(n: int = 200):
+    """The oracle on the tiny configuration, the same operations as
+    tiny_cases: microseconds per call, one core."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    T = np.array([[1, 2], [3, 4]], np.float32)
+    T8 = np.arange(1, 9, dtype=np.float32).reshape(2, 4)
+    onnx = {"split axes 0 and 1 on 4 devices": ([0, 1, 2, 3], {}, [(0, 2), (1, 2)]),
+            "broadcast through device_map": ([-1], {-1: [0, 1]}, []),
+            "split axis 0, each piece broadcast to its group": ([-1, -2], {-1: [0, 1], -2: [2, 3]}, [(0, 2)])}
+    ops = {}
+    for name, (device, dmap, sd) in onnx.items():
+        lay = oracle.layout_from_onnx(2, device, dmap, sd)
+        ops["shard: " + name] = lambda lay=lay: oracle.shard(T, lay)
+    L0, L1 = oracle.Layout((2,), (("S", 0),)), oracle.Layout((2,), (("S", 1),))
+    t2 = oracle.shard(T8, L1)
+    ops["reshard S(1) -> S(0), [2,4] on 2 ranks"] = lambda: oracle.reshard(t2, (2, 4), L1, L0)
+    parts = [synth.normal(100 + k, (4, 6), "f32") for k in range(4)]
+    LP, LB = oracle.Layout((4,), ("P",)), oracle.Layout((4,), ("B",))
+    ops["reshard P -> B, 4 partials [4,6]"] = lambda: oracle.reshard(parts, (4, 6), LP, LB)
+    X = synth.normal(0, (4, 8), "bf16")
+    A = [synth.normal(1 + i, (8, 8), "bf16") for i in range(2)]
+    B = [synth.normal(3 + i, (8, 8), "bf16") for i in range(2)]
+    ops["tp_mlp [4,8] x [8,16] x [16,8], P=2"] = lambda: oracle.tp_mlp(X, A, B)
+    out = {}
+    for name, fn in ops.items():
+        fn()
+        t = time.perf_counter()
+        for _ in range(n):
+            fn()
+        out[name] = round((time.perf_counter() - t) / n * 1e6, 2)
+    return {"us_per_call": out, "cores": 1, "kind": "oracle", "calls_each": n}
 
 
 def small_reshard_latency(rtp, torch, dev, n: int = 100):
@@ -661,6 +754,7 @@ def cpu_baseline(max_seconds: float = 12.0, with_mlp: bool = False, cases=None):
            "seconds": round(total_s, 2), "host_cores": os.cpu_count()}
     if with_mlp:
         out["tp_mlp"] = cpu_mlp_baseline()
+        out["tiny"] = cpu_tiny_baseline()
     return out
 
 
