@@ -67,7 +67,8 @@ constexpr int EPI_WARPS = 4;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int EPI_CHUNKS = BN / 32 / (EPI_WARPS / 4);  // 32-column chunks per epilogue warp
 constexpr uint32_t TMEM_COLS = 2 * BN;
-constexpr int GROUP_M = 16;
+constexpr int GROUP_M = 16;        // M tiles per raster block when K < 8192
+constexpr int GROUP_M_LONG_K = 8;  // ... and when K >= 8192
 constexpr int kOverlapBlocksPerSm = 1;  // reduction blocks per SM while a GEMM runs beside it
 constexpr int MAX_GROUPS = 8;
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;
@@ -107,10 +108,14 @@ struct GemmArgs {
     // Tile order of a non-fused launch over several groups (ranks):
     //   RANKS_OUTER  group by group;
     //   RANKS_IN_N   the groups' N tiles form one N range. For groups with the
-    //                same A operand (X in X A_i): each block of GROUP_M A row
+    //                same A operand (X in X A_i): each block of group_m A row
     //                tiles then stays in L2 while every group's B columns stream
     //                past it, instead of being fetched again for every group.
     int32_t rank_fold;
+    // M tiles per raster block (set at launch from the K extent): the tiles in
+    // flight at once cover group_m rows of tiles and about 76 / group_m
+    // columns of tiles.
+    int32_t group_m;
 };
 
 __device__ unsigned int g_tp_error;
@@ -254,7 +259,7 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32])
 }
 
 // Tile index -> (group, M tile, N tile). Within an (M range, N range) the
-// tiles go in blocks of GROUP_M M tiles, N tile after N tile within a block,
+// tiles go in blocks of group_m M tiles, N tile after N tile within a block,
 // so the tiles in flight at once share their A rows and B columns in L2. The
 // group is the outermost index, or part of the N range (rank_fold). Both maps
 // are bijections of [0, groups * m_tiles * n_tiles).
@@ -265,9 +270,9 @@ __device__ __forceinline__ void tile_coords(const GemmArgs& a, int tile, int& g,
     g = per_group ? tile / per_group : 0;
     const int r = tile - g * per_group;
     const int ntiles = in_n ? a.groups * a.n_tiles : a.n_tiles;
-    const int span = GROUP_M * ntiles;
-    const int first_m = (r / span) * GROUP_M;
-    const int rows = min(a.m_tiles - first_m, GROUP_M);
+    const int span = a.group_m * ntiles;
+    const int first_m = (r / span) * a.group_m;
+    const int rows = min(a.m_tiles - first_m, a.group_m);
     const int w = r % span;
     mt = first_m + w % rows;
     nt = w / rows;
@@ -751,6 +756,13 @@ int launch_gemm_t(GemmArgs& args, cudaStream_t stream)
         nclusters = n;
     }
     args.total_tiles = (args.fused ? 1 : args.groups) * args.m_tiles * args.n_tiles;
+    // With a short K a block of group_m A row tiles stays in L2 while the B
+    // columns stream past it, so tall blocks pay. With a long K no operand
+    // panel survives in L2 from one wave of tiles to the next, and each wave
+    // reads every row and column panel it covers: near-square waves (8 x 9.5
+    // tiles instead of 16 x 4.75) read the fewest.
+    const int64_t k_extent = (int64_t)(args.fused ? args.groups : 1) * args.kb_per_group * BK;
+    args.group_m = k_extent >= 8192 ? GROUP_M_LONG_K : GROUP_M;
     const int clusters = args.total_tiles < nclusters ? args.total_tiles : nclusters;
     if (clusters <= 0) return RTP_OK;
     cfg.gridDim = dim3(2 * clusters);
