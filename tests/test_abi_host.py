@@ -342,3 +342,31 @@ def test_overlapping_source_and_destination_are_rejected():
     pieces = rtp._ptrs([0x30020, 0x40000])  # rank 0's piece inside the full tensor
     rc = lib.rtp_shard(rtp.F32, 2, shape, full, ctypes.byref(s0), pieces, None)
     assert rc == -1 and "overlaps" in rtp.last_error()
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without librtp.so the binding raises on first use: there is no CPU or
+    library fallback behind any call. Run in a fresh interpreter whose copy of
+    the package has no compiled library next to it."""
+    import shutil
+    import subprocess
+    import sys
+
+    pkg = tmp_path / "resharding_tensor_parallelism_gb300"
+    pkg.mkdir()
+    src = os.path.join(ROOT, "resharding_tensor_parallelism_gb300")
+    for f in ("__init__.py", "_build.py"):
+        shutil.copy(os.path.join(src, f), pkg / f)
+    code = ("import resharding_tensor_parallelism_gb300 as rtp\n"
+            "for call in (lambda: rtp.lib(), lambda: rtp.spec_from_dims_mapping([0, -1], [2]),\n"
+            "             lambda: rtp.version()):\n"
+            "    try:\n"
+            "        call()\n"
+            "    except ImportError as e:\n"
+            "        assert 'librtp.so is not built' in str(e)\n"
+            "    else:\n"
+            "        raise SystemExit('no error without the library')\n"
+            "print(rtp.__file__)\n")
+    out = subprocess.run([sys.executable, "-c", code], cwd=str(tmp_path), capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.strip().startswith(str(tmp_path)), out.stdout  # the copy without a library was imported
