@@ -12,6 +12,8 @@
 #include <algorithm>
 #include <cstring>
 #include <map>
+#include <string>
+#include <unordered_map>
 
 #include "rtp_internal.h"
 
@@ -230,6 +232,43 @@ int check_no_overlap(const char* fn, std::vector<std::pair<uintptr_t, uintptr_t>
     return RTP_OK;
 }
 
+// The planner reads, of each spec, the mesh shape, the rank of every mesh
+// position and each mesh dim's kind and axis; the key holds exactly those
+// (unused array slots may hold anything and are left out).
+void append_spec(std::string* k, const rtp_spec& s)
+{
+    const int64_t n = num_ranks(s);
+    k->append(reinterpret_cast<const char*>(&s.mesh_ndim), sizeof s.mesh_ndim);
+    k->append(reinterpret_cast<const char*>(s.mesh_shape), sizeof(int64_t) * (size_t)s.mesh_ndim);
+    k->append(reinterpret_cast<const char*>(s.rank_ids), sizeof(int32_t) * (size_t)n);
+    k->append(reinterpret_cast<const char*>(s.sbp_kind), sizeof(int32_t) * (size_t)s.mesh_ndim);
+    k->append(reinterpret_cast<const char*>(s.sbp_axis), sizeof(int32_t) * (size_t)s.mesh_ndim);
+}
+
+// plan_reshard with a per-thread cache: a repeated (shape, src, dst) reuses its
+// task list (planning 64 region intersections takes about 13 us on the host).
+// Specs must have passed check_spec. The list stays valid until this thread's
+// next call.
+int cached_plan(int ndim, const int64_t* shape, const rtp_spec& src, const rtp_spec& dst,
+                const std::vector<PlanTask>** out)
+{
+    static thread_local std::unordered_map<std::string, std::vector<PlanTask>> cache;
+    std::string key(reinterpret_cast<const char*>(&ndim), sizeof ndim);
+    key.append(reinterpret_cast<const char*>(shape), sizeof(int64_t) * (size_t)ndim);
+    append_spec(&key, src);
+    append_spec(&key, dst);
+    auto it = cache.find(key);
+    if (it == cache.end()) {
+        std::vector<PlanTask> tasks;
+        int st = plan_reshard(ndim, shape, src, dst, &tasks);
+        if (st) return st;
+        if (cache.size() >= 256) cache.clear();
+        it = cache.emplace(std::move(key), std::move(tasks)).first;
+    }
+    *out = &it->second;
+    return RTP_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -243,8 +282,9 @@ int rtp_reshard(rtp_dtype dtype, int ndim, const int64_t* shape, const void* con
     if (!src || !dst || !src_dev || !dst_dev) return fail(RTP_EINVAL, "%s: NULL spec or buffer array", fn);
     if ((st = check_spec(ndim, *src, "rtp_reshard (src)"))) return st;
     if ((st = check_spec(ndim, *dst, "rtp_reshard (dst)"))) return st;
-    std::vector<PlanTask> tasks;
-    if ((st = plan_reshard(ndim, shape, *src, *dst, &tasks))) return st;
+    const std::vector<PlanTask>* plan = nullptr;
+    if ((st = cached_plan(ndim, shape, *src, *dst, &plan))) return st;
+    const std::vector<PlanTask>& tasks = *plan;
     int es = element_size(dtype);
     if ((st = check_pointers(fn, "source", tasks, src_dev, true, es))) return st;
     if ((st = check_pointers(fn, "destination", tasks, (const void* const*)dst_dev, false, es))) return st;
@@ -264,8 +304,9 @@ int rtp_shard(rtp_dtype dtype, int ndim, const int64_t* shape, const void* full,
     if (!spec || !shard_dev) return fail(RTP_EINVAL, "%s: NULL spec or buffer array", fn);
     if ((st = check_spec(ndim, *spec, fn))) return st;
     rtp_spec whole = whole_tensor_spec();
-    std::vector<PlanTask> tasks;
-    if ((st = plan_reshard(ndim, shape, whole, *spec, &tasks))) return st;
+    const std::vector<PlanTask>* plan = nullptr;
+    if ((st = cached_plan(ndim, shape, whole, *spec, &plan))) return st;
+    const std::vector<PlanTask>& tasks = *plan;
     const void* srcs[1] = {full};
     int es = element_size(dtype);
     if ((st = check_pointers(fn, "full-tensor", tasks, srcs, true, es))) return st;
@@ -286,8 +327,9 @@ int rtp_reshard_cost(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_
     if (!src || !dst) return fail(RTP_EINVAL, "%s: NULL spec", fn);
     if ((st = check_spec(ndim, *src, "rtp_reshard_cost (src)"))) return st;
     if ((st = check_spec(ndim, *dst, "rtp_reshard_cost (dst)"))) return st;
-    std::vector<PlanTask> tasks;
-    if ((st = plan_reshard(ndim, shape, *src, *dst, &tasks))) return st;
+    const std::vector<PlanTask>* plan = nullptr;
+    if ((st = cached_plan(ndim, shape, *src, *dst, &plan))) return st;
+    const std::vector<PlanTask>& tasks = *plan;
     int64_t rd = 0, wr = 0, es = element_size(dtype);
     for (const auto& t : tasks) {
         int64_t v = t.rows * t.cols * es;
@@ -310,8 +352,9 @@ int rtp_reshard_forms(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp
     if (!src || !dst || !counts) return fail(RTP_EINVAL, "%s: NULL argument", fn);
     if ((st = check_spec(ndim, *src, "rtp_reshard_forms (src)"))) return st;
     if ((st = check_spec(ndim, *dst, "rtp_reshard_forms (dst)"))) return st;
-    std::vector<PlanTask> tasks;
-    if ((st = plan_reshard(ndim, shape, *src, *dst, &tasks))) return st;
+    const std::vector<PlanTask>* plan = nullptr;
+    if ((st = cached_plan(ndim, shape, *src, *dst, &plan))) return st;
+    const std::vector<PlanTask>& tasks = *plan;
     return classify_tasks(dtype, tasks, counts);
 }
 

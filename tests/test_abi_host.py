@@ -370,3 +370,57 @@ def test_missing_library_fails_loudly(tmp_path):
     out = subprocess.run([sys.executable, "-c", code], cwd=str(tmp_path), capture_output=True, text=True)
     assert out.returncode == 0, out.stderr
     assert out.stdout.strip().startswith(str(tmp_path)), out.stdout  # the copy without a library was imported
+
+
+def test_plan_cache_returns_each_layouts_own_plan():
+    """shard / reshard and the cost and form queries reuse a per-thread cache
+    of planned tasks, keyed by the shape and both layouts. Over interleaved
+    repeats of many (shape, src, dst) triples, more than the cache holds (it
+    is then cleared), the planned bytes stay those the oracle's piece geometry
+    gives (every destination piece written; each distinct value-holding
+    destination box read once per partial member), the form counts stay the
+    first call's, and a layout whose unused array slots hold other values
+    finds the same plan."""
+    import random
+
+    def expected(shape, mesh, src_e, dst_e):
+        src_l, dst_l = oracle.Layout(mesh, src_e), oracle.Layout(mesh, dst_e)
+        n = int(np.prod(mesh))
+        vol = lambda lo, hi: int(np.prod([h - l for l, h in zip(lo, hi)]))
+        members = int(np.prod([m for m, e in zip(mesh, src_e) if e == "P"]))
+        wr, boxes = 0, set()
+        for r in range(n):
+            lo, hi, hv = oracle.shard_box(shape, dst_l, r)
+            wr += vol(lo, hi) * 4
+            if hv and vol(lo, hi):
+                boxes.add((tuple(lo), tuple(hi)))
+        rd = sum(vol(lo, hi) for lo, hi in boxes) * 4 * members
+        return rd, wr
+
+    meshes = [(2,), (4,), (2, 2), (8,), (2, 4)]
+    rng = random.Random(5)
+    cases = []
+    for _ in range(300):
+        mesh = meshes[rng.randrange(len(meshes))]
+        shape = tuple(rng.randint(1, 40) for _ in range(rng.randint(1, 3)))
+        opts = [("S", a) for a in range(len(shape))] + ["B", "P"]
+        src_e = tuple(opts[rng.randrange(len(opts))] for _ in mesh)
+        dst_e = tuple(opts[rng.randrange(len(opts) - 1)] for _ in mesh)
+        cases.append((shape, rtp.spec_nd_sbp(mesh, src_e), rtp.spec_nd_sbp(mesh, dst_e),
+                      expected(shape, mesh, src_e, dst_e)))
+    forms = {}
+    for _ in range(3):
+        order = list(range(len(cases)))
+        rng.shuffle(order)
+        for i in order:
+            sh, s, d, want = cases[i]
+            assert rtp.reshard_cost(rtp.F32, sh, s, d)[:2] == want, (sh, s, d)
+            assert forms.setdefault(i, rtp.reshard_forms(rtp.F32, sh, s, d)) == rtp.reshard_forms(rtp.F32, sh, s, d)
+    # values beyond the used slots of each array: the same plan
+    sh, s, d, want = cases[0]
+    noisy = rtp.Spec.from_buffer_copy(bytes(s))
+    for p in range(s.num_ranks, rtp.MAX_RANKS):
+        noisy.rank_ids[p] = 77
+    for m in range(s.mesh_ndim, rtp.MAX_MESH_NDIM):
+        noisy.mesh_shape[m], noisy.sbp_kind[m], noisy.sbp_axis[m] = 9, 5, 3
+    assert rtp.reshard_cost(rtp.F32, sh, noisy, d)[:2] == want
