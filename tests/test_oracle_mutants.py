@@ -4,7 +4,9 @@ Each case plants one mistake in a copy of the oracle's source (on the CPU,
 never in the CUDA path): the split order, the uneven-split rule, a dropped
 partial, a lost partial mesh dim, the GELU scale, a dropped GELU' term, a
 transposed operand, the wrong gradient in a product, a dropped rank, the
-broadcast rule's intersection. It builds that copy, points the oracle module at
+broadcast rule's intersection, the reshape rule's surviving member, the bf16
+tie rule, the partial-max identity, whose SBP the CopyCost reads, and the
+ONNX device placement. It builds that copy, points the oracle module at
 it, and checks that at least one of the named pin tests fails.
 """
 import os
@@ -58,6 +60,27 @@ MUTANTS = [
      "                    if (i < L[dk] || i >= H[dk]) ok = false;",
      "                    if (i < L[dk] && i >= H[dk]) ok = false;",
      ["test_broadcast_rule_page_examples", "test_broadcast_rule_by_execution"]),
+    ("reshape keeps the innermost member's split",
+     "        int li = i0, lo = o0;\n        while (li < i - 1 && in_shape[li] == 1) ++li;\n"
+     "        while (lo < o - 1 && out_shape[lo] == 1) ++lo;",
+     "        int li = i - 1, lo = o - 1;",
+     ["test_reshape_rule_by_brute_force", "test_reshape_configuration_cases", "test_paddle_dimtrans_examples"]),
+    ("bf16 ties rounded away from zero",
+     "        double r = std::nearbyint(x / q) * q;",
+     "        double r = std::round(x / q) * q;",
+     ["test_bf16_rounding_special_values", "test_bf16_rounding_matches_torch_on_floats"]),
+    ("partial max padded with +inf",
+     "    if (reduction == 'X') return -INFINITY;",
+     "    if (reduction == 'X') return INFINITY;",
+     ["test_shard_to_partial_min_max_holds_identity", "test_partial_min_max_against_numpy"]),
+    ("CopyCost read from the candidate, not the input",
+     "                if (k != 'S') partial_or_broadcast = true;",
+     "                if (c.dims[d].first != 'S') partial_or_broadcast = true;",
+     ["test_sbp_signature_page_examples", "test_sbp_signature_invariants"]),
+    ("ONNX devices placed group by group transposed",
+     "        for (int64_t t = 0; t < gsize; ++t) L.devices[s * gsize + t] = (int32_t)members[s][t];",
+     "        for (int64_t t = 0; t < gsize; ++t) L.devices[t * n_device + s] = (int32_t)members[s][t];",
+     ["test_onnx_sharding_examples", "test_split_broadcast_follows_rule_not_printed_value"]),
 ]
 
 
