@@ -321,9 +321,11 @@ int rtp_infer_broadcast(int n_in, const int32_t* in_ndims, const int64_t* const*
  * tp_size in ColossalAI's Linear1D_Col): F % P == 0, M % chunks == 0, K, F/P
  * and N / col_blocks multiples of 8 (16-byte rows); P <= 8 (else
  * RTP_EUNSUPPORTED); all pointers 16-byte aligned (else RTP_EINVAL).
+ * M == 0 (no tokens) launches nothing; the buffers with M rows (X, Y,
+ * partials, Z) may then be NULL.
  * Errors leave nothing launched. The kernels allocate nothing; the first call
- * on a device sets the GEMM kernel's shared-memory limit and creates two
- * events used to order s0 and s1.
+ * on a device sets the GEMM kernel's shared-memory limit and, per host thread,
+ * creates two events used to order s0 and s1.
  */
 int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X, const void* const* A_shards,
                const void* const* B_shards, void* const* Y, void* const* partials, float* Z, int mode, int chunks,
@@ -385,7 +387,8 @@ int rtp_tp_mlp_backward(int P, int64_t M, int64_t K, int64_t F, int64_t N, const
  * from the shards directly and the row-parallel GEMM sums the ranks in its
  * accumulator and writes each row to its shard. Requires M % P == 0 and
  * (M/P) % 128 == 0, K, F/P and N multiples of 8, P <= 8 (else RTP_ESHAPE /
- * RTP_EUNSUPPORTED); pointers 16-byte aligned.
+ * RTP_EUNSUPPORTED); pointers 16-byte aligned. M == 0 launches nothing, and
+ * X_shards, Y and Z_shards may then be NULL.
  */
 int rtp_tp_mlp_sp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* const* X_shards,
                   const void* const* A_shards, const void* const* B_shards, void* const* Y, float* const* Z_shards,

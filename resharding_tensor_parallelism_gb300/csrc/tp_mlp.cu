@@ -831,7 +831,7 @@ int tp_mlp_impl(const char* fn, int P, int64_t M, int64_t K, int64_t F, int64_t 
                 void* const* partials, float* Z, int mode, int chunks, int col_blocks, rtp_stream s0_, rtp_stream s1_)
 {
     if (P < 1 || P > MAX_GROUPS) return fail(RTP_EUNSUPPORTED, "%s: P = %d outside [1, %d]", fn, P, MAX_GROUPS);
-    if (!X || !A_shards || !B_shards || !Y || !Z) return fail(RTP_EINVAL, "%s: NULL argument", fn);
+    if (!A_shards || !B_shards || !Y) return fail(RTP_EINVAL, "%s: NULL argument", fn);
     if (mode != 0 && mode != 1) return fail(RTP_EINVAL, "%s: mode %d", fn, mode);
     if (mode == 0 && !partials) return fail(RTP_EINVAL, "%s: mode 0 needs partial buffers", fn);
     if (chunks != 1 && chunks != 2 && chunks != 4) return fail(RTP_EINVAL, "%s: chunks %d not in {1,2,4}", fn, chunks);
@@ -846,9 +846,12 @@ int tp_mlp_impl(const char* fn, int P, int64_t M, int64_t K, int64_t F, int64_t 
     if (N % (8 * col_blocks)) return fail(RTP_ESHAPE, "%s: N must be a multiple of %d", fn, 8 * col_blocks);
     if (M >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 31) || Fp >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31))
         return fail(RTP_ESHAPE, "%s: extents must stay below 2^31", fn);
+    // Buffers with M rows (X, Y, H, partials, Z) are empty, and may be NULL,
+    // when M == 0: then nothing is launched.
+    if (M > 0 && (!X || !Z)) return fail(RTP_EINVAL, "%s: NULL argument", fn);
     if (!aligned16(X) || !aligned16(Z)) return fail(RTP_EINVAL, "%s: X and Z must be 16-byte aligned", fn);
     for (int i = 0; i < P; ++i) {
-        if (!A_shards[i] || !B_shards[i] || !Y[i] || (mode == 0 && !partials[i]) || (H && !H[i]))
+        if (!A_shards[i] || !B_shards[i] || (M > 0 && (!Y[i] || (mode == 0 && !partials[i]) || (H && !H[i]))))
             return fail(RTP_EINVAL, "%s: NULL buffer for rank %d", fn, i);
         if (!aligned16(A_shards[i]) || !aligned16(B_shards[i]) || !aligned16(Y[i]) ||
             (mode == 0 && !aligned16(partials[i])) || (H && !aligned16(H[i])))
@@ -1111,7 +1114,9 @@ int rtp_tp_mlp_sp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void*
     if (M >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 31) || Fp >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31))
         return fail(RTP_ESHAPE, "%s: extents must stay below 2^31", fn);
     for (int i = 0; i < P; ++i) {
-        if (!X_shards[i] || !A_shards[i] || !B_shards[i] || !Y[i] || !Z_shards[i]) return fail(RTP_EINVAL, "%s: NULL buffer for rank %d", fn, i);
+        // X_shards, Y and Z_shards have rows of the M tokens: empty, and possibly NULL, when M == 0
+        if (!A_shards[i] || !B_shards[i] || (M > 0 && (!X_shards[i] || !Y[i] || !Z_shards[i])))
+            return fail(RTP_EINVAL, "%s: NULL buffer for rank %d", fn, i);
         if (!aligned16(X_shards[i]) || !aligned16(A_shards[i]) || !aligned16(B_shards[i]) || !aligned16(Y[i]) || !aligned16(Z_shards[i]))
             return fail(RTP_EINVAL, "%s: buffers of rank %d must be 16-byte aligned", fn, i);
     }

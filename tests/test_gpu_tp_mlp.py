@@ -83,7 +83,7 @@ def test_tiny_configuration():
 
 
 @pytest.mark.parametrize("M,K,F,N,P", [(300, 200, 528, 520, 2), (128, 64, 2048, 256, 8), (384, 136, 288, 264, 3),
-                                       (257, 1024, 1024, 512, 4)])
+                                       (257, 1024, 1024, 512, 4), (520, 264, 392, 136, 1)])
 def test_ragged_multi_tile(M, K, F, N, P):
     X, As, Bs = _inputs(M, K, F, N, P, seed=M + K)
     rows = np.arange(M)
@@ -178,6 +178,21 @@ def test_domino_from_two_host_threads():
     for t in threads:
         t.join()
     assert not errors, errors
+    assert rtp.device_error() == 0
+
+
+def test_no_tokens():
+    """M == 0: every form of the forward launches nothing and succeeds, with
+    the token-row buffers empty (their data pointers are NULL)."""
+    dev = lambda *s: torch.zeros(s, dtype=torch.bfloat16, device="cuda")
+    As, Bs = [dev(64, 128) for _ in range(2)], [dev(128, 64) for _ in range(2)]
+    for mode, chunks in ((1, 1), (0, 1), (0, 2)):
+        Z, Y = rtp.tp_mlp(dev(0, 64), As, Bs, mode=mode, chunks=chunks, s1=torch.cuda.Stream())
+        assert tuple(Z.shape) == (0, 64) and [tuple(y.shape) for y in Y] == [(0, 128)] * 2
+    Zs, Y = rtp.tp_mlp_sp([dev(0, 64)] * 2, As, Bs)
+    assert [tuple(z.shape) for z in Zs] == [(0, 64)] * 2
+    assert tuple(rtp.tp_mlp_noalloc(dev(0, 64), As, Bs).shape) == (0, 64)
+    torch.cuda.synchronize()
     assert rtp.device_error() == 0
 
 
