@@ -142,15 +142,27 @@ int rtp_spec_from_onnx(int ndim, int n_device, const int64_t* device, int n_grou
                        const int32_t* group_sizes, const int64_t* group_devices, int n_sharded, const int64_t* axes,
                        const int64_t* num_shards, rtp_spec* out);
 
-/* Checks a spec against a tensor rank; RTP_OK if usable. */
+/*
+ * Checks a spec against a tensor rank; RTP_OK if usable, else the reason
+ * ("ONNX multi-device proposal", validity check: a sharding spec the backend
+ * cannot honour is reported with its reason).
+ */
 int rtp_spec_check(int ndim, const rtp_spec* spec);
 
-/* Shape of rank `rank`'s piece of a tensor of shape `shape` (out_shape[ndim]). */
+/*
+ * Shape of rank `rank`'s piece of a tensor of shape `shape` (out_shape[ndim]),
+ * by the split rule of the ONNX page (index rule for multi-axis splits, outer
+ * axis first; uneven extents as in the note on divisibility, read as ceil-sized
+ * leading pieces).
+ */
 int rtp_shard_shape(int ndim, const int64_t* shape, const rtp_spec* spec, int rank, int64_t* out_shape);
 
 /*
  * Box [lo, hi) of the logical tensor covered by rank `rank`, and whether the
  * rank holds values (0 only for a non-zero partial coordinate when sharding).
+ * The split rule as in rtp_shard_shape; a broadcast mesh dim gives every rank
+ * of its group the same box (ONNX page, sharding as broadcast); the members of
+ * a partial group share one box (OneFlow page, partial sum).
  */
 int rtp_shard_box(int ndim, const int64_t* shape, const rtp_spec* spec, int rank, int64_t* lo, int64_t* hi,
                   int32_t* holds_value);
@@ -186,7 +198,9 @@ int rtp_reshard(rtp_dtype dtype, int ndim, const int64_t* shape, const void* con
 /*
  * Algorithmic traffic of a reshard (host only): bytes read (each distinct
  * source byte once; every partial read) and bytes written (every destination
- * byte), and the number of copy tasks and kernel launches it plans.
+ * byte), and the number of copy tasks and kernel launches it plans. The pages
+ * have no counterpart to this query: it reports the bytes that the
+ * measurements of this library divide by.
  */
 int rtp_reshard_cost(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_spec* src, const rtp_spec* dst,
                      int64_t* bytes_read, int64_t* bytes_written, int32_t* n_tasks, int32_t* n_launches);
@@ -199,7 +213,8 @@ int rtp_reshard_cost(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_
  * tensor map (short strided rows). Host only; assumes 256-byte aligned rank
  * buffers (as cudaMalloc returns) and the kernel alone on the GPU (beside
  * another kernel every task takes the register form). Same errors as
- * rtp_reshard_cost.
+ * rtp_reshard_cost. The pages have no counterpart: it describes this
+ * library's kernel.
  */
 int rtp_reshard_forms(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_spec* src, const rtp_spec* dst,
                       int32_t* counts);
@@ -333,7 +348,9 @@ int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
 
 /*
  * The fused forward of rtp_tp_mlp (mode 1, one chunk) that also keeps what the
- * backward pass needs: H_i = X A_i, the pre-activation, rounded to bf16.
+ * backward pass needs: H_i = X A_i, the pre-activation, rounded to bf16 (the
+ * forward of the ColossalAI "1D tensor parallelism" page, sections 2 and 2.1,
+ * keeping the input of the GELU for the backward of section 2.2).
  *   H         P bf16 [M, F/P] device pointers (caller-owned, 16-byte aligned)
  *   the rest  as in rtp_tp_mlp; Y_i = GELU of the float32 accumulator (not of
  *             the rounded H_i), so Y and Z are bit-identical to rtp_tp_mlp's
@@ -425,6 +442,7 @@ int rtp_tp_mlp_noalloc(int P, int64_t M, int64_t K, int64_t F, int64_t N, const 
  * (1 producer, 2 MMA waiting for operands, 3 MMA waiting for an accumulator,
  * 4 epilogue, 5 rtp_wait_selftest; 16: a bulk copy of the resharding kernel
  * did not complete within about 2 seconds, so that launch stopped early).
+ * The pages have no counterpart: this is the library's failure detection.
  */
 int rtp_device_error(rtp_stream stream, uint32_t* code);
 
@@ -448,10 +466,13 @@ int rtp_device_error(rtp_stream stream, uint32_t* code);
  */
 int rtp_wait_selftest(int kernel, unsigned long long limit_ns, uint32_t* out, rtp_stream stream);
 
-/* Text of the last error on the calling thread ("" if none). */
+/*
+ * Text of the last error on the calling thread ("" if none): the reason the
+ * ONNX page's validity check asks an implementation to report.
+ */
 const char* rtp_last_error(void);
 
-/* Library version string. */
+/* Library version string (no page counterpart). */
 const char* rtp_version(void);
 
 #ifdef __cplusplus
