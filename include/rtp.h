@@ -424,7 +424,9 @@ int rtp_tp_mlp_sp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void*
  * P * round_up(M * F/P * 2 bytes, 256) exceeds 16 MiB (about M * F <= 8 Mi
  * elements), and the other errors of rtp_tp_mlp.
  * The first call on a device finds the array's device address (with that
- * device current); make that first call before any stream capture.
+ * device current); make that first call before any stream capture. A device
+ * reset (cudaDeviceReset) after that first call is not supported: the array
+ * may then live at another address.
  * Every call uses the same array: calls that overlap on the GPU (on several
  * streams, or from several threads) race on it and must be ordered by the
  * caller.
@@ -465,6 +467,25 @@ int rtp_device_error(rtp_stream stream, uint32_t* code);
  * Asynchronous on `stream`.
  */
 int rtp_wait_selftest(int kernel, unsigned long long limit_ns, uint32_t* out, rtp_stream stream);
+
+/*
+ * Fault injection for tests of the host-side checks (no page counterpart: it
+ * exercises this library's own failure reporting without touching a GPU).
+ * Arms a one-shot fault on the calling thread and clears that thread's cache of
+ * reshard plans, so its next rtp_shard / rtp_reshard / rtp_reshard_cost /
+ * rtp_reshard_forms plans afresh:
+ *   RTP_HOOK_NONE        disarms;
+ *   RTP_HOOK_PLAN_SHIFT  the next plan built has the first destination offset
+ *                        of its first task moved by `arg` elements (a planted
+ *                        planning mistake). Every new plan is checked against
+ *                        both layouts' piece extents before use, so a shift that
+ *                        leaves the piece returns RTP_EINVAL, nothing launched;
+ *   RTP_HOOK_FAIL_ALLOC  the next planning step fails as if host memory ran
+ *                        out: the call returns RTP_ENOMEM, nothing launched.
+ * RTP_EINVAL for an unknown hook.
+ */
+enum { RTP_HOOK_NONE = 0, RTP_HOOK_PLAN_SHIFT = 1, RTP_HOOK_FAIL_ALLOC = 2 };
+int rtp_test_hook(int hook, int64_t arg);
 
 /*
  * Text of the last error on the calling thread ("" if none): the reason the

@@ -98,6 +98,7 @@ def _load():
         "rtp_infer_broadcast": [c_int, i32p, P(i64p), P(Spec), P(c_int), i64p, P(Spec)],
         "rtp_device_error": [vp, u32p],
         "rtp_wait_selftest": [c_int, ctypes.c_ulonglong, vp, vp],
+        "rtp_test_hook": [c_int, ctypes.c_int64],
         "rtp_tp_mlp_sp": [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vpp, vpp, vpp, vpp,
                           vpp, vp],
         "rtp_tp_mlp_noalloc": [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vpp, vpp,
@@ -563,7 +564,13 @@ def tp_mlp_sp(X_shards, A_shards, B_shards, Y=None, Z_shards=None, stream=None):
 
 def tp_mlp_noalloc(X, A_shards, B_shards, Z=None, stream=None):
     """Z = sum_i GELU(X A_i) B_i with the activations in the library's static
-    device scratch (for callers that cannot allocate). Returns Z."""
+    device scratch (for callers that cannot allocate). Returns Z.
+
+    Every call shares that one static array (16 MiB per device): calls that
+    overlap on the GPU, on several streams or from several threads, race on it
+    and must be ordered by the caller. The first call on a device finds the
+    array's address; make it before any stream capture, and do not reset the
+    device after it."""
     torch = _torch()
     P = len(A_shards)
     M, K = X.shape
@@ -600,6 +607,16 @@ def wait_selftest(limit_ns: int, out=None, stream=None, kernel: int = 0):
     _check_cuda([out], "wait_selftest")
     _check(_load().rtp_wait_selftest(int(kernel), int(limit_ns), out.data_ptr(), _stream_ptr(stream)))
     return out
+
+
+HOOK_NONE, HOOK_PLAN_SHIFT, HOOK_FAIL_ALLOC = 0, 1, 2
+
+
+def test_hook(hook: int, arg: int = 0) -> None:
+    """Arms a one-shot host-side fault for this thread's next reshard plan
+    (rtp_test_hook): HOOK_PLAN_SHIFT moves a planned destination offset by
+    `arg` elements, HOOK_FAIL_ALLOC fails the planner's next allocation."""
+    _check(_load().rtp_test_hook(int(hook), int(arg)))
 
 
 def version() -> str:

@@ -63,9 +63,9 @@ int parse_einsum(const char* s, int n_in, Parsed* p)
 
 extern "C" {
 
-int rtp_infer_spmd(const char* einsum, int n_in, const int32_t* const* in_dims_mappings, int mesh_ndim,
-                   int32_t* out_dims_mapping, uint32_t* out_partial_mask, uint32_t* in_needs_reshard_mask,
-                   int32_t* const* in_inferred)
+static int rtp_infer_spmd_body(const char* einsum, int n_in, const int32_t* const* in_dims_mappings, int mesh_ndim,
+                               int32_t* out_dims_mapping, uint32_t* out_partial_mask, uint32_t* in_needs_reshard_mask,
+                               int32_t* const* in_inferred)
 {
     if (!in_dims_mappings || !out_dims_mapping || !out_partial_mask || !in_needs_reshard_mask)
         return fail(RTP_EINVAL, "rtp_infer_spmd: NULL argument");
@@ -120,9 +120,19 @@ int rtp_infer_spmd(const char* einsum, int n_in, const int32_t* const* in_dims_m
     return RTP_OK;
 }
 
-int rtp_infer_reshape(int in_ndim, const int64_t* in_shape, const int32_t* in_dims_mapping, int out_ndim,
-                      const int64_t* out_shape, int mesh_ndim, const int64_t* mesh_shape, int32_t* in_after,
-                      int32_t* out_dims_mapping)
+int rtp_infer_spmd(const char* einsum, int n_in, const int32_t* const* in_dims_mappings, int mesh_ndim,
+                   int32_t* out_dims_mapping, uint32_t* out_partial_mask, uint32_t* in_needs_reshard_mask,
+                   int32_t* const* in_inferred)
+{
+    return guarded("rtp_infer_spmd", [&] {
+        return rtp_infer_spmd_body(einsum, n_in, in_dims_mappings, mesh_ndim, out_dims_mapping, out_partial_mask,
+                                   in_needs_reshard_mask, in_inferred);
+    });
+}
+
+static int rtp_infer_reshape_body(int in_ndim, const int64_t* in_shape, const int32_t* in_dims_mapping, int out_ndim,
+                                  const int64_t* out_shape, int mesh_ndim, const int64_t* mesh_shape, int32_t* in_after,
+                                  int32_t* out_dims_mapping)
 {
     const char* fn = "rtp_infer_reshape";
     if (!in_shape || !in_dims_mapping || !out_shape || !mesh_shape || !in_after || !out_dims_mapping)
@@ -189,12 +199,22 @@ int rtp_infer_reshape(int in_ndim, const int64_t* in_shape, const int32_t* in_di
     return RTP_OK;
 }
 
+int rtp_infer_reshape(int in_ndim, const int64_t* in_shape, const int32_t* in_dims_mapping, int out_ndim,
+                      const int64_t* out_shape, int mesh_ndim, const int64_t* mesh_shape, int32_t* in_after,
+                      int32_t* out_dims_mapping)
+{
+    return guarded("rtp_infer_reshape", [&] {
+        return rtp_infer_reshape_body(in_ndim, in_shape, in_dims_mapping, out_ndim, out_shape, mesh_ndim, mesh_shape,
+                                      in_after, out_dims_mapping);
+    });
+}
+
 }  // extern "C"
 
-extern "C" int rtp_infer_sbp_signature(int n_in, int ndim, const int64_t* shape, int elem_bytes, int mesh_ndim,
-                                       const int32_t* in_kinds, const int32_t* in_axes, const int32_t* constraint_kinds,
-                                       const int32_t* constraint_axes, int32_t* out_kinds, int32_t* out_axes,
-                                       double* out_cost, int32_t* out_order)
+static int rtp_infer_sbp_signature_body(int n_in, int ndim, const int64_t* shape, int elem_bytes, int mesh_ndim,
+                                        const int32_t* in_kinds, const int32_t* in_axes, const int32_t* constraint_kinds,
+                                        const int32_t* constraint_axes, int32_t* out_kinds, int32_t* out_axes,
+                                        double* out_cost, int32_t* out_order)
 {
     const char* fn = "rtp_infer_sbp_signature";
     if (!shape || !in_kinds || !in_axes || !out_kinds || !out_axes) return fail(RTP_EINVAL, "%s: NULL argument", fn);
@@ -277,6 +297,18 @@ extern "C" int rtp_infer_sbp_signature(int n_in, int ndim, const int64_t* shape,
     return RTP_OK;
 }
 
+extern "C" int rtp_infer_sbp_signature(int n_in, int ndim, const int64_t* shape, int elem_bytes, int mesh_ndim,
+                                       const int32_t* in_kinds, const int32_t* in_axes, const int32_t* constraint_kinds,
+                                       const int32_t* constraint_axes, int32_t* out_kinds, int32_t* out_axes,
+                                       double* out_cost, int32_t* out_order)
+{
+    return guarded("rtp_infer_sbp_signature", [&] {
+        return rtp_infer_sbp_signature_body(n_in, ndim, shape, elem_bytes, mesh_ndim, in_kinds, in_axes,
+                                            constraint_kinds, constraint_axes, out_kinds, out_axes, out_cost,
+                                            out_order);
+    });
+}
+
 // ---- ONNX sharding checker: broadcast n-ary element-wise operators ----------------
 //
 // "ONNX multi-device proposal", operator groups, broadcast n-ary element-wise
@@ -296,8 +328,8 @@ struct Interval {
 
 }  // namespace
 
-extern "C" int rtp_infer_broadcast(int n_in, const int32_t* in_ndims, const int64_t* const* in_shapes,
-                                   const rtp_spec* in_specs, int* out_ndim, int64_t* out_shape, rtp_spec* out_spec)
+static int rtp_infer_broadcast_body(int n_in, const int32_t* in_ndims, const int64_t* const* in_shapes,
+                                    const rtp_spec* in_specs, int* out_ndim, int64_t* out_shape, rtp_spec* out_spec)
 {
     using namespace rtp;
     const char* fn = "rtp_infer_broadcast";
@@ -486,4 +518,12 @@ extern "C" int rtp_infer_broadcast(int n_in, const int32_t* in_ndims, const int6
     *out_spec = o;
     clear_error();
     return RTP_OK;
+}
+
+extern "C" int rtp_infer_broadcast(int n_in, const int32_t* in_ndims, const int64_t* const* in_shapes,
+                                   const rtp_spec* in_specs, int* out_ndim, int64_t* out_shape, rtp_spec* out_spec)
+{
+    return guarded("rtp_infer_broadcast", [&] {
+        return rtp_infer_broadcast_body(n_in, in_ndims, in_shapes, in_specs, out_ndim, out_shape, out_spec);
+    });
 }

@@ -99,11 +99,60 @@ int make_task(int ndim, const int64_t* lo, const int64_t* hi, const Box& sbox, c
     return RTP_OK;
 }
 
+// One-shot test hooks of the calling thread (rtp_test_hook).
+thread_local int g_hook = RTP_HOOK_NONE;
+thread_local int64_t g_hook_arg = 0;
+
 }  // namespace
+
+void inject_alloc_fault()
+{
+    if (g_hook == RTP_HOOK_FAIL_ALLOC) {
+        g_hook = RTP_HOOK_NONE;
+        throw std::bad_alloc();
+    }
+}
+
+int check_task_bounds(const char* fn, const std::vector<PlanTask>& tasks, const std::vector<int64_t>& src_vol,
+                      const std::vector<int64_t>& dst_vol)
+{
+    for (size_t i = 0; i < tasks.size(); ++i) {
+        const PlanTask& t = tasks[i];
+        if (t.rows < 1 || t.cols < 1 || t.n_outer < 0 || t.n_outer > kMaxOuter)
+            return fail(RTP_EINVAL, "%s: planned task %zu has an empty or malformed region", fn, i);
+        int64_t rows = 1, sspan = 0, dspan = 0;  // offsets of the last row's first element
+        for (int k = 0; k < t.n_outer; ++k) {
+            if (t.ext[k] < 1 || t.sstr[k] < 0 || t.dstr[k] < 0)
+                return fail(RTP_EINVAL, "%s: planned task %zu has a malformed outer dim %d", fn, i, k);
+            rows *= t.ext[k];
+            sspan += (t.ext[k] - 1) * t.sstr[k];
+            dspan += (t.ext[k] - 1) * t.dstr[k];
+        }
+        if (rows != t.rows) return fail(RTP_EINVAL, "%s: planned task %zu has %lld rows, its dims %lld", fn, i,
+                                        (long long)t.rows, (long long)rows);
+        for (int side = 0; side < 2; ++side) {
+            const std::vector<Ref>& refs = side == 0 ? t.src : t.dst;
+            const std::vector<int64_t>& vol = side == 0 ? src_vol : dst_vol;
+            const int64_t span = (side == 0 ? sspan : dspan) + t.cols;
+            for (const Ref& r : refs) {
+                if (r.rank < 0 || (size_t)r.rank >= vol.size())
+                    return fail(RTP_EINVAL, "%s: planned task %zu names %s rank %d", fn, i, side ? "destination" : "source",
+                                r.rank);
+                if (r.offset < 0 || r.offset + span > vol[(size_t)r.rank])
+                    return fail(RTP_EINVAL,
+                                "%s: planned task %zu would %s elements [%lld, %lld) of %s piece %d, which holds %lld",
+                                fn, i, side ? "write" : "read", (long long)r.offset, (long long)(r.offset + span),
+                                side ? "destination" : "source", r.rank, (long long)vol[(size_t)r.rank]);
+            }
+        }
+    }
+    return RTP_OK;
+}
 
 int plan_reshard(int ndim, const int64_t* shape, const rtp_spec& src, const rtp_spec& dst,
                  std::vector<PlanTask>* tasks)
 {
+    inject_alloc_fault();
     tasks->clear();
     int64_t sc[RTP_MAX_RANKS * RTP_MAX_MESH_NDIM], dc[RTP_MAX_RANKS * RTP_MAX_MESH_NDIM];
     rank_coords(src, sc);
@@ -245,14 +294,30 @@ void append_spec(std::string* k, const rtp_spec& s)
     k->append(reinterpret_cast<const char*>(s.sbp_axis), sizeof(int32_t) * (size_t)s.mesh_ndim);
 }
 
+// Element count of every rank's piece (0 for pieces a reshard never touches).
+std::vector<int64_t> piece_volumes(int ndim, const int64_t* shape, const rtp_spec& spec)
+{
+    int64_t coords[RTP_MAX_RANKS * RTP_MAX_MESH_NDIM];
+    rank_coords(spec, coords);
+    std::vector<int64_t> v((size_t)num_ranks(spec));
+    for (size_t r = 0; r < v.size(); ++r)
+        v[r] = box_volume(ndim, rank_box(ndim, shape, spec, coords + r * RTP_MAX_MESH_NDIM));
+    return v;
+}
+
+// Per thread, like the rest of the launch state (no locking).
+thread_local std::unordered_map<std::string, std::vector<PlanTask>> g_plan_cache;
+
 // plan_reshard with a per-thread cache: a repeated (shape, src, dst) reuses its
 // task list (planning 64 region intersections takes about 13 us on the host).
-// Specs must have passed check_spec. The list stays valid until this thread's
-// next call.
-int cached_plan(int ndim, const int64_t* shape, const rtp_spec& src, const rtp_spec& dst,
+// A new plan is checked against both layouts' piece extents before it is used
+// or cached (check_task_bounds), so no planned access leaves its piece. Specs
+// must have passed check_spec. The list stays valid until this thread's next
+// call.
+int cached_plan(const char* fn, int ndim, const int64_t* shape, const rtp_spec& src, const rtp_spec& dst,
                 const std::vector<PlanTask>** out)
 {
-    static thread_local std::unordered_map<std::string, std::vector<PlanTask>> cache;
+    auto& cache = g_plan_cache;
     std::string key(reinterpret_cast<const char*>(&ndim), sizeof ndim);
     key.append(reinterpret_cast<const char*>(shape), sizeof(int64_t) * (size_t)ndim);
     append_spec(&key, src);
@@ -262,6 +327,12 @@ int cached_plan(int ndim, const int64_t* shape, const rtp_spec& src, const rtp_s
         std::vector<PlanTask> tasks;
         int st = plan_reshard(ndim, shape, src, dst, &tasks);
         if (st) return st;
+        if (g_hook == RTP_HOOK_PLAN_SHIFT) {  // a planted planning mistake (tests only)
+            g_hook = RTP_HOOK_NONE;
+            if (!tasks.empty() && !tasks[0].dst.empty()) tasks[0].dst[0].offset += g_hook_arg;
+        }
+        if ((st = check_task_bounds(fn, tasks, piece_volumes(ndim, shape, src), piece_volumes(ndim, shape, dst))))
+            return st;
         if (cache.size() >= 256) cache.clear();
         it = cache.emplace(std::move(key), std::move(tasks)).first;
     }
@@ -269,12 +340,8 @@ int cached_plan(int ndim, const int64_t* shape, const rtp_spec& src, const rtp_s
     return RTP_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-int rtp_reshard(rtp_dtype dtype, int ndim, const int64_t* shape, const void* const* src_dev, const rtp_spec* src,
-                void* const* dst_dev, const rtp_spec* dst, rtp_stream stream)
+int reshard_impl(rtp_dtype dtype, int ndim, const int64_t* shape, const void* const* src_dev, const rtp_spec* src,
+                 void* const* dst_dev, const rtp_spec* dst, rtp_stream stream)
 {
     const char* fn = "rtp_reshard";
     int st = check_common(fn, dtype, ndim, shape);
@@ -283,7 +350,7 @@ int rtp_reshard(rtp_dtype dtype, int ndim, const int64_t* shape, const void* con
     if ((st = check_spec(ndim, *src, "rtp_reshard (src)"))) return st;
     if ((st = check_spec(ndim, *dst, "rtp_reshard (dst)"))) return st;
     const std::vector<PlanTask>* plan = nullptr;
-    if ((st = cached_plan(ndim, shape, *src, *dst, &plan))) return st;
+    if ((st = cached_plan(fn, ndim, shape, *src, *dst, &plan))) return st;
     const std::vector<PlanTask>& tasks = *plan;
     int es = element_size(dtype);
     if ((st = check_pointers(fn, "source", tasks, src_dev, true, es))) return st;
@@ -295,8 +362,8 @@ int rtp_reshard(rtp_dtype dtype, int ndim, const int64_t* shape, const void* con
     return launch_tasks(dtype, tasks, src_dev, dst_dev, stream, nullptr);
 }
 
-int rtp_shard(rtp_dtype dtype, int ndim, const int64_t* shape, const void* full, const rtp_spec* spec,
-              void* const* shard_dev, rtp_stream stream)
+int shard_impl(rtp_dtype dtype, int ndim, const int64_t* shape, const void* full, const rtp_spec* spec,
+               void* const* shard_dev, rtp_stream stream)
 {
     const char* fn = "rtp_shard";
     int st = check_common(fn, dtype, ndim, shape);
@@ -305,7 +372,7 @@ int rtp_shard(rtp_dtype dtype, int ndim, const int64_t* shape, const void* full,
     if ((st = check_spec(ndim, *spec, fn))) return st;
     rtp_spec whole = whole_tensor_spec();
     const std::vector<PlanTask>* plan = nullptr;
-    if ((st = cached_plan(ndim, shape, whole, *spec, &plan))) return st;
+    if ((st = cached_plan(fn, ndim, shape, whole, *spec, &plan))) return st;
     const std::vector<PlanTask>& tasks = *plan;
     const void* srcs[1] = {full};
     int es = element_size(dtype);
@@ -318,8 +385,8 @@ int rtp_shard(rtp_dtype dtype, int ndim, const int64_t* shape, const void* full,
     return launch_tasks(dtype, tasks, srcs, shard_dev, stream, nullptr);
 }
 
-int rtp_reshard_cost(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_spec* src, const rtp_spec* dst,
-                     int64_t* bytes_read, int64_t* bytes_written, int32_t* n_tasks, int32_t* n_launches)
+int reshard_cost_impl(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_spec* src, const rtp_spec* dst,
+                      int64_t* bytes_read, int64_t* bytes_written, int32_t* n_tasks, int32_t* n_launches)
 {
     const char* fn = "rtp_reshard_cost";
     int st = check_common(fn, dtype, ndim, shape);
@@ -328,7 +395,7 @@ int rtp_reshard_cost(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_
     if ((st = check_spec(ndim, *src, "rtp_reshard_cost (src)"))) return st;
     if ((st = check_spec(ndim, *dst, "rtp_reshard_cost (dst)"))) return st;
     const std::vector<PlanTask>* plan = nullptr;
-    if ((st = cached_plan(ndim, shape, *src, *dst, &plan))) return st;
+    if ((st = cached_plan(fn, ndim, shape, *src, *dst, &plan))) return st;
     const std::vector<PlanTask>& tasks = *plan;
     int64_t rd = 0, wr = 0, es = element_size(dtype);
     for (const auto& t : tasks) {
@@ -343,8 +410,8 @@ int rtp_reshard_cost(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_
     return RTP_OK;
 }
 
-int rtp_reshard_forms(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_spec* src, const rtp_spec* dst,
-                      int32_t* counts)
+int reshard_forms_impl(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_spec* src, const rtp_spec* dst,
+                       int32_t* counts)
 {
     const char* fn = "rtp_reshard_forms";
     int st = check_common(fn, dtype, ndim, shape);
@@ -353,9 +420,49 @@ int rtp_reshard_forms(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp
     if ((st = check_spec(ndim, *src, "rtp_reshard_forms (src)"))) return st;
     if ((st = check_spec(ndim, *dst, "rtp_reshard_forms (dst)"))) return st;
     const std::vector<PlanTask>* plan = nullptr;
-    if ((st = cached_plan(ndim, shape, *src, *dst, &plan))) return st;
+    if ((st = cached_plan(fn, ndim, shape, *src, *dst, &plan))) return st;
     const std::vector<PlanTask>& tasks = *plan;
     return classify_tasks(dtype, tasks, counts);
+}
+
+}  // namespace
+
+extern "C" {
+
+int rtp_reshard(rtp_dtype dtype, int ndim, const int64_t* shape, const void* const* src_dev, const rtp_spec* src,
+                void* const* dst_dev, const rtp_spec* dst, rtp_stream stream)
+{
+    return guarded("rtp_reshard", [&] { return reshard_impl(dtype, ndim, shape, src_dev, src, dst_dev, dst, stream); });
+}
+
+int rtp_shard(rtp_dtype dtype, int ndim, const int64_t* shape, const void* full, const rtp_spec* spec,
+              void* const* shard_dev, rtp_stream stream)
+{
+    return guarded("rtp_shard", [&] { return shard_impl(dtype, ndim, shape, full, spec, shard_dev, stream); });
+}
+
+int rtp_reshard_cost(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_spec* src, const rtp_spec* dst,
+                     int64_t* bytes_read, int64_t* bytes_written, int32_t* n_tasks, int32_t* n_launches)
+{
+    return guarded("rtp_reshard_cost", [&] {
+        return reshard_cost_impl(dtype, ndim, shape, src, dst, bytes_read, bytes_written, n_tasks, n_launches);
+    });
+}
+
+int rtp_reshard_forms(rtp_dtype dtype, int ndim, const int64_t* shape, const rtp_spec* src, const rtp_spec* dst,
+                      int32_t* counts)
+{
+    return guarded("rtp_reshard_forms", [&] { return reshard_forms_impl(dtype, ndim, shape, src, dst, counts); });
+}
+
+int rtp_test_hook(int hook, int64_t arg)
+{
+    if (hook != RTP_HOOK_NONE && hook != RTP_HOOK_PLAN_SHIFT && hook != RTP_HOOK_FAIL_ALLOC)
+        return fail(RTP_EINVAL, "rtp_test_hook: unknown hook %d", hook);
+    g_hook = hook;
+    g_hook_arg = arg;
+    g_plan_cache.clear();  // the next reshard or shard plans afresh
+    return RTP_OK;
 }
 
 }  // extern "C"

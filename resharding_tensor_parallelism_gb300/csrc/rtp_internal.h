@@ -2,6 +2,8 @@
 #pragma once
 
 #include <cstdint>
+#include <exception>
+#include <new>
 #include <string>
 #include <vector>
 
@@ -13,6 +15,21 @@ namespace rtp {
 // Records a message for rtp_last_error() on this thread and returns `status`.
 int fail(int status, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 void clear_error();
+
+// Runs the body of an entry point that allocates host memory: a failed
+// allocation (std::bad_alloc) becomes RTP_ENOMEM, and no exception crosses the
+// C ABI.
+template <class F>
+int guarded(const char* fn, F&& body) noexcept
+{
+    try {
+        return body();
+    } catch (const std::bad_alloc&) {
+        return fail(RTP_ENOMEM, "%s: a host allocation failed", fn);
+    } catch (const std::exception& e) {
+        return fail(RTP_EUNSUPPORTED, "%s: internal error: %s", fn, e.what());
+    }
+}
 
 // ---- spec geometry -------------------------------------------------------------
 int64_t num_ranks(const rtp_spec& s);
@@ -62,6 +79,18 @@ int plan_reshard(int ndim, const int64_t* shape, const rtp_spec& src, const rtp_
 
 // The single-rank, broadcast spec of an unsharded tensor.
 rtp_spec whole_tensor_spec();
+
+// Every element a task touches lies inside the piece it reads or writes: for
+// each source (destination) reference, its first element offset is >= 0 and
+// its last is below src_vol[rank] (dst_vol[rank]), the piece's element count.
+// RTP_EINVAL (message names fn, the task and the piece) otherwise.
+int check_task_bounds(const char* fn, const std::vector<PlanTask>& tasks, const std::vector<int64_t>& src_vol,
+                      const std::vector<int64_t>& dst_vol);
+
+// Test hooks (rtp_test_hook), one-shot and per thread. inject_alloc_fault()
+// throws std::bad_alloc when the allocation-failure hook is armed (and
+// disarms it); it marks the host allocations of planning.
+void inject_alloc_fault();
 
 // ---- launches (boxing.cu) --------------------------------------------------------------
 // Executes planned tasks on `stream`; src/dst buffer arrays are indexed by Ref::rank.

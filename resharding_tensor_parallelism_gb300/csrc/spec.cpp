@@ -15,21 +15,21 @@
 namespace rtp {
 
 namespace {
-thread_local std::string g_last_error;
+// A fixed buffer, so that reporting an error (an allocation failure among
+// them) never allocates.
+thread_local char g_last_error[1024];
 }
 
 int fail(int status, const char* fmt, ...)
 {
-    char buf[1024];
     va_list ap;
     va_start(ap, fmt);
-    vsnprintf(buf, sizeof buf, fmt, ap);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
     va_end(ap);
-    g_last_error = buf;
     return status;
 }
 
-void clear_error() { g_last_error.clear(); }
+void clear_error() { g_last_error[0] = 0; }
 
 int64_t num_ranks(const rtp_spec& s)
 {
@@ -152,7 +152,7 @@ using namespace rtp;
 
 extern "C" {
 
-const char* rtp_last_error(void) { return g_last_error.c_str(); }
+const char* rtp_last_error(void) { return g_last_error; }
 
 const char* rtp_version(void) { return "rtp 0.1 (sm_103a)"; }
 
@@ -200,9 +200,9 @@ int rtp_spec_from_dims_mapping(int ndim, const int32_t* dims_mapping, int mesh_n
     return RTP_OK;
 }
 
-int rtp_spec_from_onnx(int ndim, int n_device, const int64_t* device, int n_groups, const int64_t* group_keys,
-                       const int32_t* group_sizes, const int64_t* group_devices, int n_sharded, const int64_t* axes,
-                       const int64_t* num_shards, rtp_spec* out)
+static int rtp_spec_from_onnx_body(int ndim, int n_device, const int64_t* device, int n_groups, const int64_t* group_keys,
+                                   const int32_t* group_sizes, const int64_t* group_devices, int n_sharded, const int64_t* axes,
+                                   const int64_t* num_shards, rtp_spec* out)
 {
     const char* fn = "rtp_spec_from_onnx";
     if (!device || !out || n_device < 1) return fail(RTP_EINVAL, "%s: empty device list", fn);
@@ -276,6 +276,16 @@ int rtp_spec_from_onnx(int ndim, int n_device, const int64_t* device, int n_grou
     if (st) return st;
     *out = sp;
     return RTP_OK;
+}
+
+int rtp_spec_from_onnx(int ndim, int n_device, const int64_t* device, int n_groups, const int64_t* group_keys,
+                       const int32_t* group_sizes, const int64_t* group_devices, int n_sharded, const int64_t* axes,
+                       const int64_t* num_shards, rtp_spec* out)
+{
+    return guarded("rtp_spec_from_onnx", [&] {
+        return rtp_spec_from_onnx_body(ndim, n_device, device, n_groups, group_keys, group_sizes, group_devices,
+                                       n_sharded, axes, num_shards, out);
+    });
 }
 
 int rtp_shard_box(int ndim, const int64_t* shape, const rtp_spec* spec, int rank, int64_t* lo, int64_t* hi,

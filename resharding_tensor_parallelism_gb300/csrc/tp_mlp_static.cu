@@ -30,7 +30,10 @@ constexpr size_t kAlign = 256;
 static __device__ __align__(256) unsigned char g_tp_static_scratch[kStaticScratchBytes];
 
 // Device address of the array, per device, found once with that device current
-// (threads racing on a first call find the same address).
+// (threads racing on a first call find the same address). The address belongs
+// to the device's context at that time: after a device reset
+// (cudaDeviceReset) the module is loaded again and the array may move, so this
+// entry point does not support a reset after its first call on a device.
 std::atomic<void*> g_scratch_addr[64];
 
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -46,8 +49,16 @@ extern "C" int rtp_tp_mlp_noalloc(int P, int64_t M, int64_t K, int64_t F, int64_
     if (M < 0 || K < 1 || F < 1 || N < 1 || F % P)
         return rtp::fail(RTP_ESHAPE, "%s: sizes M=%lld K=%lld F=%lld N=%lld P=%d", fn, (long long)M, (long long)K,
                          (long long)F, (long long)N, P);
-    const size_t per_rank = round_up((size_t)M * (size_t)(F / P) * 2u);
-    if (per_rank * (size_t)P > kStaticScratchBytes)
+    // Checked factor by factor first, so that no product below can wrap: each
+    // rank's activations must fit the array on their own before M x F/P is formed.
+    const size_t Fp = (size_t)(F / P);
+    if ((size_t)M > kStaticScratchBytes / 2 || Fp > kStaticScratchBytes / 2 ||
+        (M > 0 && (size_t)M * Fp > kStaticScratchBytes / 2))
+        return rtp::fail(RTP_ESHAPE,
+                         "%s: M=%lld x F/P=%zu bf16 activations of one rank exceed the static scratch of %zu bytes",
+                         fn, (long long)M, Fp, kStaticScratchBytes);
+    const size_t per_rank = round_up((size_t)M * Fp * 2u);
+    if (per_rank > kStaticScratchBytes / (size_t)P)
         return rtp::fail(RTP_ESHAPE,
                          "%s: the GELU activations need %zu bytes (M x F bf16, each rank padded to %zu bytes); "
                          "the static scratch holds %zu bytes (M x F <= about %zu elements)",

@@ -424,3 +424,63 @@ def test_plan_cache_returns_each_layouts_own_plan():
     for m in range(s.mesh_ndim, rtp.MAX_MESH_NDIM):
         noisy.mesh_shape[m], noisy.sbp_kind[m], noisy.sbp_axis[m] = 9, 5, 3
     assert rtp.reshard_cost(rtp.F32, sh, noisy, d)[:2] == want
+
+
+def test_planted_plan_mistake_is_rejected_before_any_launch():
+    """A planning mistake (a destination offset moved past its piece) is caught
+    by the host-side bounds check that every new plan passes before use: the
+    call fails with RTP_EINVAL and nothing is launched (the buffers are fake
+    host addresses that must never be touched). The layouts are chosen so that
+    the first task fills its destination piece exactly: any shift leaves it."""
+    shape = (4, 6)
+    whole, dst = rtp.spec_nd_sbp((1,), ("B",)), rtp.spec_nd_sbp((2,), (("S", 0),))
+    assert rtp.reshard_cost(rtp.F32, shape, whole, dst)[:2] == (96, 96)
+    for shift in (1, -1, 1000):
+        rtp.test_hook(rtp.HOOK_PLAN_SHIFT, shift)
+        with pytest.raises(rtp.RtpError) as e:
+            rtp.reshard_cost(rtp.F32, shape, whole, dst)
+        assert e.value.status == -1 and "planned task 0" in rtp.last_error()
+    rtp.test_hook(rtp.HOOK_PLAN_SHIFT, 0)  # a shift of 0 leaves the plan correct
+    assert rtp.reshard_cost(rtp.F32, shape, whole, dst)[:2] == (96, 96)
+    # through rtp_reshard and rtp_shard themselves, with fake pointers
+    lib = rtp.lib()
+    rtp.test_hook(rtp.HOOK_PLAN_SHIFT, 1)
+    rc = lib.rtp_reshard(rtp.F32, 2, rtp._i64(shape), rtp._ptrs([4096]), whole, rtp._ptrs([16384, 20480]), dst, None)
+    assert rc == -1 and "would write elements [1, 13) of destination piece 0, which holds 12" in rtp.last_error()
+    rtp.test_hook(rtp.HOOK_PLAN_SHIFT, -1)
+    rc = lib.rtp_shard(rtp.F32, 2, rtp._i64(shape), 4096, dst, rtp._ptrs([16384, 20480]), None)
+    assert rc == -1 and "planned task 0" in rtp.last_error()
+    # the rejected plans were not cached: a clean plan of the same layouts works
+    assert rtp.reshard_cost(rtp.F32, shape, whole, dst)[:2] == (96, 96)
+
+
+def test_injected_allocation_failure_returns_enomem():
+    """A host allocation that fails while planning becomes RTP_ENOMEM (no
+    exception crosses the C ABI) and nothing is launched; the next call
+    plans normally."""
+    shape = (8, 8)
+    src, dst = rtp.spec_nd_sbp((4,), ("P",)), rtp.spec_nd_sbp((2, 2), (("S", 0), ("S", 1)))
+    rtp.test_hook(rtp.HOOK_FAIL_ALLOC)
+    with pytest.raises(rtp.RtpError) as e:
+        rtp.reshard_cost(rtp.F32, shape, src, dst)
+    assert e.value.status == -6 and "allocation failed" in rtp.last_error()
+    assert rtp.reshard_cost(rtp.F32, shape, src, dst)[0] == 4 * 8 * 8 * 4
+    lib = rtp.lib()
+    rtp.test_hook(rtp.HOOK_FAIL_ALLOC)
+    rc = lib.rtp_reshard(rtp.F32, 2, rtp._i64(shape), rtp._ptrs([4096] * 4), src, rtp._ptrs([8192] * 4), dst, None)
+    assert rc == -6
+    rtp.test_hook(rtp.HOOK_FAIL_ALLOC)
+    rtp.test_hook(rtp.HOOK_NONE)  # disarmed before use
+    assert rtp.reshard_cost(rtp.F32, shape, src, dst)[0] == 4 * 8 * 8 * 4
+    assert rtp.lib().rtp_test_hook(7, 0) == -1
+
+
+def test_noalloc_size_check_cannot_wrap():
+    """Sizes whose activation bytes would wrap a 64-bit product are rejected on
+    the host (RTP_ESHAPE) before any CUDA call; the pointers are fake."""
+    lib = rtp.lib()
+    fake = rtp._ptrs([4096] * 8)
+    for (P, M, Fp) in [(1, 2 ** 30, 2 ** 30), (8, 2 ** 30, 2 ** 30), (8, 2 ** 31 - 1, 8), (2, 8, 2 ** 31 - 8),
+                       (8, 4096, 512)]:
+        rc = lib.rtp_tp_mlp_noalloc(P, M, 64, P * Fp, 64, 4096, fake, fake, 8192, None)
+        assert rc == -2 and "static scratch" in rtp.last_error(), (P, M, Fp, rc, rtp.last_error())
