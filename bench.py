@@ -45,6 +45,12 @@ CONFIG = {"workload": "resharding sweep [8,2048,4096] f32+bf16 on virtual meshes
           "l2": "flushed before every timed call: a 512 MiB write, then a 512 MiB read, so that no dirty line of "
                 "the flush is written back inside the timed region"}
 L2_FLUSH_BYTES = 512 * 1024 * 1024
+# What the reference arm (the CPU oracle) times: a bounded sample of the
+# resharding sweep, float32 only, on a slice of the activation tensor.
+REFERENCE_CONFIG = {"workload": "resharding sweep sample: the 12 float32 transitions (meshes 1x8 and 2x4) on a "
+                                "[8,256,4096] slice of the [8,2048,4096] activation tensor, called in turn",
+                    "parallelism": "virtual mesh of 8 ranks, single-threaded CPU oracle on rank 0",
+                    "l2": "host caches: each tensor is 32 MiB and the partials 256 MiB, larger than the host caches"}
 
 
 def _peaks():
@@ -279,20 +285,22 @@ def run_ours(args, rank, world, local_rank):
     def run_sp():
         rtp.tp_mlp_sp(sp_x, mlp["A"], mlp["B"], Y=mlp["Y"], Z_shards=sp_z)
 
-    def run_domino():
-        rtp.tp_mlp(dom["X"], dom["A"], dom["B"], Y=dom["Y"], partials=dom["parts"], Z=dom["Z"], mode=0, chunks=2,
-                   s1=s1)
-
-    def run_domino4():
-        rtp.tp_mlp(dom["X"], dom["A"], dom["B"], Y=dom["Y"], partials=dom["parts"], Z=dom["Z"], mode=0, chunks=4,
-                   s1=s1)
-
-    def run_domino2d():
-        rtp.tp_mlp(dom["X"], dom["A"], dom["B"], Y=dom["Y"], partials=dom["parts"], Z=dom["Z"], mode=0, chunks=2,
-                   col_blocks=2, s1=s1)
+    def domino(chunks, col_blocks, in_epilogue):
+        """The Domino schedule: the rank partials summed in the row-parallel
+        GEMM's epilogue (the default), or by kernels of their own on the
+        second stream, after each window."""
+        def run():
+            prev = rtp.tp_mlp_overlap(1 if in_epilogue else 0)
+            rtp.tp_mlp(dom["X"], dom["A"], dom["B"], Y=dom["Y"], partials=dom["parts"], Z=dom["Z"], mode=0,
+                       chunks=chunks, col_blocks=col_blocks, s1=s1)
+            rtp.tp_mlp_overlap(prev)
+        return run
 
     def run_serial():
+        """No overlap: the GEMMs, then one kernel sums the partials (one stream)."""
+        prev = rtp.tp_mlp_overlap(0)
         rtp.tp_mlp(dom["X"], dom["A"], dom["B"], Y=dom["Y"], partials=dom["parts"], Z=dom["Z"], mode=0, chunks=1)
+        rtp.tp_mlp_overlap(prev)
 
     def run_dom_fused():
         rtp.tp_mlp(dom["X"], dom["A"], dom["B"], Y=dom["Y"], Z=dom["Z"], mode=1)
@@ -307,19 +315,33 @@ def run_ours(args, rank, world, local_rank):
         rtp.tp_mlp_backward(mlp["X"], mlp["A"], mlp["B"], trn["H"], mlp["Y"], trn["dZ"], dH=trn["dH"], dX=trn["dX"],
                             dA=trn["dA"], dB=trn["dB"], mode=1)
 
-    def run_bwd_overlap():
-        rtp.tp_mlp_backward(mlp["X"], mlp["A"], mlp["B"], trn["H"], mlp["Y"], trn["dZ"], dH=trn["dH"], dX=trn["dX"],
-                            dA=trn["dA"], dB=trn["dB"], dX_partials=trn["parts"], mode=0, s1=s1)
+    def bwd_overlap(in_epilogue):
+        """Backward with the dX partials written and summed: in the dX GEMM's
+        epilogue (the default) or by a kernel of its own on the second stream
+        beside the weight-gradient GEMMs."""
+        def run():
+            prev = rtp.tp_mlp_overlap(1 if in_epilogue else 0)
+            rtp.tp_mlp_backward(mlp["X"], mlp["A"], mlp["B"], trn["H"], mlp["Y"], trn["dZ"], dH=trn["dH"],
+                                dX=trn["dX"], dA=trn["dA"], dB=trn["dB"], dX_partials=trn["parts"], mode=0, s1=s1)
+            rtp.tp_mlp_overlap(prev)
+        return run
 
     ops = [(label, (lambda c=c, i=i, s=s, o=o, d=d: rtp.reshard(i, SWEEP_SHAPE, s, d, out=o)), nbytes, nl)
            for (label, c, i, s, o, d, nbytes, nl) in sweep]
     shard_ops = [(label, (lambda T=T, sp=sp, o=o: rtp.shard(T, sp, out=o)), nbytes, nl)
                  for (label, T, sp, o, nbytes, nl) in shards]
-    launches_per_step = (sum(x[3] for x in ops) + sum(x[3] for x in shard_ops) +
-                         2 + 2 + 6 + 12 + 10 + 3 + 2 + 1 + 2 + 4 + 5)
-    # mlp 2, sequence parallel 2, domino 2 chunks x 3, 4 chunks x 3, 2 chunks x (1 + 2 column blocks x 2), serial 3,
-    # fused on the Domino shape 2, reduce 1, training forward 2, backward 4, backward with the separate, overlapped
-    # dX sum 5
+    # (kind, function, launches of the library's kernels per call)
+    mlp_ops = [("mlp", run_mlp, 2), ("sp", run_sp, 2),
+               # the pages' schedule: every window's sum a launch of its own on the second stream
+               ("domino", domino(2, 1, False), 2 * 3), ("domino4", domino(4, 1, False), 4 * 3),
+               ("domino2d", domino(2, 2, False), 2 * (1 + 2 * 2)),
+               # the sums in the row-parallel GEMM's epilogue: the GEMM launches only
+               ("domino_esum", domino(2, 1, True), 2 * 2), ("domino4_esum", domino(4, 1, True), 4 * 2),
+               ("domino2d_esum", domino(2, 2, True), 2 * 3), ("domino1_esum", domino(1, 1, True), 2),
+               ("serial", run_serial, 3), ("dom_fused", run_dom_fused, 2), ("reduce", run_reduce, 1),
+               ("train_fwd", run_train_fwd, 2), ("bwd", run_bwd, 4),
+               ("bwd_overlap", bwd_overlap(False), 5), ("bwd_overlap_esum", bwd_overlap(True), 4)]
+    launches_per_step = sum(x[3] for x in ops) + sum(x[3] for x in shard_ops) + sum(x[2] for x in mlp_ops)
     E = lambda: torch.cuda.Event(enable_timing=True)
 
     def step(record):
@@ -337,10 +359,7 @@ def run_ours(args, rank, world, local_rank):
             fn()
             e1.record()
             record.append(("reshard", label, e0, e1, nbytes))
-        for kind, fn in (("mlp", run_mlp), ("sp", run_sp), ("domino", run_domino), ("domino4", run_domino4),
-                         ("domino2d", run_domino2d), ("serial", run_serial),
-                         ("dom_fused", run_dom_fused), ("reduce", run_reduce), ("train_fwd", run_train_fwd), ("bwd", run_bwd),
-                         ("bwd_overlap", run_bwd_overlap)):
+        for kind, fn, _ in mlp_ops:
             flush.zero_()
             e0, e1 = E(), E()
             e0.record()
@@ -376,16 +395,10 @@ def run_ours(args, rank, world, local_rank):
     reshard_ms = sum(v[0] for (k, _), v in per.items() if k == "reshard")
     reshard_bytes = sum(v[2] * v[1] for (k, _), v in per.items() if k == "reshard")
     mlp_ms = per[("mlp", "mlp")][0]
-    dom_ms = per[("domino", "domino")][0] / args.steps
-    dom4_ms = per[("domino4", "domino4")][0] / args.steps
-    dom2d_ms = per[("domino2d", "domino2d")][0] / args.steps
-    ser_ms = per[("serial", "serial")][0] / args.steps
-    dfu_ms = per[("dom_fused", "dom_fused")][0] / args.steps
-    red_ms = per[("reduce", "reduce")][0] / args.steps
-    sp_ms = per[("sp", "sp")][0] / args.steps
-    tf_ms = per[("train_fwd", "train_fwd")][0] / args.steps
-    bwd_ms = per[("bwd", "bwd")][0] / args.steps
-    bwo_ms = per[("bwd_overlap", "bwd_overlap")][0] / args.steps
+    avg = lambda kind: per[(kind, kind)][0] / args.steps
+    ser_ms, dfu_ms, red_ms, sp_ms = avg("serial"), avg("dom_fused"), avg("reduce"), avg("sp")
+    tf_ms, bwd_ms, bwo_ms, bwoe_ms = avg("train_fwd"), avg("bwd"), avg("bwd_overlap"), avg("bwd_overlap_esum")
+    hide = lambda ms: round((ser_ms - ms) / red_ms, 3) if red_ms > 0 else None
 
     def max_over_ranks(x):
         return reduce_over_ranks(dist, x, dev, "max")
@@ -396,6 +409,14 @@ def run_ours(args, rank, world, local_rank):
         return by / (ms * 1e-3) / 1e9 if ms > 0 else None
 
     red_bytes = 8 * DOMINO["M"] * DOMINO["N"] * 4 + DOMINO["M"] * DOMINO["N"] * 4
+    # Domino schedules on the Llama-70B MLP shape (2 and 4 row chunks; 2 chunks x 2 column blocks of B)
+    dom_rows = {}
+    for kind, name in (("domino", "2_chunks"), ("domino4", "4_chunks"), ("domino2d", "2_chunks_2_column_blocks")):
+        ms, ms_e = avg(kind), avg(kind + "_esum")
+        dom_rows[name] = {"ms": round(ms, 4), "hiding": hide(ms), "ms_epilogue_sum": round(ms_e, 4),
+                          "hiding_epilogue_sum": hide(ms_e)}
+    ms1 = avg("domino1_esum")
+    dom_rows["1_chunk_epilogue_sum"] = {"ms": round(ms1, 4), "hiding": hide(ms1)}
     host = host_inference_timings(rtp)
     rows = {
         "a1_shard": {"gbs": round(gbs_of("shard"), 1), "frac_hbm": round(gbs_of("shard") / hbm_peak, 4),
@@ -406,16 +427,10 @@ def run_ours(args, rank, world, local_rank):
                          "frac_hbm": round(gbs_of("reshard", lambda l: "P8" in l) / hbm_peak, 4)},
         "a4_infer_spmd": {"us_per_call": host["infer_spmd_us"], "where": "host"},
         "a4p_reshape_rule": {"us_per_call": host["infer_reshape_us"], "where": "host"},
-        "a5_a6_a7_tp_mlp_fused": {"tflops": None, "frac_bf16": None},
         "a7_reduce_separate": {"ms": round(red_ms, 4), "gbs": round(red_bytes / (red_ms * 1e-3) / 1e9, 1),
                                "frac_hbm": round(red_bytes / (red_ms * 1e-3) / 1e9 / hbm_peak, 4),
                                "shape": "8 float32 partials [4096,8192] -> Z"},
         "a6_a7_separate_schedule": {"ms": round(ser_ms, 4), "tflops": round(DOMINO_FLOPS / (ser_ms * 1e-3) / 1e12, 1)},
-        "a8_domino": {"ms": round(dom_ms, 4), "hiding": round((ser_ms - dom_ms) / red_ms, 3) if red_ms > 0 else None,
-                      "ms_4_chunks": round(dom4_ms, 4),
-                      "hiding_4_chunks": round((ser_ms - dom4_ms) / red_ms, 3) if red_ms > 0 else None,
-                      "ms_2_chunks_2_column_blocks": round(dom2d_ms, 4),
-                      "hiding_2_chunks_2_column_blocks": round((ser_ms - dom2d_ms) / red_ms, 3) if red_ms > 0 else None},
         "a5_a7_fused_domino_shape": {"ms": round(dfu_ms, 4), "tflops": round(DOMINO_FLOPS / (dfu_ms * 1e-3) / 1e12, 1),
                                      "frac_bf16": round(DOMINO_FLOPS / (dfu_ms * 1e-3) / 1e12 / bf16_peak, 4)},
         "f2_tp_mlp_sequence_parallel": {"ms": round(sp_ms, 4), "tflops": round(MLP_FLOPS / (sp_ms * 1e-3) / 1e12, 1),
@@ -427,7 +442,8 @@ def run_ours(args, rank, world, local_rank):
         "f1_tp_mlp_backward": {"ms": round(bwd_ms, 4), "tflops": round(2 * MLP_FLOPS / (bwd_ms * 1e-3) / 1e12, 1),
                                "frac_bf16": round(2 * MLP_FLOPS / (bwd_ms * 1e-3) / 1e12 / bf16_peak, 4),
                                "dX_sum": "fused in the GEMM",
-                               "ms_separate_dX_sum_overlapped": round(bwo_ms, 4),
+                               "ms_separate_dX_sum_second_stream": round(bwo_ms, 4),
+                               "ms_separate_dX_sum_in_epilogue": round(bwoe_ms, 4),
                                "train_forward_ms": round(tf_ms, 4),
                                "train_forward_tflops": round(MLP_FLOPS / (tf_ms * 1e-3) / 1e12, 1),
                                "traffic": _traffic("tp_gemm_kernel", "mlp_backward")},
@@ -438,8 +454,10 @@ def run_ours(args, rank, world, local_rank):
     gbs = whole_job_gbs(reshard_bytes, world, reshard_ms)
     tflops = MLP_FLOPS * args.steps * world / (mlp_ms * 1e-3) / 1e12
     per_launch_gbs = reshard_bytes / (reshard_ms * 1e-3) / 1e9
-
-    rows["a5_a6_a7_tp_mlp_fused"] = {"tflops": round(tflops / world, 1), "frac_bf16": round(tflops / world / bf16_peak, 4)}
+    tp_frac = round(tflops / world / bf16_peak, 4)
+    rows["a5_a6_a7_tp_mlp_fused"] = {"tflops": round(tflops / world, 1), "frac_bf16": tp_frac}
+    # The order of the keys puts both halves of the metric (resharding GB/s,
+    # TP-MLP TFLOP/s) and the Domino figures at the end of the line.
     result = {
         "metric": METRIC,
         "value": round(gbs, 1),
@@ -454,36 +472,67 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "f32+bf16",
         "data": "synthetic (seeded Philox normals on the device)",
         "config": dict(CONFIG),
-        "roofline": {"bound": "hbm", "kernel": "boxing_kernel", "achieved": round(per_launch_gbs, 1),
-                     "peak": hbm_peak, "unit": "GB/s", "frac": round(per_launch_gbs / hbm_peak, 4),
-                     "peak_source": peak_src, "traffic": _traffic("boxing_kernel", "sweep")},
-        "tp_mlp": {"value": round(tflops, 1), "unit": "TFLOP/s", "mode": "fused reduction",
-                   "ms_per_call": round(mlp_ms / args.steps, 4),
-                   "roofline": {"bound": "tensor", "kernel": "tp_gemm_kernel", "achieved": round(tflops / world, 1),
-                                "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(tflops / world / bf16_peak, 4),
-                                "frac_of_sustained": round(tflops / world / bf16_sust, 4), "peak_source": peak_src,
-                                "traffic": _traffic("tp_gemm_kernel", "mlp")}},
-        "domino": {"ms_serial": round(ser_ms, 4), "ms_overlap_2_chunks": round(dom_ms, 4),
-                   "ms_overlap_4_chunks": round(dom4_ms, 4), "ms_overlap_2_chunks_2_column_blocks": round(dom2d_ms, 4),
-                   "ms_fused": round(dfu_ms, 4),
-                   "ms_reduce_alone": round(red_ms, 4),
-                   "hiding": round((ser_ms - dom_ms) / red_ms, 3) if red_ms > 0 else None,
-                   "tflops_overlap": round(DOMINO_FLOPS / (dom_ms * 1e-3) / 1e12, 1)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
         "rows": rows,
         "per_transition_gbs": {label: round(v[2] * v[1] / (v[0] * 1e-3) / 1e9, 1)
                                for (k, label), v in per.items() if k == "reshard"},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks.summary(),
+        "psum_error": psum_errors(rtp, torch, sweep),
+        "roofline": {"bound": "hbm", "kernel": "boxing_kernel", "achieved": round(per_launch_gbs, 1),
+                     "peak": hbm_peak, "unit": "GB/s", "frac": round(per_launch_gbs / hbm_peak, 4),
+                     "peak_source": peak_src, "traffic": _traffic("boxing_kernel", "sweep")},
     }
     if rank == 0 and not args.no_e2e:
         result["e2e"] = e2e_sweep(rtp, torch, dev, sweep)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(max_seconds=args.cpu_seconds, with_mlp=True)
+    result["tp_mlp"] = {"value": round(tflops, 1), "unit": "TFLOP/s", "mode": "fused reduction",
+                        "shape": "8192x4096x16384x4096 P=8", "ms_per_call": round(mlp_ms / args.steps, 4),
+                        "roofline": {"bound": "tensor", "kernel": "tp_gemm_kernel", "achieved": round(tflops / world, 1),
+                                     "peak": bf16_peak, "unit": "TFLOP/s", "frac": tp_frac,
+                                     "frac_of_sustained": round(tflops / world / bf16_sust, 4),
+                                     "peak_source": peak_src, "traffic": _traffic("tp_gemm_kernel", "mlp")},
+                        "backward_tflops": rows["f1_tp_mlp_backward"]["tflops"],
+                        "backward_frac": rows["f1_tp_mlp_backward"]["frac_bf16"]}
+    result["domino"] = {"shape": "4096x8192x28672x8192 P=8", "ms_serial": round(ser_ms, 4),
+                        "ms_reduce_alone": round(red_ms, 4), "ms_fused": round(dfu_ms, 4), **dom_rows,
+                        "tflops_2_chunks": round(DOMINO_FLOPS / (avg("domino") * 1e-3) / 1e12, 1)}
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def psum_errors(rtp, torch, sweep):
+    """Error of the float32 partial sums of the sweep (P-sum of 8 -> B and ->
+    S(2), meshes 1x8 and 2x4) against their exact sums, taken in float64 on
+    the device from the same partials: the normwise max|err| / max|exact| and
+    the element-wise max |err| / sum_i |x_i| (the condition-aware form; both
+    bounded by 1e-6). Every destination piece is compared."""
+    out = {}
+    for label, code, ins, src, outs, dst, _, _ in sweep:
+        if code != rtp.F32 or "P8" not in label:
+            continue
+        exact = torch.zeros(ins[0].shape, dtype=torch.float64, device=ins[0].device)
+        mag = torch.zeros_like(exact)
+        for x in ins:
+            exact += x.double()
+            mag += x.double().abs()
+        err = torch.zeros_like(exact)
+        covered = torch.zeros(exact.shape, dtype=torch.bool, device=exact.device)
+        for r in range(dst.num_ranks):
+            lo, hi, _ = rtp.shard_box(SWEEP_SHAPE, dst, r)
+            sl = tuple(slice(a, b) for a, b in zip(lo, hi))
+            e = (outs[r].double() - exact[sl]).abs()
+            err[sl] = torch.maximum(err[sl], e)
+            covered[sl] = True
+        assert bool(covered.all())
+        out[label] = {"normwise": float(err.max() / exact.abs().max()),
+                      "elementwise_over_sum_abs": float((err / mag.clamp_min(1e-300)).max())}
+        del exact, mag, err, covered
+    torch.cuda.empty_cache()
+    return out
 
 
 def tiny_cases(torch, dev):
@@ -694,15 +743,36 @@ def e2e_sweep(rtp, torch, dev, sweep):
                     h.copy_(d, non_blocking=True)
         torch.cuda.synchronize()
 
+    def copies_only():
+        """The same copies on the same streams with no reshard between them:
+        what the host link alone allows for this workload."""
+        with torch.cuda.stream(s_in):
+            for i in range(len(sel)):
+                for d, h in zip(dev_in[i], host_in[i]):
+                    d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            for i in range(len(sel)):
+                for h, d in zip(host_out[i], dev_out[i]):
+                    h.copy_(d, non_blocking=True)
+        torch.cuda.synchronize()
+
     one()
     t = time.perf_counter()
     for _ in range(2):
         one()
     dt = (time.perf_counter() - t) / 2
+    copies_only()
+    t = time.perf_counter()
+    for _ in range(2):
+        copies_only()
+    dt_link = (time.perf_counter() - t) / 2
     return {"value": round(nbytes / dt / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "h2d_d2h_gbs": round((h2d + d2h) / dt / 1e9, 1),
+            "link_ceiling_gbs": round(nbytes / dt_link / 1e9, 1),
+            "frac_of_link_ceiling": round(dt_link / dt, 4),
+            "link_h2d_d2h_gbs": round((h2d + d2h) / dt_link / 1e9, 1),
             "workload": "the six bf16 transitions on the 1x8 mesh, host pinned buffers in and out, pipelined on "
-                        "three streams"}
+                        "three streams; link_ceiling_gbs: the same copies alone on the same streams"}
 
 
 # ---- CPU oracle (baseline and reference arm) ---------------------------------------------
@@ -834,7 +904,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(wall / args.steps * 1e3, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded generator)",
-        "config": dict(CONFIG),  # the same workload; each step times a bounded sample of it (cpu_baseline.sample)
+        "config": dict(REFERENCE_CONFIG),
         "cpu_baseline": cb, "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 

@@ -326,12 +326,24 @@ int rtp_infer_broadcast(int n_in, const int32_t* in_ndims, const int64_t* const*
  *   mode      0: row-parallel GEMM writes per-rank partials, a separate
  *             kernel sums them (the all-reduce); 1: the row-parallel GEMM
  *             walks all ranks' K ranges in one accumulator (fused reduction)
- *   chunks    1, 2 or 4: Domino row split of X (and Z); in mode 0 the sum of
- *             chunk c runs on s1 while chunk c+1's GEMMs run on s0
- *   col_blocks 1 or 2: Domino column split of B_i (mode 0); the sum of
- *             column block 0 overlaps the GEMM of block 1
+ *   chunks    1, 2 or 4: Domino row split of X (and Z) (DeepSpeed Domino page,
+ *             row split of the input X); in mode 0 the sum of chunk c overlaps
+ *             chunk c+1's GEMMs
+ *   col_blocks 1 or 2: Domino column split of B_i (mode 0) (Domino page,
+ *             column split of the weight B); the sum of column block 0
+ *             overlaps the GEMM of block 1
  *   s0, s1    streams; all work is ordered after prior work on s0 and the
  *             call's completion is ordered on s0 (s1 is joined back)
+ * Mode 0 sums the partials (the all-reduce) in one of two ways
+ * (rtp_tp_mlp_overlap). By default every window (one chunk and one column
+ * block) is summed by a kernel of its own after its row-parallel GEMM, on s1
+ * beside the next window's GEMMs when s1 != s0 (the Domino schedule as the
+ * page draws it). Otherwise the row-parallel GEMM's clusters take every
+ * rank's tile of one output tile in turn, and the epilogue that writes rank
+ * i's partial tile also adds it into Z (the reduction fused into the GEMM's
+ * epilogue, beside the GEMM of the other tiles). Either way
+ * Z = ((0 + p_0) + p_1) + ... in float32 in rank order, so Z is
+ * bit-identical across chunks, column blocks and both ways.
  * Requirements (else RTP_ESHAPE, like the ValueError on out_features %
  * tp_size in ColossalAI's Linear1D_Col): F % P == 0, M % chunks == 0, K, F/P
  * and N / col_blocks multiples of 8 (16-byte rows); P <= 8 (else
@@ -376,10 +388,11 @@ int rtp_tp_mlp_train_forward(int P, int64_t M, int64_t K, int64_t F, int64_t N, 
  *   dX        float32 [M, K]; dA: P float32 [K, F/P]; dB: P float32 [F/P, N]
  *   mode      1: the input-gradient GEMM walks all ranks' F/P ranges in one
  *             accumulator (the all-reduce fused); 0: it writes per-rank
- *             partials and a separate kernel sums them; with s1 != s0 that sum
- *             runs on s1 beside the weight-gradient GEMMs on s0 (the DeepSpeed
- *             Domino page, backward: the all-reduce of the input gradient
- *             overlaps the same micro-batch's weight-gradient GEMMs)
+ *             partials and their rank sum: by default a kernel of its own,
+ *             on s1 beside the weight-gradient GEMMs on s0 when s1 != s0 (the
+ *             DeepSpeed Domino page, backward: the all-reduce of the input
+ *             gradient overlaps the same micro-batch's weight-gradient GEMMs);
+ *             or in the dX GEMM's epilogue (rtp_tp_mlp_overlap)
  *   s0, s1    streams; the call's completion is ordered on s0
  * float32 accumulation of bf16 products throughout; GELU' is evaluated in
  * float32 on the bf16 H_i. Requirements: F % P == 0, K, F/P, N multiples of 8,
@@ -390,6 +403,18 @@ int rtp_tp_mlp_backward(int P, int64_t M, int64_t K, int64_t F, int64_t N, const
                         const void* const* B_shards, const void* const* H, const void* const* Y, const void* dZ,
                         void* const* dH, void* const* dX_partials, float* dX, float* const* dA, float* const* dB,
                         int mode, rtp_stream s0, rtp_stream s1);
+
+/*
+ * Where mode 0 of rtp_tp_mlp and rtp_tp_mlp_backward sums the partials, for
+ * later calls from the calling thread (no page counterpart: it chooses how
+ * this library places the all-reduce on one GPU). sum_in_epilogue = 0 (the
+ * default): in kernels of their own, on s1 beside the next GEMMs when a
+ * second stream is given; 1: in the epilogue of the GEMM that writes them, as
+ * each output tile's rank partials finish. Results are bit-identical.
+ * *previous (if not NULL) receives the setting it replaces. RTP_EINVAL for a
+ * value other than 0 or 1.
+ */
+int rtp_tp_mlp_overlap(int sum_in_epilogue, int* previous);
 
 /*
  * The tensor-parallel MLP with sequence parallelism (ColossalAI "1D tensor

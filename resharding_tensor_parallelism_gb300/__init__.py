@@ -99,6 +99,7 @@ def _load():
         "rtp_device_error": [vp, u32p],
         "rtp_wait_selftest": [c_int, ctypes.c_ulonglong, vp, vp],
         "rtp_test_hook": [c_int, ctypes.c_int64],
+        "rtp_tp_mlp_overlap": [c_int, P(c_int)],
         "rtp_tp_mlp_sp": [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vpp, vpp, vpp, vpp,
                           vpp, vp],
         "rtp_tp_mlp_noalloc": [c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vpp, vpp,
@@ -469,6 +470,16 @@ def tp_mlp(X, A_shards, B_shards, Y=None, partials=None, Z=None, mode: int = 1, 
                               _ptrs([b.data_ptr() for b in B_shards]), _ptrs([y.data_ptr() for y in Y]), pp,
                               Z.data_ptr(), mode, chunks, col_blocks, _stream_ptr(s0), _stream_ptr(s1)))
     return Z, Y
+
+
+def tp_mlp_overlap(sum_in_epilogue: int) -> int:
+    """Where mode 0 sums the rank partials, for later calls from this thread:
+    0 (the default) in kernels of their own (on s1 beside the next GEMMs when
+    given), 1 in the epilogue of the GEMM that writes them. Returns the
+    previous setting."""
+    prev = ctypes.c_int()
+    _check(_load().rtp_tp_mlp_overlap(int(sum_in_epilogue), ctypes.byref(prev)))
+    return prev.value
 
 
 def tp_mlp_train_forward(X, A_shards, B_shards, Y=None, H=None, Z=None, stream=None):

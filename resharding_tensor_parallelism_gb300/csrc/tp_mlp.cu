@@ -50,6 +50,7 @@
 
 #include <atomic>
 #include <cstring>
+#include <unordered_map>
 #include <vector>
 
 #include "rtp_internal.h"
@@ -92,9 +93,14 @@ enum : int { RANKS_OUTER = 0, RANKS_IN_N = 1 };
 struct GemmArgs {
     CUtensorMap ta[MAX_GROUPS];  // A operand of each group ([M rows, K] K-major, or [K rows, M] M-major)
     CUtensorMap tb[MAX_GROUPS];  // B operand of each group ([K rows, N] N-major, or [N rows, K] K-major)
-    void* out[MAX_GROUPS];       // output of each group (out[0] when fused)
-    void* out2[MAX_GROUPS];      // GELU epilogue: also store the pre-activation here (if not NULL)
+    // Output of each group (to[0] when fused; of each row shard with
+    // out_rows_per_ptr > 0), as a tensor map of the launch's window: rows
+    // [0, m_end) and columns [0, n_end) of the buffer, box 32 x 32. TMA stores
+    // write only inside the map, so the window's edges clip every store.
+    CUtensorMap to[MAX_GROUPS];
+    CUtensorMap to2[MAX_GROUPS]; // GELU epilogue with store_h: the pre-activation's outputs
     const void* aux[MAX_GROUPS]; // GELU-gradient epilogue: the pre-activation H read at each output
+    int32_t store_h;             // GELU epilogue: also store the bf16 pre-activation (to2)
     int64_t ldo;                 // output row stride, elements
     int32_t groups, fused, epi;
     int32_t m_tiles, n_tiles, kb_per_group;
@@ -120,6 +126,13 @@ struct GemmArgs {
     // flight at once cover group_m rows of tiles and about 76 / group_m
     // columns of tiles.
     int32_t group_m;
+    // Rank sum in the epilogue (mode 0 of the row-parallel GEMMs): the
+    // groups' tiles of one output tile go to one cluster, rank after rank,
+    // and its epilogue, besides writing rank g's partial, adds it to sum_dst
+    // (row stride ldo): sum_dst = ((0 + p_0) + p_1) + ... in float32, the same
+    // bits as summing the finished partials in rank order.
+    int32_t sum_into;
+    float* sum_dst;
 };
 
 __device__ unsigned int g_tp_error;
@@ -269,10 +282,14 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32])
 // are bijections of [0, groups * m_tiles * n_tiles).
 __device__ __forceinline__ void tile_coords(const GemmArgs& a, int tile, int& g, int& mt, int& nt)
 {
-    const bool in_n = !a.fused && a.rank_fold == RANKS_IN_N;
-    const int per_group = a.fused || in_n ? 0 : a.m_tiles * a.n_tiles;
+    const bool in_n = !a.fused && !a.sum_into && a.rank_fold == RANKS_IN_N;
+    const int per_group = a.fused || in_n || a.sum_into ? 0 : a.m_tiles * a.n_tiles;
     g = per_group ? tile / per_group : 0;
-    const int r = tile - g * per_group;
+    int r = tile - g * per_group;
+    if (a.sum_into) {  // rank innermost: tile = output tile * groups + rank
+        g = tile % a.groups;
+        r = tile / a.groups;
+    }
     const int ntiles = in_n ? a.groups * a.n_tiles : a.n_tiles;
     const int span = a.group_m * ntiles;
     const int first_m = (r / span) * a.group_m;
@@ -284,6 +301,20 @@ __device__ __forceinline__ void tile_coords(const GemmArgs& a, int tile, int& g,
         g = nt / a.n_tiles;
         nt -= g * a.n_tiles;
     }
+}
+
+// The k-th tile of cluster `pair` of `npairs`, or -1 when it has no more.
+// Clusters take tiles in turn; with the rank sum in the epilogue they take
+// whole groups (every rank's tile of one output tile, rank after rank), so one
+// cluster adds up each output tile's partials in rank order.
+__device__ __forceinline__ int nth_tile(const GemmArgs& a, int pair, int npairs, int k)
+{
+    if (!a.sum_into) {
+        const int t = pair + k * npairs;
+        return t < a.total_tiles ? t : -1;
+    }
+    const int grp = pair + (k / a.groups) * npairs;
+    return grp < a.total_tiles / a.groups ? grp * a.groups + k % a.groups : -1;
 }
 
 __device__ __forceinline__ float gelu(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752440f)); }
@@ -320,7 +351,14 @@ constexpr int STAGES2 = 6;
 constexpr uint32_t A2_BYTES = 128 * BK * 2;           // 16 KB
 constexpr uint32_t B2_BYTES = 128 * BK * 2;           // 16 KB: 2 boxes of 64(N) x 64(K)
 constexpr uint32_t STAGE2_BYTES = A2_BYTES + B2_BYTES;  // 32 KB
-constexpr size_t SMEM2_BYTES = STAGES2 * STAGE2_BYTES + 1024 + 1024;
+// Epilogue staging: per epilogue warp two 4 KB buffers, each one 32 x 32 output
+// chunk (float32, or bf16 Y and H side by side), swizzled as its TMA store
+// reads it.
+constexpr uint32_t EPI_STAGE_BYTES = 4096;
+constexpr uint32_t EPI_WARP_BYTES = 2 * EPI_STAGE_BYTES;
+constexpr size_t SMEM2_BYTES =
+    STAGES2 * STAGE2_BYTES + 1024 + EPI_WARPS * EPI_WARP_BYTES + 1024;  // ring, barriers, staging, alignment
+static_assert(SMEM2_BYTES <= 232448, "at most 227 KB of shared memory per CTA");
 // Instruction descriptor of tcgen05.mma kind::f16: D float32 (bits 4-5 = 1),
 // A and B bf16 (bits 7-9 = 1, 10-12 = 1), bit 15 = A M-major, bit 16 = B
 // N-major, N >> 3 in bits 17-22, M >> 4 in bits 24-28 (M = 256 for the pair).
@@ -370,6 +408,26 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
         : "memory");
 }
+// TMA tile store shared -> global (bulk async group of the issuing thread).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Until at most one of this thread's bulk groups still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// Until every bulk group of this thread has completed (its writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Makes this thread's shared-memory writes visible to the TMA (async proxy).
+__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+
 __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                               uint32_t accumulate)
 {
@@ -434,6 +492,13 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
             prefetch_map(&a.tb[g]);
         }
     }
+    if (warp == 2 && lane == 0) {
+        const int nout = SP_OUT ? a.out_ptrs : (a.fused ? 1 : a.groups);
+        for (int g = 0; g < nout; ++g) {
+            prefetch_map(&a.to[g]);
+            if (EPI == EPI_GELU_BF16 && a.store_h) prefetch_map(&a.to2[g]);
+        }
+    }
     if (warp == 1) {
         // one warp in each CTA of the pair allocates collectively
         asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -446,6 +511,12 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
     cluster_sync();  // the peer's barriers are initialised before any remote use
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Launched as a programmatic dependent of the previous kernel in the
+    // stream, this CTA may have started (and run the set-up above) while that
+    // kernel was finishing: wait for it to complete, and its writes to be
+    // visible, before any global memory access. Without such a launch this
+    // returns at once.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int kbs = a.fused ? a.groups * a.kb_per_group : a.kb_per_group;
 
     if (warp == 0) {
@@ -457,7 +528,7 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
             bool ok = true;
             const uint32_t smem0 = smem_u32(smem);
             const uint32_t leader_full0 = map_to_rank(full_bar(0), 0);  // barriers are 8 bytes apart
-            for (int tile = pair; ok && tile < a.total_tiles; tile += npairs) {
+            for (int k = 0, tile; ok && (tile = nth_tile(a, pair, npairs, k)) >= 0; ++k) {
                 int g, mt, nt;
                 tile_coords(a, tile, g, mt, nt);
                 const int row = a.m0 + mt * BM2 + (int)cta * 128, col = a.n0 + nt * BN + (int)cta * 128;
@@ -535,7 +606,7 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
             const uint64_t desc_b0 = smem_desc(smem_u32(smem) + A2_BYTES, B_K ? 16u : B_SUB, 1024u);
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int tile = pair; ok && tile < a.total_tiles; tile += npairs) {
+            for (int k = 0, tile; ok && (tile = nth_tile(a, pair, npairs, k)) >= 0; ++k) {
                 if (!wait_bar(acc_empty(acc), acc_phase ^ 1u, abort_flag, ERR_MMA_ACC)) {
                     ok = false;
                     break;
@@ -577,11 +648,12 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
         __syncwarp();
     } else {
         // ---------------- epilogue (both CTAs) ----------------
+        const uint32_t stage_epi = smem_u32(smem) + STAGES2 * STAGE2_BYTES + 1024u + (uint32_t)(warp - 2) * EPI_WARP_BYTES;
         const int quarter = warp & 3;
         const int c_begin = ((warp - 2) >> 2) * EPI_CHUNKS;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = pair; tile < a.total_tiles; tile += npairs) {
+        for (int k = 0, tile; (tile = nth_tile(a, pair, npairs, k)) >= 0; ++k) {
             int g, mt, nt;
             tile_coords(a, tile, g, mt, nt);
             int ok = 1;
@@ -589,19 +661,20 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            const int64_t row = a.m0 + (int64_t)mt * BM2 + cta * 128 + quarter * 32 + lane;
+            // this warp's 32 rows: lane l holds row row0 + l of the accumulator
+            const int64_t row0 = a.m0 + (int64_t)mt * BM2 + cta * 128 + quarter * 32;
+            const int64_t row = row0 + lane;
             const int64_t col = a.n0 + (int64_t)nt * BN;
             const bool row_ok = row < a.m_end;
-            void* out_base = a.out[g];
-            int64_t orow = row;
-            if (SP_OUT && row_ok) {
-                const int sh = min((int)(row / a.out_rows_per_ptr), a.out_ptrs - 1);
-                out_base = a.out[sh];
-                orow = row - (int64_t)sh * a.out_rows_per_ptr;
+            int om = g;  // output map
+            int64_t orow0 = row0;
+            if constexpr (SP_OUT) {  // the warp's rows lie in one shard (shards are multiples of 128 rows)
+                om = min((int)(row0 / a.out_rows_per_ptr), a.out_ptrs - 1);
+                orow0 = row0 - (int64_t)om * a.out_rows_per_ptr;
             }
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
             const __nv_bfloat16* hrow = nullptr;
-            if constexpr (EPI == EPI_DGELU_BF16) hrow = static_cast<const __nv_bfloat16*>(a.aux[g]) + orow * a.ldo;
+            if constexpr (EPI == EPI_DGELU_BF16) hrow = static_cast<const __nv_bfloat16*>(a.aux[g]) + row * a.ldo;
             // H of chunk c (GELU-gradient epilogue only)
             auto load_h = [&](int c, uint4 (&h)[4]) {
                 if constexpr (EPI == EPI_DGELU_BF16) {
@@ -613,57 +686,82 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
                     }
                 }
             };
-            // writes chunk c (32 columns of this thread's row) from its accumulator values
+            // Chunk c (32 columns of the warp's 32 rows): each lane writes its row
+            // to a staging buffer in the TMA's swizzled layout (16-byte unit u of
+            // row r at unit u ^ (r / 2 % 4) of a 64-byte bf16 row, u ^ (r % 8) of a
+            // 128-byte float32 row: the 8 lanes of each store phase hit distinct
+            // banks), then one lane stores the 32 x 32 tile. The map's window
+            // clips rows past m_end and columns past n_end.
             auto emit = [&](int c, const uint32_t (&r)[32], const uint4 (&h)[4]) {
                 const int64_t c0 = col + 32 * c;
-                if (!row_ok || c0 >= a.n_end) return;
-                if constexpr (EPI == EPI_DGELU_BF16) {
-                    // dH = dY * GELU'(H): the accumulator is dY, H was read at the same place
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_base) + orow * a.ldo + c0);
+                if (c0 >= a.n_end || row0 >= a.m_end) return;  // warp-uniform: nothing of the window here
+                const uint32_t buf = stage_epi + (uint32_t)(c & 1) * EPI_STAGE_BYTES;
+                if (lane == 0) bulk_wait_read_1();  // the store two chunks back has read this buffer
+                __syncwarp();
+                if constexpr (EPI == EPI_F32) {
+                    const uint32_t rb = buf + (uint32_t)lane * 128u;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        st_shared_v4(rb + 16u * (uint32_t)(q ^ (lane & 7)), r[4 * q + 0], r[4 * q + 1], r[4 * q + 2],
+                                     r[4 * q + 3]);
+                } else {
+                    const uint32_t rb = buf + (uint32_t)lane * 64u;
+                    const int sw = (lane >> 1) & 3;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        if (c0 + 8 * q >= a.n_end) break;
-                        uint4 v;
-                        v.x = pack_bf16(__uint_as_float(r[8 * q + 0]) * gelu_grad(bf16_lo(h[q].x)),
-                                        __uint_as_float(r[8 * q + 1]) * gelu_grad(bf16_hi(h[q].x)));
-                        v.y = pack_bf16(__uint_as_float(r[8 * q + 2]) * gelu_grad(bf16_lo(h[q].y)),
-                                        __uint_as_float(r[8 * q + 3]) * gelu_grad(bf16_hi(h[q].y)));
-                        v.z = pack_bf16(__uint_as_float(r[8 * q + 4]) * gelu_grad(bf16_lo(h[q].z)),
-                                        __uint_as_float(r[8 * q + 5]) * gelu_grad(bf16_hi(h[q].z)));
-                        v.w = pack_bf16(__uint_as_float(r[8 * q + 6]) * gelu_grad(bf16_lo(h[q].w)),
-                                        __uint_as_float(r[8 * q + 7]) * gelu_grad(bf16_hi(h[q].w)));
-                        __stcs(dst + q, v);
-                    }
-                } else if constexpr (EPI == EPI_GELU_BF16) {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out_base) + orow * a.ldo + c0);
-                    uint4* hdst = a.out2[g] ? reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out2[g]) +
-                                                                       orow * a.ldo + c0)
-                                            : nullptr;
+                        uint32_t w[4];
+                        if constexpr (EPI == EPI_DGELU_BF16) {
+                            // dH = dY * GELU'(H): the accumulator is dY, H was read at the same place
+                            w[0] = pack_bf16(__uint_as_float(r[8 * q + 0]) * gelu_grad(bf16_lo(h[q].x)),
+                                             __uint_as_float(r[8 * q + 1]) * gelu_grad(bf16_hi(h[q].x)));
+                            w[1] = pack_bf16(__uint_as_float(r[8 * q + 2]) * gelu_grad(bf16_lo(h[q].y)),
+                                             __uint_as_float(r[8 * q + 3]) * gelu_grad(bf16_hi(h[q].y)));
+                            w[2] = pack_bf16(__uint_as_float(r[8 * q + 4]) * gelu_grad(bf16_lo(h[q].z)),
+                                             __uint_as_float(r[8 * q + 5]) * gelu_grad(bf16_hi(h[q].z)));
+                            w[3] = pack_bf16(__uint_as_float(r[8 * q + 6]) * gelu_grad(bf16_lo(h[q].w)),
+                                             __uint_as_float(r[8 * q + 7]) * gelu_grad(bf16_hi(h[q].w)));
+                        } else {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (c0 + 8 * q >= a.n_end) break;
-                        uint4 v;
-                        v.x = pack_bf16(gelu(__uint_as_float(r[8 * q + 0])), gelu(__uint_as_float(r[8 * q + 1])));
-                        v.y = pack_bf16(gelu(__uint_as_float(r[8 * q + 2])), gelu(__uint_as_float(r[8 * q + 3])));
-                        v.z = pack_bf16(gelu(__uint_as_float(r[8 * q + 4])), gelu(__uint_as_float(r[8 * q + 5])));
-                        v.w = pack_bf16(gelu(__uint_as_float(r[8 * q + 6])), gelu(__uint_as_float(r[8 * q + 7])));
-                        __stcs(dst + q, v);
-                        if (hdst) {  // the pre-activation, for the backward pass
-                            uint4 hv;
-                            hv.x = pack_bf16(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]));
-                            hv.y = pack_bf16(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]));
-                            hv.z = pack_bf16(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]));
-                            hv.w = pack_bf16(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]));
-                            __stcs(hdst + q, hv);
+                            for (int e = 0; e < 4; ++e)
+                                w[e] = pack_bf16(gelu(__uint_as_float(r[8 * q + 2 * e])),
+                                                 gelu(__uint_as_float(r[8 * q + 2 * e + 1])));
+                        }
+                        st_shared_v4(rb + 16u * (uint32_t)(q ^ sw), w[0], w[1], w[2], w[3]);
+                        if (EPI == EPI_GELU_BF16 && a.store_h) {  // the pre-activation, for the backward pass
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                w[e] = pack_bf16(__uint_as_float(r[8 * q + 2 * e]), __uint_as_float(r[8 * q + 2 * e + 1]));
+                            st_shared_v4(rb + 2048u + 16u * (uint32_t)(q ^ sw), w[0], w[1], w[2], w[3]);
                         }
                     }
-                } else {
-                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out_base) + orow * a.ldo + c0);
+                }
+                fence_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&a.to[om], buf, (int)c0, (int)orow0);
+                    if (EPI == EPI_GELU_BF16 && a.store_h) tma_store_2d(&a.to2[om], buf + 2048u, (int)c0, (int)orow0);
+                    bulk_commit();
+                }
+                if constexpr (EPI == EPI_F32) {
+                    if (a.sum_into) {
+                        // sum_dst[rows, c0 + lane] += the staged chunk's column `lane`, rank g after
+                        // rank g - 1 (the same lane of the same warp added those: program order);
+                        // rank 0 starts from +0. Each access of the warp is one 128-byte row.
+                        const bool col_in = c0 + lane < a.n_end;
+                        float* zc = a.sum_dst + row0 * a.ldo + c0 + lane;
+                        const uint32_t sbase = buf + 4u * (uint32_t)(lane & 3);
+                        float prev[32];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        if (c0 + 4 * q >= a.n_end) break;
-                        __stcs(dst + q, make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
-                                                    __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
+                        for (int rr = 0; rr < 32; ++rr)
+                            prev[rr] = (g > 0 && col_in && row0 + rr < a.m_end) ? __ldcg(zc + rr * a.ldo) : 0.0f;
+#pragma unroll
+                        for (int rr = 0; rr < 32; ++rr) {
+                            float v;
+                            asm volatile("ld.shared.f32 %0, [%1];"
+                                         : "=f"(v)
+                                         : "r"(sbase + (uint32_t)rr * 128u + 16u * (uint32_t)((lane >> 2) ^ (rr & 7))));
+                            if (col_in && row0 + rr < a.m_end) __stcg(zc + rr * a.ldo, prev[rr] + v);
+                        }
                     }
                 }
             };
@@ -696,9 +794,16 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
                 acc_phase ^= 1u;
             }
         }
+        if (lane == 0) bulk_wait_all();  // every output tile written before the CTA leaves
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
+    // This CTA's work is done: the next kernel of the stream may be scheduled
+    // once every CTA of this grid has come here (or exited). Every CTA of this
+    // grid is then resident or done, so the next kernel's CTAs only take SMs
+    // this grid no longer needs.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     cluster_sync();  // no CTA leaves while its peer may still signal or read it
     tc_fence_after();
     if (warp == 1)
@@ -729,6 +834,56 @@ int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int bo
     return RTP_OK;
 }
 
+// Everything an output map is encoded from.
+struct OutKey {
+    uintptr_t ptr;
+    int64_t rows, cols, ld;
+    bool f32;
+    bool operator==(const OutKey& o) const
+    {
+        return ptr == o.ptr && rows == o.rows && cols == o.cols && ld == o.ld && f32 == o.f32;
+    }
+};
+struct OutKeyHash {
+    size_t operator()(const OutKey& k) const
+    {
+        uint64_t h = k.ptr * 0x9E3779B97F4A7C15ull;
+        for (uint64_t v : {(uint64_t)k.rows, (uint64_t)k.cols, (uint64_t)k.ld, (uint64_t)k.f32}) h = (h ^ v) * 0x100000001B3ull;
+        return (size_t)h;
+    }
+};
+
+// Tensor map of an output window: rows [0, rows) and columns [0, cols) of a
+// row-major buffer with a row stride of ld elements, box 32 x 32 (one
+// epilogue warp's chunk), swizzled like the staging buffer: 64-byte swizzle
+// for bf16 (64-byte box rows), 128-byte for float32. Repeated calls with the
+// same buffers reuse their maps (cached per thread).
+int make_out_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, bool f32)
+{
+    static thread_local std::unordered_map<OutKey, CUtensorMap, OutKeyHash> cache;
+    const OutKey key{reinterpret_cast<uintptr_t>(ptr), rows, cols, ld, f32};
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+        *m = it->second;
+        return RTP_OK;
+    }
+    auto fn = encode_fn();
+    if (!fn) return fail(RTP_ECUDA, "tp_mlp: cuTensorMapEncodeTiled is unavailable");
+    const int es = f32 ? 4 : 2;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * es)};
+    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr),
+                    dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(RTP_ECUDA, "tp_mlp: cuTensorMapEncodeTiled (output) failed (%d)", (int)r);
+    if (cache.size() >= 4096) cache.clear();
+    cache.emplace(key, *m);
+    return RTP_OK;
+}
+
 template <int CFG>
 int launch_gemm_t(GemmArgs& args, cudaStream_t stream)
 {
@@ -738,11 +893,16 @@ int launch_gemm_t(GemmArgs& args, cudaStream_t stream)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(RTP_ECUDA, "tp_mlp: no CUDA device");
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // Programmatic dependent launch: the kernel may be set up while the
+    // previous kernel of the stream finishes; it waits for that kernel's
+    // completion (griddepcontrol.wait) before touching global memory.
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = SMEM2_BYTES;
     cfg.stream = stream;
@@ -767,9 +927,13 @@ int launch_gemm_t(GemmArgs& args, cudaStream_t stream)
     // tiles instead of 16 x 4.75) read the fewest.
     const int64_t k_extent = (int64_t)(args.fused ? args.groups : 1) * args.kb_per_group * BK;
     args.group_m = k_extent >= 8192 ? GROUP_M_LONG_K : GROUP_M;
-    const int clusters = args.total_tiles < nclusters ? args.total_tiles : nclusters;
+    // clusters take tiles (or, with the rank sum in the epilogue, whole groups
+    // of every rank's tile of one output tile) in turn
+    const int units = args.sum_into ? args.total_tiles / args.groups : args.total_tiles;
+    const int clusters = units < nclusters ? units : nclusters;
     if (clusters <= 0) return RTP_OK;
     cfg.gridDim = dim3(2 * clusters);
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, tp_gemm_kernel<CFG>, args);
     if (e != cudaSuccess) return fail(RTP_ECUDA, "tp_mlp: GEMM launch failed: %s", cudaGetErrorString(e));
     return RTP_OK;
@@ -816,6 +980,15 @@ int events(Events** out)
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Where the row-parallel GEMMs of mode 0 sum their partials, per host thread
+// (rtp_tp_mlp_overlap): 0 (the default) in kernels of their own, 1 in the
+// GEMM's epilogue. The epilogue sum needs every rank's tile of an output tile
+// on one cluster, rank after rank; with that order the ranks' operand panels
+// stop sharing L2 and the partials' stream evicts the running sums, so on the
+// Llama-70B MLP shape the GEMM took as long as the summing kernel it replaces
+// (1205 against 1051 us, DRAM reads 2.6 against 1.0 GB).
+thread_local int g_sum_in_epilogue = 0;
 
 }  // namespace
 
@@ -867,6 +1040,9 @@ int tp_mlp_impl(const char* fn, int P, int64_t M, int64_t K, int64_t F, int64_t 
     }
     const int64_t Mc = M / chunks;
     const int64_t Nb = N / col_blocks;
+    // mode 0: the partials' rank sum in the row-parallel GEMM's epilogue, or
+    // in kernels of their own (on s1 beside the next GEMMs when given)
+    const bool sum_in_gemm = mode == 0 && g_sum_in_epilogue;
 
     // GEMM1 arguments (tensor maps shared by every chunk)
     static thread_local GemmArgs g1, g2;
@@ -876,12 +1052,10 @@ int tp_mlp_impl(const char* fn, int P, int64_t M, int64_t K, int64_t F, int64_t 
     for (int i = 0; i < P; ++i) {
         if ((st = make_map(&g1.ta[i], X, M, K, 128))) return st;
         if ((st = make_map(&g1.tb[i], A_shards[i], K, Fp, BK))) return st;
-        g1.out[i] = Y[i];
-        g1.out2[i] = H ? H[i] : nullptr;
         if ((st = make_map(&g2.ta[i], Y[i], M, Fp, 128))) return st;
         if ((st = make_map(&g2.tb[i], B_shards[i], Fp, N, BK))) return st;
-        g2.out[i] = mode == 0 ? partials[i] : (void*)Z;
     }
+    g1.store_h = H != nullptr;
     g1.ldo = Fp;
     g1.groups = P;
     g1.fused = 0;
@@ -901,18 +1075,30 @@ int tp_mlp_impl(const char* fn, int P, int64_t M, int64_t K, int64_t F, int64_t 
     g2.n_tiles = (int)((Nb + BN - 1) / BN);
     g2.kb_per_group = (int)((Fp + BK - 1) / BK);
 
+    // The launches in order: per chunk c, GEMM1 (all ranks), then per column
+    // block b the row-parallel GEMM of window (c, b) (rows of chunk c, columns
+    // of block b of Z). In mode 0 a window's partials are complete once its
+    // GEMM2 has run, and Z's window is their sum: computed in that GEMM's
+    // epilogue as the ranks' tiles finish (sum_in_gemm), or by a kernel of its
+    // own that runs on s1 beside the next window's GEMMs.
+    struct Launch {
+        bool gemm2;
+        int c, b;
+    };
+    std::vector<Launch> ls;  // host allocations all happen before the first launch
     for (int c = 0; c < chunks; ++c) {
-        g1.m0 = (int)(c * Mc);
-        g1.m_end = (int)((c + 1) * Mc);
-        if ((st = launch_gemm(g1, s0))) return st;
-        for (int b = 0; b < (mode == 0 ? col_blocks : 1); ++b) {
-            g2.m0 = (int)(c * Mc);
-            g2.m_end = (int)((c + 1) * Mc);
-            g2.n0 = (int)(b * Nb);
-            g2.n_end = (int)((b + 1) * Nb);
-            if ((st = launch_gemm(g2, s0))) return st;
-            if (mode == 1) continue;
-            // sum of the P partials over this window: Z[rows, cols] = sum_i partial_i[rows, cols]
+        ls.push_back(Launch{false, c, 0});
+        for (int b = 0; b < (mode == 0 ? col_blocks : 1); ++b) ls.push_back(Launch{true, c, b});
+    }
+    const int nwin = mode == 0 ? chunks * col_blocks : 0;
+    // Window sums as kernels of their own: one boxing task each,
+    // Z[rows, cols] = sum_i partial_i[rows, cols].
+    std::vector<std::vector<PlanTask>> red_tasks(sum_in_gemm ? 0 : (size_t)nwin);
+    if (!red_tasks.empty()) {
+        inject_alloc_fault();
+        const std::vector<int64_t> vol_src((size_t)P, M * N), vol_dst(1, M * N);
+        for (int w = 0; w < nwin; ++w) {
+            const int c = w / col_blocks, b = w % col_blocks;
             PlanTask t;
             t.cols = Nb;
             t.rows = Mc;
@@ -928,43 +1114,66 @@ int tp_mlp_impl(const char* fn, int P, int64_t M, int64_t K, int64_t F, int64_t 
             const int64_t off = c * Mc * N + b * Nb;
             for (int i = 0; i < P; ++i) t.src.push_back(Ref{i, off});
             t.dst.push_back(Ref{0, off});
-            std::vector<PlanTask> tasks{t};
-            void* zdst[1] = {Z};
-            cudaStream_t rs = s0;
-            if (two_streams) {
-                if (cudaEventRecord(ev->fwd, s0) != cudaSuccess || cudaStreamWaitEvent(s1, ev->fwd, 0) != cudaSuccess)
-                    return fail(RTP_ECUDA, "tp_mlp: event ordering failed");
-                rs = s1;
-            }
-            // Beside the next chunk's GEMM (one CTA per SM), the reduction runs
-            // kOverlapBlocksPerSm blocks per SM so that both fit on every SM at
-            // once; the last window's reduction has nothing to overlap and takes
-            // the whole GPU.
-            const bool last = c == chunks - 1 && b == col_blocks - 1;
-            const int bps = two_streams && !last ? kOverlapBlocksPerSm : 4;
-            if ((st = launch_tasks(RTP_F32, tasks, (const void* const*)partials, zdst, rs, nullptr, bps))) return st;
+            red_tasks[(size_t)w].push_back(std::move(t));
+            if ((st = check_task_bounds(fn, red_tasks[(size_t)w], vol_src, vol_dst))) return st;
         }
     }
-    if (mode == 0 && two_streams) {
+    // Output maps of every launch, encoded before the first launch: each
+    // covers the launch's window, so its TMA stores stay inside it.
+    std::vector<CUtensorMap> omaps(ls.size() * 2 * MAX_GROUPS);
+    for (size_t j = 0; j < ls.size(); ++j) {
+        const Launch& L = ls[j];
+        CUtensorMap* o = &omaps[j * 2 * MAX_GROUPS];
+        const int64_t m_end = (L.c + 1) * Mc, n_end = (L.b + 1) * Nb;
+        for (int i = 0; i < P; ++i) {
+            if (!L.gemm2) {
+                if ((st = make_out_map(&o[i], Y[i], m_end, Fp, Fp, false))) return st;
+                if (H && (st = make_out_map(&o[MAX_GROUPS + i], H[i], m_end, Fp, Fp, false))) return st;
+            } else if (mode == 0) {
+                if ((st = make_out_map(&o[i], partials[i], m_end, n_end, N, true))) return st;
+            } else if (i == 0) {
+                if ((st = make_out_map(&o[0], Z, m_end, N, N, true))) return st;
+            }
+        }
+    }
+    g2.sum_into = sum_in_gemm;
+    g2.sum_dst = sum_in_gemm ? Z : nullptr;
+
+    void* zdst[1] = {Z};
+    for (size_t j = 0; j < ls.size(); ++j) {
+        const Launch& L = ls[j];
+        GemmArgs& g = L.gemm2 ? g2 : g1;
+        g.m0 = (int)(L.c * Mc);
+        g.m_end = (int)((L.c + 1) * Mc);
+        if (L.gemm2) {
+            g.n0 = (int)(L.b * Nb);
+            g.n_end = (int)((L.b + 1) * Nb);
+        }
+        std::memcpy(g.to, &omaps[j * 2 * MAX_GROUPS], sizeof g.to);
+        std::memcpy(g.to2, &omaps[j * 2 * MAX_GROUPS + MAX_GROUPS], sizeof g.to2);
+        if ((st = launch_gemm(g, s0))) return st;
+        if (!L.gemm2 || mode == 1 || sum_in_gemm) continue;
+        const int w = L.c * col_blocks + L.b;
+        cudaStream_t rs = s0;
+        if (two_streams) {
+            if (cudaEventRecord(ev->fwd, s0) != cudaSuccess || cudaStreamWaitEvent(s1, ev->fwd, 0) != cudaSuccess)
+                return fail(RTP_ECUDA, "tp_mlp: event ordering failed");
+            rs = s1;
+        }
+        // Beside the next chunk's GEMM (one CTA per SM), a sum on s1 runs
+        // kOverlapBlocksPerSm blocks per SM so that both fit on every SM at
+        // once; the last window's sum has nothing to overlap and takes the
+        // whole GPU.
+        const bool last = w == nwin - 1;
+        const int bps = rs != s0 && !last ? kOverlapBlocksPerSm : 4;
+        if ((st = launch_tasks(RTP_F32, red_tasks[(size_t)w], (const void* const*)partials, zdst, rs, nullptr, bps)))
+            return st;
+    }
+    if (mode == 0 && two_streams && !sum_in_gemm) {
         if (cudaEventRecord(ev->back, s1) != cudaSuccess || cudaStreamWaitEvent(s0, ev->back, 0) != cudaSuccess)
             return fail(RTP_ECUDA, "tp_mlp: event ordering failed");
     }
     return RTP_OK;
-}
-
-// Sum over the ranks of a float32 [M, cols] buffer: dst = sum_i parts[i], as
-// one task of the boxing kernel on `stream`.
-int reduce_partials(int P, int64_t M, int64_t cols, void* const* parts, float* dst, cudaStream_t stream, int blocks_per_sm)
-{
-    PlanTask t;
-    t.cols = M * cols;
-    t.rows = 1;
-    t.n_outer = 0;
-    for (int i = 0; i < P; ++i) t.src.push_back(Ref{i, 0});
-    t.dst.push_back(Ref{0, 0});
-    std::vector<PlanTask> tasks{t};
-    void* d[1] = {dst};
-    return launch_tasks(RTP_F32, tasks, (const void* const*)parts, d, stream, nullptr, blocks_per_sm);
 }
 
 }  // namespace
@@ -975,8 +1184,10 @@ int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
                const void* const* B_shards, void* const* Y, void* const* partials, float* Z, int mode, int chunks,
                int col_blocks, rtp_stream s0, rtp_stream s1)
 {
-    return tp_mlp_impl("rtp_tp_mlp", P, M, K, F, N, X, A_shards, B_shards, Y, nullptr, partials, Z, mode, chunks,
-                       col_blocks, s0, s1);
+    return guarded("rtp_tp_mlp", [&] {
+        return tp_mlp_impl("rtp_tp_mlp", P, M, K, F, N, X, A_shards, B_shards, Y, nullptr, partials, Z, mode, chunks,
+                           col_blocks, s0, s1);
+    });
 }
 
 int rtp_tp_mlp_train_forward(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
@@ -984,14 +1195,26 @@ int rtp_tp_mlp_train_forward(int P, int64_t M, int64_t K, int64_t F, int64_t N, 
                              float* Z, rtp_stream stream)
 {
     if (!H) return fail(RTP_EINVAL, "rtp_tp_mlp_train_forward: NULL H");
-    return tp_mlp_impl("rtp_tp_mlp_train_forward", P, M, K, F, N, X, A_shards, B_shards, Y, H, nullptr, Z, 1, 1, 1,
-                       stream, stream);
+    return guarded("rtp_tp_mlp_train_forward", [&] {
+        return tp_mlp_impl("rtp_tp_mlp_train_forward", P, M, K, F, N, X, A_shards, B_shards, Y, H, nullptr, Z, 1, 1, 1,
+                           stream, stream);
+    });
 }
 
-int rtp_tp_mlp_backward(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X, const void* const* A_shards,
-                        const void* const* B_shards, const void* const* H, const void* const* Y, const void* dZ,
-                        void* const* dH, void* const* dX_partials, float* dX, float* const* dA, float* const* dB,
-                        int mode, rtp_stream s0_, rtp_stream s1_)
+int rtp_tp_mlp_overlap(int sum_in_epilogue, int* previous)
+{
+    if (sum_in_epilogue != 0 && sum_in_epilogue != 1)
+        return fail(RTP_EINVAL, "rtp_tp_mlp_overlap: %d is not 0 or 1", sum_in_epilogue);
+    if (previous) *previous = g_sum_in_epilogue;
+    g_sum_in_epilogue = sum_in_epilogue;
+    return RTP_OK;
+}
+
+static int tp_mlp_backward_body(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X,
+                                const void* const* A_shards, const void* const* B_shards, const void* const* H,
+                                const void* const* Y, const void* dZ, void* const* dH, void* const* dX_partials,
+                                float* dX, float* const* dA, float* const* dB, int mode, rtp_stream s0_,
+                                rtp_stream s1_)
 {
     const char* fn = "rtp_tp_mlp_backward";
     if (P < 1 || P > MAX_GROUPS) return fail(RTP_EUNSUPPORTED, "%s: P = %d outside [1, %d]", fn, P, MAX_GROUPS);
@@ -1042,20 +1265,21 @@ int rtp_tp_mlp_backward(int P, int64_t M, int64_t K, int64_t F, int64_t N, const
         // dH_i = (dZ B_i^T) * GELU'(H_i): dZ K-major [M, N], B_i^T read K-major from B_i [F/P, N]
         if ((st = make_map(&gh.ta[i], dZ, M, N, 128))) return st;
         if ((st = make_map(&gh.tb[i], B_shards[i], Fp, N, 128))) return st;
-        gh.out[i] = dH[i];
+        if ((st = make_out_map(&gh.to[i], dH[i], M, Fp, Fp, false))) return st;
         gh.aux[i] = H[i];
         // dX (+)= dH_i A_i^T: dH_i K-major [M, F/P], A_i^T read K-major from A_i [K, F/P]
         if ((st = make_map(&gx.ta[i], dH[i], M, Fp, 128))) return st;
         if ((st = make_map(&gx.tb[i], A_shards[i], K, Fp, 128))) return st;
-        gx.out[i] = mode == 0 ? dX_partials[i] : (void*)dX;
+        if (mode == 0 && (st = make_out_map(&gx.to[i], dX_partials[i], M, K, K, true))) return st;
+        if (mode == 1 && i == 0 && (st = make_out_map(&gx.to[0], dX, M, K, K, true))) return st;
         // dA_i = X^T dH_i: X^T read M-major from X [M, K], dH_i N-major
         if ((st = make_map(&ga.ta[i], X, M, K, 64))) return st;
         if ((st = make_map(&ga.tb[i], dH[i], M, Fp, BK))) return st;
-        ga.out[i] = dA[i];
+        if ((st = make_out_map(&ga.to[i], dA[i], K, Fp, Fp, true))) return st;
         // dB_i = Y_i^T dZ: Y_i^T read M-major from Y_i [M, F/P], dZ N-major
         if ((st = make_map(&gb.ta[i], Y[i], M, Fp, 64))) return st;
         if ((st = make_map(&gb.tb[i], dZ, M, N, BK))) return st;
-        gb.out[i] = dB[i];
+        if ((st = make_out_map(&gb.to[i], dB[i], Fp, N, N, true))) return st;
     }
     auto shape = [&](GemmArgs& g, int64_t rows, int64_t cols, int64_t kdim, int epi, int cfg, int fused) {
         g.groups = P;
@@ -1079,23 +1303,56 @@ int rtp_tp_mlp_backward(int P, int64_t M, int64_t K, int64_t F, int64_t N, const
     // are already near square (8 x 9.5 tiles on the 8192x4096x16384x4096 MLP).
     gh.rank_fold = RANKS_IN_N;
     ga.rank_fold = RANKS_IN_N;
+    // Mode 0: the dX partials' rank sum. By default the dX GEMM adds each
+    // output tile's partials up in its epilogue as the ranks' tiles finish;
+    // otherwise it is a kernel of its own, on s1 beside the weight-gradient
+    // GEMMs when a second stream is given (the Domino backward).
+    const bool sum_in_gemm = mode == 0 && g_sum_in_epilogue;
+    std::vector<PlanTask> dx_tasks;  // host allocations before the first launch
+    if (mode == 0 && !sum_in_gemm) {
+        inject_alloc_fault();
+        PlanTask t;
+        t.cols = M * K;
+        t.rows = 1;
+        t.n_outer = 0;
+        for (int i = 0; i < P; ++i) t.src.push_back(Ref{i, 0});
+        t.dst.push_back(Ref{0, 0});
+        dx_tasks.push_back(std::move(t));
+        if ((st = check_task_bounds(fn, dx_tasks, std::vector<int64_t>((size_t)P, M * K), std::vector<int64_t>(1, M * K))))
+            return st;
+    }
+    gx.sum_into = sum_in_gemm;
+    gx.sum_dst = sum_in_gemm ? dX : nullptr;
     if ((st = launch_gemm(gh, s0)) || (st = launch_gemm(gx, s0))) return st;
-    if (mode == 0) {
-        // The rank sum of dX, beside the weight-gradient GEMMs when a second stream is given.
+    if (mode == 0 && !sum_in_gemm) {
         cudaStream_t rs = s0;
         if (two_streams) {
             if (cudaEventRecord(ev->fwd, s0) != cudaSuccess || cudaStreamWaitEvent(s1, ev->fwd, 0) != cudaSuccess)
                 return fail(RTP_ECUDA, "%s: event ordering failed", fn);
             rs = s1;
         }
-        if ((st = reduce_partials(P, M, K, dX_partials, dX, rs, two_streams ? kOverlapBlocksPerSm : 4))) return st;
+        void* d[1] = {dX};
+        if ((st = launch_tasks(RTP_F32, dx_tasks, (const void* const*)dX_partials, d, rs, nullptr,
+                               two_streams ? kOverlapBlocksPerSm : 4)))
+            return st;
     }
     if ((st = launch_gemm(ga, s0)) || (st = launch_gemm(gb, s0))) return st;
-    if (two_streams) {
+    if (two_streams && !sum_in_gemm) {
         if (cudaEventRecord(ev->back, s1) != cudaSuccess || cudaStreamWaitEvent(s0, ev->back, 0) != cudaSuccess)
             return fail(RTP_ECUDA, "%s: event ordering failed", fn);
     }
     return RTP_OK;
+}
+
+int rtp_tp_mlp_backward(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X, const void* const* A_shards,
+                        const void* const* B_shards, const void* const* H, const void* const* Y, const void* dZ,
+                        void* const* dH, void* const* dX_partials, float* dX, float* const* dA, float* const* dB,
+                        int mode, rtp_stream s0_, rtp_stream s1_)
+{
+    return guarded("rtp_tp_mlp_backward", [&] {
+        return tp_mlp_backward_body(P, M, K, F, N, X, A_shards, B_shards, H, Y, dZ, dH, dX_partials, dX, dA, dB, mode,
+                                    s0_, s1_);
+    });
 }
 
 int rtp_tp_mlp_sp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* const* X_shards,
@@ -1129,10 +1386,10 @@ int rtp_tp_mlp_sp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void*
     for (int i = 0; i < P; ++i) {
         if ((st = make_map(&g1.ta[i], X_shards[i], Mr, K, 128))) return st;  // X rows by shard
         if ((st = make_map(&g1.tb[i], A_shards[i], K, Fp, BK))) return st;
-        g1.out[i] = Y[i];
+        if ((st = make_out_map(&g1.to[i], Y[i], M, Fp, Fp, false))) return st;
         if ((st = make_map(&g2.ta[i], Y[i], M, Fp, 128))) return st;
         if ((st = make_map(&g2.tb[i], B_shards[i], Fp, N, BK))) return st;
-        g2.out[i] = Z_shards[i];  // Z rows by shard
+        if ((st = make_out_map(&g2.to[i], Z_shards[i], Mr, N, N, true))) return st;  // Z rows by shard
     }
     // column-parallel GEMM with the all-gather of X fused into its loads
     g1.ldo = Fp;

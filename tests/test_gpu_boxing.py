@@ -14,7 +14,7 @@ import torch
 
 import oracle
 import synth
-from gpu_util import as_f64, assert_psum, to_dev, to_host
+from gpu_util import Guarded, as_f64, assert_psum, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -38,14 +38,21 @@ def _both(mesh, entries, ranks=()):
 
 
 def _gpu_shard(T, spec):
-    out = rtp.shard(to_dev(T), spec)
-    torch.cuda.synchronize()
+    """rtp.shard into guarded pieces (every write outside a piece is caught)."""
+    x = to_dev(T)
+    g = Guarded()
+    out = rtp.shard(x, spec, out=g.many([rtp.shard_shape(T.shape, spec, r) for r in range(spec.num_ranks)], x.dtype))
+    g.check("shard")
     return [to_host(p) for p in out]
 
 
 def _gpu_reshard(pieces, shape, s_src, s_dst):
-    out = rtp.reshard([to_dev(p) for p in pieces], shape, s_src, s_dst)
-    torch.cuda.synchronize()
+    """rtp.reshard into guarded pieces (every write outside a piece is caught)."""
+    ins = [to_dev(p) for p in pieces]
+    g = Guarded()
+    out = rtp.reshard(ins, shape, s_src, s_dst,
+                      out=g.many([rtp.shard_shape(shape, s_dst, r) for r in range(s_dst.num_ranks)], ins[0].dtype))
+    g.check("reshard")
     return [to_host(p) for p in out]
 
 
@@ -284,8 +291,10 @@ def test_sweep_full_size(sweep_inputs, dt, mesh, name, sdm, spart, ddm, dpart):
     else:
         pieces = [np.ascontiguousarray(_slice(T, shape, lsrc, r)[0]) for r in range(src.num_ranks)]
     dev_in = [to_dev(p) for p in pieces]
-    outs = rtp.reshard(dev_in, shape, src, dst)
-    torch.cuda.synchronize()
+    guard = Guarded()
+    outs = rtp.reshard(dev_in, shape, src, dst,
+                       out=guard.many([rtp.shard_shape(shape, dst, r) for r in range(dst.num_ranks)], dev_in[0].dtype))
+    guard.check(name)
     if spart != "all":
         for r, o in enumerate(outs):
             want, hv = _slice(T, shape, ldst, r)

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 import synth
-from gpu_util import as_f64, bf16_ulp, to_dev, to_host
+from gpu_util import Guarded, as_f64, bf16_ulp, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -43,10 +43,17 @@ def _inputs(M, K, F, N, P, seed=0, wstd=0.02):
 
 
 def _gpu(X, As, Bs, mode, chunks=1, col_blocks=1, second_stream=False):
+    """rtp.tp_mlp with Y, the partials and Z in guarded buffers (every write
+    outside them is caught)."""
     s1 = torch.cuda.Stream() if second_stream else None
-    Z, Y = rtp.tp_mlp(to_dev(X), [to_dev(a) for a in As], [to_dev(b) for b in Bs], mode=mode, chunks=chunks,
-                      col_blocks=col_blocks, s1=s1)
-    torch.cuda.synchronize()
+    P, (M, _), Fp, N = len(As), X.shape, As[0].shape[1], Bs[0].shape[1]
+    g = Guarded()
+    Y = g.many([(M, Fp)] * P, torch.bfloat16, "Y")
+    parts = g.many([(M, N)] * P, torch.float32, "partials") if mode == 0 else None
+    Z = g.empty((M, N), torch.float32, "Z")
+    rtp.tp_mlp(to_dev(X), [to_dev(a) for a in As], [to_dev(b) for b in Bs], Y=Y, partials=parts, Z=Z, mode=mode,
+               chunks=chunks, col_blocks=col_blocks, s1=s1)
+    g.check("tp_mlp mode %d, %d chunks x %d blocks" % (mode, chunks, col_blocks))
     return to_host(Z), [to_host(y) for y in Y]
 
 
@@ -136,6 +143,54 @@ def test_domino_configuration_full_size():
     _check(X, As, Bs, Z2, Ys2, rows, "domino 2 chunks, 2 column blocks")
     Z4, _ = _gpu(X, As, Bs, 0, chunks=4, col_blocks=1, second_stream=True)
     np.testing.assert_array_equal(Z4, Z2)
+
+
+@pytest.mark.parametrize("M,K,F,N,P", [(520, 264, 400, 144, 2), (1024, 512, 2048, 1024, 8), (4096, 8192, 28672, 8192, 8)])
+def test_domino_overlap_settings_give_identical_bits(M, K, F, N, P):
+    """Mode 0 sums the rank partials in kernels of their own after each Domino
+    window (overlap 0, the default), on the same or a second stream, or in the
+    row-parallel GEMM's epilogue (each output tile's ranks in turn on one
+    cluster).
+    Every way adds the same float32 partials in rank order, so Z is
+    bit-identical to the serial schedule (one chunk, one summing kernel after
+    the GEMMs), whose Z is checked against the oracle, and the partials are
+    the same everywhere."""
+    X, As, Bs = _inputs(M, K, F, N, P, seed=M + N + 7)
+    Xd, Ad, Bd = to_dev(X), [to_dev(a) for a in As], [to_dev(b) for b in Bs]
+    prev = rtp.tp_mlp_overlap(0)
+    try:
+        parts0 = [torch.empty((M, N), dtype=torch.float32, device="cuda") for _ in range(P)]
+        Zs, Ys = rtp.tp_mlp(Xd, Ad, Bd, partials=parts0, mode=0, chunks=1)
+        torch.cuda.synchronize()
+        want = to_host(Zs)
+        want_parts = [to_host(p) for p in parts0]
+        _check(X, As, Bs, want, [to_host(y) for y in Ys], _sample_rows(M, 8), "serial")
+        for setting in (1, 0):
+            rtp.tp_mlp_overlap(setting)
+            for chunks, cb in ((1, 1), (2, 1), (2, 2), (4, 1), (4, 2)):
+                for s1 in (None, torch.cuda.Stream()):
+                    g = Guarded()  # every write stays inside Z and the partials
+                    Z = g.empty((M, N), torch.float32, "Z")
+                    parts = g.many([(M, N)] * P, torch.float32, "partials")
+                    rtp.tp_mlp(Xd, Ad, Bd, Z=Z, partials=parts, mode=0, chunks=chunks, col_blocks=cb, s1=s1)
+                    what = "sum in epilogue %d, %d chunks x %d blocks" % (setting, chunks, cb)
+                    g.check(what)
+                    np.testing.assert_array_equal(to_host(Z), want, err_msg=what)
+                    for p, w in zip(parts, want_parts):
+                        np.testing.assert_array_equal(to_host(p), w, err_msg=what + " partials")
+    finally:
+        rtp.tp_mlp_overlap(prev)
+    assert rtp.device_error() == 0
+
+
+def test_domino_overlap_setting_errors():
+    with pytest.raises(rtp.RtpError) as e:
+        rtp.tp_mlp_overlap(2)
+    assert e.value.status == -1
+    with pytest.raises(rtp.RtpError):
+        rtp.tp_mlp_overlap(-1)
+    assert rtp.tp_mlp_overlap(1) == 0  # the default: kernels of their own
+    assert rtp.tp_mlp_overlap(0) == 1
 
 
 def test_domino_from_two_host_threads():
@@ -229,8 +284,11 @@ def test_sequence_parallel_matches_oracle_and_fused(M, K, F, N, P):
     X, As, Bs = _inputs(M, K, F, N, P, seed=M + 3 * K)
     Mr = M // P
     Xs = [np.ascontiguousarray(X[r * Mr:(r + 1) * Mr]) for r in range(P)]
-    Zs, Ys = rtp.tp_mlp_sp([to_dev(x) for x in Xs], [to_dev(a) for a in As], [to_dev(b) for b in Bs])
-    torch.cuda.synchronize()
+    g = Guarded()  # every write outside Y and the Z shards is caught
+    Zs, Ys = rtp.tp_mlp_sp([to_dev(x) for x in Xs], [to_dev(a) for a in As], [to_dev(b) for b in Bs],
+                           Y=g.many([(M, F // P)] * P, torch.bfloat16, "Y"),
+                           Z_shards=g.many([(Mr, N)] * P, torch.float32, "Z_shards"))
+    g.check("sequence parallel")
     Z = np.concatenate([to_host(z) for z in Zs], axis=0)
     _check(X, As, Bs, Z, [to_host(y) for y in Ys], np.arange(M), "sequence parallel")
     # the same accumulation as the fused MLP on the gathered X: identical bits

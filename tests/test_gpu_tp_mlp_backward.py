@@ -28,7 +28,7 @@ import torch
 
 import oracle
 import synth
-from gpu_util import as_f64, bf16_ulp, to_dev, to_host
+from gpu_util import Guarded, as_f64, bf16_ulp, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -61,12 +61,20 @@ def _inputs(M, K, F, N, P, seed=0, wstd=0.02):
 
 
 def _run(X, As, Bs, dZ, mode=1, second_stream=False):
-    """Training forward then backward on the GPU; everything back on the host."""
+    """Training forward then backward on the GPU, every output in a guarded
+    buffer (writes outside them are caught); everything back on the host."""
     Xd, Ad, Bd, dZd = to_dev(X), [to_dev(a) for a in As], [to_dev(b) for b in Bs], to_dev(dZ)
-    Z, Y, H = rtp.tp_mlp_train_forward(Xd, Ad, Bd)
+    P, (M, K), Fp, N = len(As), X.shape, As[0].shape[1], Bs[0].shape[1]
+    g = Guarded()
+    bf, f32 = torch.bfloat16, torch.float32
+    Z, Y, H = rtp.tp_mlp_train_forward(Xd, Ad, Bd, Y=g.many([(M, Fp)] * P, bf, "Y"), H=g.many([(M, Fp)] * P, bf, "H"),
+                                       Z=g.empty((M, N), f32, "Z"))
     s1 = torch.cuda.Stream() if second_stream else None
-    dX, dA, dB, dH = rtp.tp_mlp_backward(Xd, Ad, Bd, H, Y, dZd, mode=mode, s1=s1)
-    torch.cuda.synchronize()
+    dX, dA, dB, dH = rtp.tp_mlp_backward(
+        Xd, Ad, Bd, H, Y, dZd, dH=g.many([(M, Fp)] * P, bf, "dH"),
+        dX_partials=g.many([(M, K)] * P, f32, "dX_partials") if mode == 0 else None, dX=g.empty((M, K), f32, "dX"),
+        dA=g.many([(K, Fp)] * P, f32, "dA"), dB=g.many([(Fp, N)] * P, f32, "dB"), mode=mode, s1=s1)
+    g.check("training forward and backward, mode %d" % mode)
     h = lambda ts: [to_host(t) for t in ts]
     return {"Z": to_host(Z), "Y": h(Y), "H": h(H), "dX": to_host(dX), "dA": h(dA), "dB": h(dB), "dH": h(dH)}
 
@@ -188,6 +196,33 @@ def test_backward_configuration_full_size(cfg4):
             np.testing.assert_array_equal(a, b)
     g1b = _run(X, As, Bs, dZ, 1)
     np.testing.assert_array_equal(g1b["dX"], g1["dX"])
+
+
+@pytest.mark.parametrize("M,K,F,N,P", [(520, 264, 400, 144, 2), (1024, 512, 2048, 1024, 8)])
+def test_overlapped_dx_sum_settings_give_identical_bits(M, K, F, N, P):
+    """Mode 0 sums the dX partials in a kernel of its own beside the
+    weight-gradient GEMMs on the same or a second stream (overlap 0, the
+    default), or in the dX GEMM's epilogue (each output tile's ranks in turn
+    on one cluster). The same
+    float32 partials are added in rank order, so every way gives the same
+    bits, and the weight gradients do not depend on it."""
+    X, As, Bs, dZ = _inputs(M, K, F, N, P, seed=M + 11)
+    rows, cols = _rows(M, 8, 3), _cols(F, 8, 4)
+    base = None
+    prev = rtp.tp_mlp_overlap(0)
+    try:
+        for setting in (0, 1):
+            rtp.tp_mlp_overlap(setting)
+            for second in (False, True):
+                g = _run(X, As, Bs, dZ, 0, second_stream=second)
+                if base is None:
+                    _check(X, As, Bs, dZ, g, rows, cols, "separate dX sum")
+                    base = g
+                for k in ("dX", "dA", "dB", "dH"):
+                    got, want = (g[k], base[k]) if k == "dX" else (np.stack(g[k]), np.stack(base[k]))
+                    np.testing.assert_array_equal(got, want, err_msg="%s, sum in epilogue %d" % (k, setting))
+    finally:
+        rtp.tp_mlp_overlap(prev)
 
 
 def test_argument_errors():
