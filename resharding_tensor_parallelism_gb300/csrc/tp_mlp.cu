@@ -17,7 +17,12 @@
 //              CTA's TMEM; 2 accumulators of 256 columns let the epilogue of one
 //              tile overlap the next tile's K loop;
 //   warps 2-5  epilogue, in each CTA: tcgen05.ld of its accumulator rows, GELU
-//              and bf16 rounding (GEMM1) or float32 (GEMM2), streaming stores.
+//              and bf16 rounding (GEMM1) or float32 (GEMM2), staged 32 x 32 at
+//              a time in swizzled shared memory and written by TMA tensor
+//              stores clipped to the launch's output window.
+// Consecutive GEMM launches overlap their set-up with the previous kernel's end
+// (programmatic dependent launch); a kernel waits for its predecessor before
+// touching global memory.
 // Per SM the pair tile halves the operand bytes fetched from L2 and staged in
 // shared memory per FLOP compared with a 128x256 single-SM tile. Tiles are
 // walked in groups of 16 M-tiles so that the pairs running at one time share
@@ -25,9 +30,12 @@
 //
 // The row-parallel GEMM has two forms. Separate: each rank's Y_i B_i is a
 // float32 partial, and a multi-source kernel sums the partials (the
-// all-reduce of the pages). Fused: the K loop of one output tile walks every
-// rank's K range in turn, so the sum of ranks happens in the TMEM accumulator
-// and no partial is ever written.
+// all-reduce of the pages), or, optionally, the epilogue that writes a
+// partial tile also adds it to Z in rank order (one cluster takes every
+// rank's tile of an output tile in turn; the same bits as the separate sum).
+// Fused: the K loop of one output tile walks every rank's K range in turn, so
+// the sum of ranks happens in the TMEM accumulator and no partial is ever
+// written.
 //
 // Sequence parallelism (ColossalAI page, section 5.3: the column layer
 // all-gathers its sequence-split input, the row layer reduce-scatters its
