@@ -352,7 +352,12 @@ int rtp_infer_broadcast(int n_in, const int32_t* in_ndims, const int64_t* const*
  * partials, Z) may then be NULL.
  * Errors leave nothing launched. The kernels allocate nothing; the first call
  * on a device sets the GEMM kernel's shared-memory limit and, per host thread,
- * creates two events used to order s0 and s1.
+ * creates two events used to order s0 and s1. The GEMM kernels are launched
+ * as programmatic dependents of the previous kernel in their stream: they may
+ * start their set-up early but wait for that kernel to complete before they
+ * touch global memory, so stream order is kept; a caller's own kernel launched
+ * the same way after them must wait likewise (griddepcontrol.wait) before
+ * reading their outputs.
  */
 int rtp_tp_mlp(int P, int64_t M, int64_t K, int64_t F, int64_t N, const void* X, const void* const* A_shards,
                const void* const* B_shards, void* const* Y, void* const* partials, float* Z, int mode, int chunks,
