@@ -675,7 +675,7 @@ __global__ void __launch_bounds__(kBlock, 4) boxing_kernel(const __grid_constant
 // Launches whose every task is a TMA-tile copy to one destination: thread 0
 // of a block moves a chunk (one bulk or tile load, then one tile or bulk
 // store) and the other threads only wait, so the block is small and has no
-// row tables: up to 7 blocks (7 chunks in flight) fit on an SM where 4 of
+// row tables: 6 blocks (6 chunks in flight) fit on an SM where 4 of
 // boxing_kernel's do. Measured on the bf16 S(2) -> S(1) move of the
 // [8,2048,4096] sweep on a 1x8 mesh (4D tiles): 6.30 -> 6.61 TB/s.
 constexpr int kTileBlock = 128;
