@@ -484,3 +484,27 @@ def test_noalloc_size_check_cannot_wrap():
                        (8, 4096, 512)]:
         rc = lib.rtp_tp_mlp_noalloc(P, M, 64, P * Fp, 64, 4096, fake, fake, 8192, None)
         assert rc == -2 and "static scratch" in rtp.last_error(), (P, M, Fp, rc, rtp.last_error())
+
+
+def test_bounds_check_accepts_every_correct_plan():
+    """The host-side bounds check runs on every new plan: over random shapes
+    (ragged, some empty pieces), meshes and layouts of every kind, it passes
+    each correct plan (no call is refused) and the planned bytes still equal
+    the oracle's piece sizes."""
+    rng = np.random.default_rng(21)
+    meshes = [(1,), (2,), (3,), (4,), (2, 2), (2, 3), (3, 2), (2, 2, 2), (1, 4), (8,)]
+    for case in range(400):
+        ndim = int(rng.integers(1, 5))
+        shape = tuple(int(x) for x in rng.integers(1, 12, size=ndim))
+        m1, m2 = meshes[rng.integers(len(meshes))], meshes[rng.integers(len(meshes))]
+        red = ("P", "Pmin", "Pmax")[case % 3]
+        opts = [("S", a) for a in range(ndim)] + ["B", red]
+        e1 = tuple(opts[i] for i in rng.integers(len(opts), size=len(m1)))
+        e2 = tuple(opts[i] for i in rng.integers(len(opts), size=len(m2)))
+        r1 = tuple(int(x) for x in rng.permutation(int(np.prod(m1))))
+        r2 = tuple(int(x) for x in rng.permutation(int(np.prod(m2))))
+        src, dst = rtp.spec_nd_sbp(m1, e1, r1), rtp.spec_nd_sbp(m2, e2, r2)
+        rd, wr, nt, nl = rtp.reshard_cost(rtp.F32, shape, src, dst)
+        ldst = oracle.Layout(m2, e2, r2)
+        written = sum(int(np.prod(oracle.shard_shape(shape, ldst, r))) for r in range(len(r2)))
+        assert wr == 4 * written, (case, shape, m1, e1, m2, e2)
