@@ -486,11 +486,15 @@ def run_ours(args, rank, world, local_rank):
         result["e2e"] = e2e_sweep(rtp, torch, dev, sweep)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(max_seconds=args.cpu_seconds, with_mlp=True)
+    # The MLP is timed inside a long step (seconds of back-to-back work at the
+    # power cap), so its roofline is the sustained bf16 figure; the burst
+    # figure's fraction is given beside it.
     result["tp_mlp"] = {"value": round(tflops, 1), "unit": "TFLOP/s", "mode": "fused reduction",
                         "shape": "8192x4096x16384x4096 P=8", "ms_per_call": round(mlp_ms / args.steps, 4),
                         "roofline": {"bound": "tensor", "kernel": "tp_gemm_kernel", "achieved": round(tflops / world, 1),
-                                     "peak": bf16_peak, "unit": "TFLOP/s", "frac": tp_frac,
-                                     "frac_of_sustained": round(tflops / world / bf16_sust, 4),
+                                     "peak": bf16_sust, "peak_kind": "sustained (timed inside a long step)",
+                                     "unit": "TFLOP/s", "frac": round(tflops / world / bf16_sust, 4),
+                                     "frac_of_burst": tp_frac, "burst_peak": bf16_peak,
                                      "peak_source": peak_src, "traffic": _traffic("tp_gemm_kernel", "mlp")},
                         "backward_tflops": rows["f1_tp_mlp_backward"]["tflops"],
                         "backward_frac": rows["f1_tp_mlp_backward"]["frac_bf16"]}
