@@ -484,6 +484,7 @@ def run_ours(args, rank, world, local_rank):
     }
     if rank == 0 and not args.no_e2e:
         result["e2e"] = e2e_sweep(rtp, torch, dev, sweep)
+    lib_cmp = library_gemm_same_run(torch, mlp, run_mlp, flush) if rank == 0 else None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(max_seconds=args.cpu_seconds, with_mlp=True)
     # The MLP is timed inside a long step (seconds of back-to-back work at the
@@ -498,6 +499,8 @@ def run_ours(args, rank, world, local_rank):
                                      "peak_source": peak_src, "traffic": _traffic("tp_gemm_kernel", "mlp")},
                         "backward_tflops": rows["f1_tp_mlp_backward"]["tflops"],
                         "backward_frac": rows["f1_tp_mlp_backward"]["frac_bf16"]}
+    if lib_cmp is not None:
+        result["tp_mlp"]["beside_library_gemm"] = lib_cmp
     result["domino"] = {"shape": "4096x8192x28672x8192 P=8", "ms_serial": round(ser_ms, 4),
                         "ms_reduce_alone": round(red_ms, 4), "ms_fused": round(dfu_ms, 4), **dom_rows,
                         "tflops_2_chunks": round(DOMINO_FLOPS / (avg("domino") * 1e-3) / 1e12, 1)}
@@ -506,6 +509,49 @@ def run_ours(args, rank, world, local_rank):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def library_gemm_same_run(torch, mlp, run_mlp, flush, reps: int = 7):
+    """The fused TP-MLP beside the library GEMM (torch.mm, i.e. cuBLAS) on the
+    same problem, in the same process and at the same clocks: Y = X [A_0..A_7]
+    and Z = Y [B_0; ..; B_7] as two plain bf16 GEMMs (8192x16384x4096 and
+    8192x4096x16384), alternated with the library's own call, L2 flushed
+    before each. For comparison only: the library GEMMs compute no GELU and
+    write Z in bf16 (ours float32), so they do slightly less work. Medians."""
+    X, A, B = mlp["X"], mlp["A"], mlp["B"]
+    a_cat = torch.cat(A, dim=1)
+    b_cat = torch.cat(B, dim=0)
+    y_cat = torch.empty((X.shape[0], a_cat.shape[1]), dtype=torch.bfloat16, device=X.device)
+    z_lib = torch.empty((X.shape[0], b_cat.shape[1]), dtype=torch.bfloat16, device=X.device)
+
+    def lib():
+        torch.mm(X, a_cat, out=y_cat)
+        torch.mm(y_cat, b_cat, out=z_lib)
+
+    def one(fn):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        return e0, e1
+
+    for _ in range(3):
+        one(lib)
+        one(run_mlp)
+    ours, theirs = [], []
+    for _ in range(reps):
+        theirs.append(one(lib))
+        ours.append(one(run_mlp))
+    torch.cuda.synchronize()
+    med = lambda ev: statistics.median(a.elapsed_time(b) for a, b in ev)
+    ms_ours, ms_lib = med(ours), med(theirs)
+    del a_cat, b_cat, y_cat, z_lib
+    return {"ms": round(ms_ours, 4), "tflops": round(MLP_FLOPS / (ms_ours * 1e-3) / 1e12, 1),
+            "library_ms": round(ms_lib, 4), "library_tflops": round(MLP_FLOPS / (ms_lib * 1e-3) / 1e12, 1),
+            "speedup_over_library": round(ms_lib / ms_ours, 4),
+            "library": "torch.mm (cuBLAS) bf16: X[A_i] then Y[B_i], bf16 outputs, no GELU; alternated with ours, "
+                       "L2 flushed before each, median of %d" % reps}
 
 
 def psum_errors(rtp, torch, sweep):
@@ -787,9 +833,11 @@ def e2e_sweep(rtp, torch, dev, sweep):
             "frac_of_link_ceiling": round(dt_link / dt, 4),
             "link_h2d_gbs": round(h2d / t_up / 1e9, 1), "link_d2h_gbs": round(d2h / t_down / 1e9, 1),
             "link_both_at_once_gbs": round((h2d + d2h) / t_both / 1e9, 1),
+            "frac_of_both_at_once": round(t_both / dt, 4),
             "workload": "the six bf16 transitions on the 1x8 mesh, host pinned buffers in and out, pipelined on "
                         "three streams; link_ceiling_gbs: the same copies with both directions fully overlapped "
-                        "(the slower direction's copies alone)"}
+                        "(the slower direction's copies alone); frac_of_both_at_once: the same copies, both "
+                        "directions started together, no reshard, against the e2e step"}
 
 
 # ---- CPU oracle (baseline and reference arm) ---------------------------------------------
