@@ -484,7 +484,7 @@ def run_ours(args, rank, world, local_rank):
     }
     if rank == 0 and not args.no_e2e:
         result["e2e"] = e2e_sweep(rtp, torch, dev, sweep)
-    lib_cmp = library_gemm_same_run(torch, mlp, run_mlp, flush) if rank == 0 else None
+    lib_cmp = library_gemm_same_run(torch, mlp, run_mlp, flush) if rank == 0 and not args.no_library_gemm else None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(max_seconds=args.cpu_seconds, with_mlp=True)
     # The MLP is timed inside a long step (seconds of back-to-back work at the
@@ -1067,6 +1067,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-library-gemm", action="store_true",
+                    help="skip timing the fused MLP beside the library (cuBLAS) GEMMs after the timed region")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
