@@ -661,6 +661,11 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
         const int c_begin = ((warp - 2) >> 2) * EPI_CHUNKS;
         int acc = 0;
         uint32_t acc_phase = 0;
+        // TMA stores this warp has issued (warp-uniform). The two staging
+        // buffers alternate by store, not by chunk: a tile cut by the window's
+        // column edge stores fewer chunks, and by chunk parity the next tile's
+        // first chunk could reuse the buffer of the store issued just before.
+        uint32_t stores = 0;
         for (int k = 0, tile; (tile = nth_tile(a, pair, npairs, k)) >= 0; ++k) {
             int g, mt, nt;
             tile_coords(a, tile, g, mt, nt);
@@ -703,8 +708,8 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
             auto emit = [&](int c, const uint32_t (&r)[32], const uint4 (&h)[4]) {
                 const int64_t c0 = col + 32 * c;
                 if (c0 >= a.n_end || row0 >= a.m_end) return;  // warp-uniform: nothing of the window here
-                const uint32_t buf = stage_epi + (uint32_t)(c & 1) * EPI_STAGE_BYTES;
-                if (lane == 0) bulk_wait_read_1();  // the store two chunks back has read this buffer
+                const uint32_t buf = stage_epi + (stores & 1u) * EPI_STAGE_BYTES;
+                if (lane == 0) bulk_wait_read_1();  // the store two stores back has read this buffer
                 __syncwarp();
                 if constexpr (EPI == EPI_F32) {
                     const uint32_t rb = buf + (uint32_t)lane * 128u;
@@ -750,6 +755,7 @@ __global__ void __launch_bounds__(THREADS, 1) tp_gemm_kernel(const __grid_consta
                     if (EPI == EPI_GELU_BF16 && a.store_h) tma_store_2d(&a.to2[om], buf + 2048u, (int)c0, (int)orow0);
                     bulk_commit();
                 }
+                ++stores;
                 if constexpr (EPI == EPI_F32) {
                     if (a.sum_into) {
                         // sum_dst[rows, c0 + lane] += the staged chunk's column `lane`, rank g after
