@@ -986,6 +986,7 @@ PROFILE_CASES = {
     "mlp_fused": ("mlp", MLP),
     "domino_fused": ("mlp", DOMINO),
     "mlp_backward": ("mlp_backward", MLP),
+    "mlp_beside_library": ("mlp_library", MLP),
 }
 
 
@@ -1050,6 +1051,21 @@ def run_profile_case(name: str, repeats: int = 2):
             torch.cuda.synchronize()
             print(json.dumps({"case": name, "flops_per_gemm": [2 * M * K * F, 2 * M * F * N, 2 * M * N * F,
                                                                2 * M * F * K, 2 * K * M * F, 2 * F * M * N]}))
+        elif kind == "mlp_library":
+            # the fused MLP (2 launches), then the library GEMMs of the same
+            # shapes (torch.mm: X [A_i] and Y [B_i], bf16 outputs, no GELU),
+            # once each, inside the NVTX range "gemms"
+            a_cat, b_cat = torch.cat(A, dim=1), torch.cat(B, dim=0)
+            y_cat = torch.empty((M, F), dtype=torch.bfloat16, device="cuda")
+            z_lib = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            torch.cuda.synchronize()
+            torch.cuda.nvtx.range_push("gemms")
+            rtp.tp_mlp(X, A, B, Y=Y, Z=Z, mode=1)
+            torch.mm(X, a_cat, out=y_cat)
+            torch.mm(y_cat, b_cat, out=z_lib)
+            torch.cuda.nvtx.range_pop()
+            torch.cuda.synchronize()
+            print(json.dumps({"case": name, "flops_per_gemm": 2 * M * K * F}))
         else:
             for _ in range(repeats):
                 rtp.tp_mlp(X, A, B, Y=Y, Z=Z, mode=1)
