@@ -214,8 +214,11 @@ def run_ours(args, rank, world, local_rank):
         return (torch.randn(shape, generator=gen, device=dev, dtype=torch.float32) * std).to(dtype)
 
     # ---- sweep inputs: pieces resident in HBM ----
-    flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    # the flush buffers are at least 4x the L2 size the device reports
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0))
+    flush_bytes = max(L2_FLUSH_BYTES, 4 * l2_bytes) // 4096 * 4096
+    flush_w = torch.empty(flush_bytes // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.ones(flush_bytes // 4, dtype=torch.float32, device=dev)
 
     class _Flush:
         """L2 flush before a timed call: write a buffer larger than L2, then read
@@ -471,7 +474,7 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "f32+bf16",
         "data": "synthetic (seeded Philox normals on the device)",
-        "config": dict(CONFIG),
+        "config": dict(CONFIG, l2_cache_bytes=l2_bytes, l2_flush_bytes=flush_bytes),
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
         "rows": rows,
