@@ -36,6 +36,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "reshard GB/s (% of HBM peak); TP-MLP TFLOP/s (% of bf16 peak), 1 GB300"
 SWEEP_SHAPE = (8, 2048, 4096)
+UNEVEN_SHAPE = (12289, 6143)
 MLP = dict(M=8192, K=4096, F=16384, N=4096, P=8)
 DOMINO = dict(M=4096, K=8192, F=28672, N=8192, P=8)
 # The workload both arms report (the reference arm times a bounded sample of it).
@@ -248,6 +249,17 @@ def run_ours(args, rank, world, local_rank):
                 if not partial:
                     srd, swr, _, snl = rtp.reshard_cost(code, SWEEP_SHAPE, whole, src)
                     shards.append((label, T, src, ins, srd + swr, snl))
+    # the uneven configuration: [12289, 6143] float32 U[-1,1) on a 2x2 mesh,
+    # (S0,S1) -> (S1,S0) and (S0,S1) -> (B,S1)
+    u_src = rtp.spec_nd_sbp((2, 2), (("S", 0), ("S", 1)))
+    u_pieces = rtp.shard(torch.rand(UNEVEN_SHAPE, generator=gen, device=dev) * 2 - 1, u_src)
+    uneven = []  # (label, src pieces, dst spec, dst pieces, bytes, launches)
+    for name, ents in (("(S0,S1)->(S1,S0)", (("S", 1), ("S", 0))), ("(S0,S1)->(B,S1)", ("B", ("S", 1)))):
+        dst = rtp.spec_nd_sbp((2, 2), ents)
+        outs = [torch.empty(rtp.shard_shape(UNEVEN_SHAPE, dst, r), dtype=torch.float32, device=dev)
+                for r in range(dst.num_ranks)]
+        rd, wr, nt, nl = rtp.reshard_cost(rtp.F32, UNEVEN_SHAPE, u_src, dst)
+        uneven.append((name, u_pieces, dst, outs, rd + wr, nl))
     torch.cuda.synchronize()
 
     # ---- MLP inputs ----
@@ -333,6 +345,8 @@ def run_ours(args, rank, world, local_rank):
            for (label, c, i, s, o, d, nbytes, nl) in sweep]
     shard_ops = [(label, (lambda T=T, sp=sp, o=o: rtp.shard(T, sp, out=o)), nbytes, nl)
                  for (label, T, sp, o, nbytes, nl) in shards]
+    uneven_ops = [(label, (lambda i=i, d=d, o=o: rtp.reshard(i, UNEVEN_SHAPE, u_src, d, out=o)), nbytes, nl)
+                  for (label, i, d, o, nbytes, nl) in uneven]
     # (kind, function, launches of the library's kernels per call)
     mlp_ops = [("mlp", run_mlp, 2), ("sp", run_sp, 2),
                # the pages' schedule: every window's sum a launch of its own on the second stream
@@ -344,7 +358,8 @@ def run_ours(args, rank, world, local_rank):
                ("serial", run_serial, 3), ("dom_fused", run_dom_fused, 2), ("reduce", run_reduce, 1),
                ("train_fwd", run_train_fwd, 2), ("bwd", run_bwd, 4),
                ("bwd_overlap", bwd_overlap(False), 5), ("bwd_overlap_esum", bwd_overlap(True), 4)]
-    launches_per_step = sum(x[3] for x in ops) + sum(x[3] for x in shard_ops) + sum(x[2] for x in mlp_ops)
+    launches_per_step = (sum(x[3] for x in ops) + sum(x[3] for x in shard_ops) + sum(x[3] for x in uneven_ops) +
+                         sum(x[2] for x in mlp_ops))
     E = lambda: torch.cuda.Event(enable_timing=True)
 
     def step(record):
@@ -362,6 +377,13 @@ def run_ours(args, rank, world, local_rank):
             fn()
             e1.record()
             record.append(("reshard", label, e0, e1, nbytes))
+        for label, fn, nbytes, nl in uneven_ops:
+            flush.zero_()
+            e0, e1 = E(), E()
+            e0.record()
+            fn()
+            e1.record()
+            record.append(("uneven", label, e0, e1, nbytes))
         for kind, fn, _ in mlp_ops:
             flush.zero_()
             e0, e1 = E(), E()
@@ -428,6 +450,10 @@ def run_ours(args, rank, world, local_rank):
                            "frac_hbm": round(gbs_of("reshard", lambda l: "P8" not in l) / hbm_peak, 4)},
         "a3_reshard_P": {"gbs": round(gbs_of("reshard", lambda l: "P8" in l), 1),
                          "frac_hbm": round(gbs_of("reshard", lambda l: "P8" in l) / hbm_peak, 4)},
+        "a2_uneven_2x2": {"gbs": round(gbs_of("uneven"), 1), "frac_hbm": round(gbs_of("uneven") / hbm_peak, 4),
+                          "per_call_gbs": {label: round(v[2] * v[1] / (v[0] * 1e-3) / 1e9, 1)
+                                           for (k, label), v in per.items() if k == "uneven"},
+                          "shape": "[12289,6143] float32 on 2x2 from (S0,S1)"},
         "a4_infer_spmd": {"us_per_call": host["infer_spmd_us"], "where": "host"},
         "a4p_reshape_rule": {"us_per_call": host["infer_reshape_us"], "where": "host"},
         "a7_reduce_separate": {"ms": round(red_ms, 4), "gbs": round(red_bytes / (red_ms * 1e-3) / 1e9, 1),

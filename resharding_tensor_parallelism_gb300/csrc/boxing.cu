@@ -356,6 +356,41 @@ __device__ __forceinline__ void copy_chunk(const void* const* ptrs, const KTask&
     }
 }
 
+// One source, float32, narrow vectors (8 or 4 bytes: a row or pointer not
+// 16-byte aligned) and long rows: the block walks the chunk row by row, each thread
+// moving UR vectors of a row (strided by the block size) per pass, loads
+// first, so that 8 vectors a thread are in flight with no per-item row table
+// (copy_chunk's (row, vector) items keep 4 a thread); the row's last partial
+// pass goes one vector at a time.
+template <int VB, int ES>
+__device__ __forceinline__ void copy_rows(const void* const* ptrs, const KTask& t, int nr, int nv, const int64_t* s_off,
+                                          const int64_t* d_off)
+{
+    constexpr int UR = 8;
+    using V = typename Raw<VB>::T;
+    const char* sb = static_cast<const char*>(ptrs[t.ptr0]);
+    const void* const* dp = ptrs + t.ptr0 + 1;
+    for (int q = 0; q < nr; ++q) {
+        const V* src = reinterpret_cast<const V*>(sb + s_off[q] * ES);
+        int v0 = threadIdx.x;
+        for (; v0 + (UR - 1) * kBlock < nv; v0 += kBlock * UR) {
+            V x[UR];
+#pragma unroll
+            for (int u = 0; u < UR; ++u) x[u] = __ldcs(src + v0 + u * kBlock);
+            for (int j = 0; j < t.n_dst; ++j) {
+                V* dst = reinterpret_cast<V*>(static_cast<char*>(const_cast<void*>(dp[j])) + d_off[q] * ES) + v0;
+#pragma unroll
+                for (int u = 0; u < UR; ++u) __stcs(dst + u * kBlock, x[u]);
+            }
+        }
+        for (; v0 < nv; v0 += kBlock) {
+            const V x = __ldcs(src + v0);
+            for (int j = 0; j < t.n_dst; ++j)
+                __stcs(reinterpret_cast<V*>(static_cast<char*>(const_cast<void*>(dp[j])) + d_off[q] * ES) + v0, x);
+        }
+    }
+}
+
 template <int OP>
 __device__ __forceinline__ float combine(float acc, float x)
 {
@@ -425,6 +460,8 @@ __device__ __forceinline__ void run_chunk(const void* const* ptrs, const KTask& 
     const int total = nr * nv;
     if (t.n_src == 0) {
         fill_chunk<VB, ES>(ptrs, t, total, nv, s_off, d_off);
+    } else if (ES == 4 && VB < 16 && (!SUM || t.n_src == 1) && nv >= 4 * kBlock) {
+        if constexpr (ES == 4 && VB < 16) copy_rows<VB, ES>(ptrs, t, nr, nv, s_off, d_off);
     } else if (!SUM || t.n_src == 1) {
         copy_chunk<VB, ES>(ptrs, t, total, nv, s_off, d_off);
     } else if constexpr (SUM) {

@@ -1,6 +1,8 @@
 """GPU parity of each form of the resharding kernel on ragged cases.
 
-The kernel runs a task in registers, staged through shared memory by bulk
+The kernel runs a task in registers (float32 rows of 1024 vectors or more
+that only allow 8- or 4-byte vectors go row by row, the rest as (row, vector)
+items spread over the block), staged through shared memory by bulk
 copies, or with TMA tiles of a 3D / 4D tensor map (rtp.reshard_forms tells
 which). Each case below is chosen so that one form carries it, with a ragged
 last chunk (or segment), in float32 and bf16, for copies and for sum, min and
@@ -34,6 +36,8 @@ def lib():
 
 # (name, shape, mesh, src entries, dst entries, form that carries every task)
 CASES = [
+    ("registers, long rows of 4- and 8-byte vectors", (40, 8195), (2,), (("S", 1),), (("S", 0),), REG),
+    ("registers, long rows, to a split of columns", (40, 8195), (2,), (("S", 0),), (("S", 1),), REG),
     ("bulk copy, ragged rows", (10, 2048), (4,), ("B",), (("S", 0),), BULK),
     ("bulk sum, ragged segment", (5, 3000), (4,), ("P",), ("B",), BULK),
     ("bulk min", (7, 5000), (4,), ("Pmin",), ("B",), BULK),
