@@ -1016,6 +1016,7 @@ PROFILE_CASES = {
     "domino_fused": ("mlp", DOMINO),
     "mlp_backward": ("mlp_backward", MLP),
     "mlp_beside_library": ("mlp_library", MLP),
+    "uneven": ("uneven", None),
 }
 
 
@@ -1047,6 +1048,21 @@ def run_profile_case(name: str, repeats: int = 2):
                                   "algorithmic_bytes": rd + wr, "launches": nl})
                     del ins, outs
                     torch.cuda.empty_cache()
+        print(json.dumps({"case": name, "calls": order}))
+    elif kind == "uneven":
+        # [12289, 6143] float32 on 2x2: (S0,S1) -> (S1,S0), then (S0,S1) -> (B,S1), one launch each
+        src = rtp.spec_nd_sbp((2, 2), (("S", 0), ("S", 1)))
+        ins = rtp.shard(torch.rand(UNEVEN_SHAPE, generator=gen, device="cuda") * 2 - 1, src)
+        order = []
+        for tname, ents in (("(S0,S1)->(S1,S0)", (("S", 1), ("S", 0))), ("(S0,S1)->(B,S1)", ("B", ("S", 1)))):
+            dst = rtp.spec_nd_sbp((2, 2), ents)
+            outs = [torch.empty(rtp.shard_shape(UNEVEN_SHAPE, dst, r), device="cuda") for r in range(dst.num_ranks)]
+            rd, wr, nt, nl = rtp.reshard_cost(rtp.F32, UNEVEN_SHAPE, src, dst)
+            torch.cuda.synchronize()
+            rtp.reshard(ins, UNEVEN_SHAPE, src, dst, out=outs)
+            torch.cuda.synchronize()
+            order.append({"call": tname, "algorithmic_bytes": rd + wr, "launches": nl,
+                          "forms": list(rtp.reshard_forms(rtp.F32, UNEVEN_SHAPE, src, dst))})
         print(json.dumps({"case": name, "calls": order}))
     elif kind == "reshard":
         mesh_name, idx, dt = det
