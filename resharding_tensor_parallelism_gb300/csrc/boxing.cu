@@ -360,11 +360,12 @@ __device__ __forceinline__ void copy_chunk(const void* const* ptrs, const KTask&
 // 16-byte aligned) and long rows: the block walks the chunk row by row, each thread
 // moving UR vectors of a row (strided by the block size) per pass, loads
 // first, so that 8 vectors a thread are in flight with no per-item row table
-// (copy_chunk's (row, vector) items keep 4 a thread); the row's last partial
-// pass goes one vector at a time.
+// (copy_chunk's (row, vector) items keep 4 a thread); the row's end goes in
+// one pass of 4, then one vector at a time. Not inlined: its registers stay
+// out of the allocation of the kernel's other paths.
 template <int VB, int ES>
-__device__ __forceinline__ void copy_rows(const void* const* ptrs, const KTask& t, int nr, int nv, const int64_t* s_off,
-                                          const int64_t* d_off)
+__device__ __noinline__ void copy_rows(const void* const* ptrs, const KTask& t, int nr, int nv, const int64_t* s_off,
+                                       const int64_t* d_off)
 {
     constexpr int UR = 8;
     using V = typename Raw<VB>::T;
@@ -382,6 +383,17 @@ __device__ __forceinline__ void copy_rows(const void* const* ptrs, const KTask& 
 #pragma unroll
                 for (int u = 0; u < UR; ++u) __stcs(dst + u * kBlock, x[u]);
             }
+        }
+        if (v0 + 3 * kBlock < nv) {  // a pass of 4
+            V x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) x[u] = __ldcs(src + v0 + u * kBlock);
+            for (int j = 0; j < t.n_dst; ++j) {
+                V* dst = reinterpret_cast<V*>(static_cast<char*>(const_cast<void*>(dp[j])) + d_off[q] * ES) + v0;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) __stcs(dst + u * kBlock, x[u]);
+            }
+            v0 += 4 * kBlock;
         }
         for (; v0 < nv; v0 += kBlock) {
             const V x = __ldcs(src + v0);
