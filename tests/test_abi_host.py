@@ -290,6 +290,19 @@ def test_forms_cover_the_sweep():
     assert rtp.reshard_forms(rtp.F32, (64, 36), s, d)[0] > 0
 
 
+def test_form_test_cases_take_their_form():
+    """Each case of the GPU form tests is carried by the form it names, on the
+    host planner alone (no GPU): registers, including the float32 rows that
+    go row by row, bulk staging, 3D and 4D TMA tiles."""
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+    import test_gpu_boxing_forms as tf
+    for name, shape, mesh, src, dst, form in tf.CASES:
+        for code in (rtp.F32, rtp.BF16):
+            c = rtp.reshard_forms(code, shape, rtp.spec_nd_sbp(mesh, src), rtp.spec_nd_sbp(mesh, dst))
+            assert c[form] > 0 and sum(c) == c[form], (name, code, c)
+
+
 def test_binding_checks_buffers_before_any_launch():
     """The library sees raw pointers only, so the binding checks every buffer's
     count, shape, dtype and device against what the call will touch; a wrong
