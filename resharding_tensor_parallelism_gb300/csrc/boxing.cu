@@ -902,8 +902,12 @@ int64_t fill_task(KTask& k, const PlanTask& t, int vec, int es, bool allow_bulk)
     }
     // Register path: a copy to several destinations writes each chunk several
     // times, so its chunks shrink to keep the bytes a block moves near 2 x 32 KB
-    // (4 KB at least).
+    // (4 KB at least). A float32 copy of 8- or 4-byte vectors takes 64 KB
+    // chunks whatever its destinations: long rows go row by row there, and
+    // more rows a chunk spread the chunk's set-up over more bytes (measured:
+    // 12 KB rows to two destinations 5.15 -> 5.79 TB/s).
     const int64_t chunk_bytes = k.bulk ? bulk_chunk_bytes
+                                : (ns == 1 && es == 4 && vec < 16) ? 2 * kChunkBytes
                                 : ns <= 1 ? std::max<int64_t>(4096, 2 * kChunkBytes / (int64_t)(1 + t.dst.size()))
                                           : kChunkBytes;
     if (row_bytes >= chunk_bytes) {
